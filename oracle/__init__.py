@@ -1,0 +1,124 @@
+"""CPU oracle for dense GEMV — test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package. It wraps ``gemv_oracle.c`` (plain C, fp64 accumulation
+over the exactly decoded stored values, k ascending) through ctypes and shares no
+code with the CUDA library.
+
+The definition it follows: y[b][m] = s_m * sum_k A[m][k] * x[b][k] + bias[m]
+("16-sgemv" notes, problem definition; "GEMV and row-level parallelism" lesson,
+section 1; int8 weights with per-row scale from the NPU MatMul post, section 1.2).
+
+Pins (checked by ``tests/test_oracle.py`` against values fixed by the pages and by
+mathematics, not by this code): exact-rational brute force on tiny inputs, the
+identity and permutation matrices, one-hot x, linearity, bias == NULL, the all-ones
+closed form, rank-1 matrices, exact integer results for int8 weights with unit
+scale, and the fp16/bf16 decoders against independent decoders over all 65,536
+bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemv_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_gemv.so")
+
+KIND = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3}
+
+
+def build(force: bool = False) -> str:
+    """Compile gemv_oracle.c into liboracle_gemv.so next to it (gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-std=c11", _SRC, "-o", tmp]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:] + ["-lm"], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + ["-lm"], check=True, capture_output=True, text=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        L.oracle_gemv.argtypes = [ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, vp, vp, ctypes.c_int]
+        L.oracle_gemv.restype = ctypes.c_int
+        L.oracle_decode.argtypes = [ctypes.c_int, vp, i64, vp]
+        L.oracle_decode.restype = ctypes.c_int
+        L.oracle_max_threads.argtypes = []
+        L.oracle_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _storage(a, dtype_code):
+    """Contiguous numpy array with the storage layout the C code expects."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    want = {0: np.float32, 1: np.uint16, 2: np.uint16, 3: np.int8}[dtype_code]
+    if a.dtype == np.float16 and want == np.uint16:
+        a = a.view(np.uint16)
+    if a.dtype != want:
+        raise TypeError(f"expected storage {np.dtype(want)}, got {a.dtype}")
+    return a
+
+
+def gemv(dtype: str, A, x, bias=None, scale=None, nthreads: int = 1):
+    """Oracle GEMV on stored values.
+
+    dtype: "f32" | "f16" | "bf16" | "w8".  A: (M, K) storage (float32, uint16 bit
+    patterns of fp16/bf16, or int8); x: (B, K) storage (bf16 bits for "w8");
+    bias: (M,) storage or None; scale: (M,) float32 for "w8".
+    Returns (y, absdot), both float64 of shape (B, M).
+    """
+    code = KIND[dtype]
+    A = _storage(A, code)
+    xcode = KIND["bf16"] if dtype == "w8" else code
+    x = _storage(x, xcode)
+    bias = _storage(bias, xcode)
+    if scale is not None:
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M, K = A.shape
+    B = x.shape[0]
+    if x.shape[1] != K or (bias is not None and bias.shape != (M,)):
+        raise ValueError("shape mismatch")
+    y = np.empty((B, M), dtype=np.float64)
+    absdot = np.empty((B, M), dtype=np.float64)
+    rc = lib().oracle_gemv(code, _ptr(A), _ptr(scale), _ptr(x), _ptr(bias), M, K, B,
+                           _ptr(y), _ptr(absdot), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemv rejected its arguments")
+    return y, absdot
+
+
+def decode(kind: str, bits) -> np.ndarray:
+    """Decode stored values ("f32", "f16", "bf16" bit patterns, or "w8" int8) to float64."""
+    code = KIND[kind]
+    a = _storage(np.asarray(bits).reshape(-1), code)
+    out = np.empty(a.size, dtype=np.float64)
+    if lib().oracle_decode(code, _ptr(a), a.size, _ptr(out)) != 0:
+        raise ValueError("bad decode request")
+    return out
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
