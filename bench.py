@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of libgemv on GB300: achieved HBM GB/s (cold L2) and % of the measured peak.
+
+One step = one pass of the fp32 workload with bias at M = 16384 over K in
+{16, 32, 4096}: three GEMVs back to back, inputs resident in HBM, L2 flushed
+(a write of twice the L2 size) before every GEMV.  Each GEMV is timed with CUDA
+events on the stream it runs on; the step time is the sum of the three.
+
+    value      = sum of Q_min bytes of the step / step time   (GB/s, whole job)
+    Q_min      = M*K*s_A + B*K*s_x + B*M*s_y                 (per GEMV)
+    roofline   = the K = 4096 GEMV (the dominant kernel): its Q_min / its mean
+                 event time, against the measured HBM copy bandwidth
+    e2e        = the same metric with A, x, bias copied from pinned host memory
+                 and y copied back inside the timed region, every step
+    cpu_baseline = the CPU oracle on the same step, on the host's cores
+    sweep      = every configuration at its full size, timed the same way
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs the same workload on its own GPU (replicas: the
+GEMV needs no exchange between GPUs); value adds the ranks' bytes over the
+slowest rank's time.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "GEMV achieved HBM GB/s (cold L2) & % of GB300 peak; µs per y=A·x"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gemv_kernels.cuh", "gemv_launch.cuh", "gemv_plan.cpp", "gemv_plan.h",
+                  "gemv_api.cu", "gemv_f32.cu", "gemv_f16.cu", "gemv_bf16.cu", "gemv_w8.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+HEADLINE_DESC = "f32 GEMV + bias at M=16384 over K in {16, 32, 4096}: 3 GEMVs per step"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--sweep-iters", type=int, default=30)
+    ap.add_argument("--only", default=None, help="sweep only these comma-separated configs")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "decode_linear_layers_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    sha = kernel_sha()
+    cur = None
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) >= 2 and parts[0] == "kernel_sha":
+            cur = parts[1]
+        elif len(parts) >= 3 and parts[0] == workload and parts[1] == "traffic_bytes" and cur == sha:
+            return int(parts[2].replace(",", ""))
+    return None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.perf_counter(), [c.strip() for c in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.rows and time.perf_counter() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for (_, r) in self.rows[-3:]]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(torch, dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ------------------------------------------------------------------ our arm
+def call_gemv(g, w, d, y):
+    if w.dtype == "w8":
+        g.gemv_w8(d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
+    else:
+        getattr(g, f"gemv_{w.dtype}")(d["A"], d["x"], d["bias"], y, w.M, w.K, w.B)
+
+
+def out_dtype(torch, dtype):
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "w8": torch.bfloat16}[dtype]
+
+
+def time_gemvs(torch, g, items, flush, iters, warmup):
+    """Per-GEMV CUDA-event times (ms), L2 flushed before each launch."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for (w, d, y) in items:
+            flush.zero_()
+            call_gemv(g, w, d, y)
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in items] for _ in range(iters)]
+    for s in range(iters):
+        for i, (w, d, y) in enumerate(items):
+            flush.zero_()
+            ev[s][i][0].record(stream)
+            call_gemv(g, w, d, y)
+            ev[s][i][1].record(stream)
+    torch.cuda.synchronize()
+    return [[ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(iters)] for i in range(len(items))]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import decode_linear_layers_gb300 as g
+
+    g.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    def allmax(v: float) -> float:
+        if pg is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peaks()
+
+    head = [W.BY_NAME[n] for n in W.HEADLINE]
+    host_inputs = [W.make_inputs(w) for w in head]
+    items = []
+    for w, inp in zip(head, host_inputs):
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        items.append((w, d, torch.empty((w.B, w.M), dtype=out_dtype(torch, w.dtype), device=dev)))
+
+    # ---- device-resident timed region
+    for _ in range(args.warmup):
+        for (w, d, y) in items:
+            flush.zero_()
+            call_gemv(g, w, d, y)
+    barrier()
+    sampler = ClockSampler(gpu_id_for(torch, dev)) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    n0 = g.launch_count()
+    t0 = time.perf_counter()
+    times = time_gemvs(torch, g, items, flush, args.steps, 0)
+    barrier()
+    t1 = time.perf_counter()
+    launches = g.launch_count() - n0
+    if sampler:
+        sampler.stop()
+    per_gemv_ms = [statistics.mean(t) for t in times]
+    step_ms = allmax(sum(per_gemv_ms))
+    step_bytes = sum(w.qmin_bytes for w in head)
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+
+    dom = max(range(len(head)), key=lambda i: per_gemv_ms[i])
+    wd = head[dom]
+    dom_ms = per_gemv_ms[dom]
+    achieved = wd.qmin_bytes / (dom_ms * 1e-3) / 1e9
+    plans = []
+    for (w, d, y) in items:
+        call_gemv(g, w, d, y)
+        plans.append(g.last_plan())
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": read_traffic(wd.name),
+                "kernel": plans[dom]["kernel_name"], "workload": wd.name, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": wd.qmin_bytes, "mean_us": round(dom_ms * 1e3, 3)}
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if rank == 0 or world > 1:
+        pinned = []
+        for (w, d, y), inp in zip(items, host_inputs):
+            hp = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+            hy = torch.empty((w.B, w.M), dtype=y.dtype).pin_memory()
+            pinned.append((hp, hy))
+        h2d = sum(sum(v.numel() * v.element_size() for v in hp.values() if v is not None) for hp, _ in pinned)
+        d2h = sum(hy.numel() * hy.element_size() for _, hy in pinned)
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for (w, d, y), (hp, hy) in zip(items, pinned):
+                for k, v in hp.items():
+                    if v is not None:
+                        d[k].copy_(v, non_blocking=True)
+                call_gemv(g, w, d, y)
+                hy.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e_ev.record()
+        torch.cuda.synchronize()
+        e2e_ms = allmax(s_ev.elapsed_time(e_ev) / e2e_steps)
+        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+               "steps": e2e_steps}
+
+    if rank != 0:
+        if pg is not None:
+            pg.barrier()
+        return None
+
+    clocks = sampler.summary(t0, t1) if sampler else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64: A ~ N(0, 1/K), x ~ N(0, 1), bias ~ N(0, 1))",
+        "config": {"workload": HEADLINE_DESC, "M": 16384, "K": [16, 32, 4096], "B": 1, "bias": True,
+                   "dtype": "f32", "l2": "flushed before every GEMV (write of 2x L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "per_gemv_us": {w.name: round(t * 1e3, 3) for w, t in zip(head, per_gemv_ms)},
+        "per_gemv_kernel": {w.name: p["kernel_name"] for w, p in zip(head, plans)},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+        "wall_s_timed_region": round(t1 - t0, 3),
+    }
+
+    if not args.no_sweep:
+        line["sweep"] = sweep(args, torch, g, dev, flush, peak)
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(head, host_inputs)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+    return line
+
+
+def sweep(args, torch, g, dev, flush, peak):
+    """Every configuration at full size: µs, GB/s and fraction of peak."""
+    out = []
+    names = [w.name for w in W.CONFIGS]
+    if args.only:
+        names = [n for n in names if n in args.only.split(",")]
+    for n in names:
+        w = W.BY_NAME[n]
+        inp = W.make_inputs(w)
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        del inp
+        y = torch.empty((w.B, w.M), dtype=out_dtype(torch, w.dtype), device=dev)
+        t = time_gemvs(torch, g, [(w, d, y)], flush, args.sweep_iters, 3)[0]
+        plan = g.last_plan()
+        med = statistics.median(t)
+        ts = sorted(t)
+        gbs = w.qmin_bytes / (med * 1e-3) / 1e9
+        out.append({"config": n, "kernel": plan["kernel_name"], "us_median": round(med * 1e3, 3),
+                    "us_p10": round(ts[len(ts) // 10] * 1e3, 3), "us_p90": round(ts[(9 * len(ts)) // 10] * 1e3, 3),
+                    "qmin_bytes": w.qmin_bytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                    "gflops": round(w.flops / (med * 1e-3) / 1e9, 1),
+                    "roofline_us": round(w.qmin_bytes / (peak * 1e9) * 1e6, 3)})
+        del d, y
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline(head, host_inputs, budget_s=10.0):
+    """The oracle (as it stands) on the same step, on all host cores."""
+    import oracle
+
+    cores = host_cores()
+    bits = [(w, W.storage_bits(i["A"]), W.storage_bits(i["x"]), W.storage_bits(i["bias"])) for w, i in zip(head, host_inputs)]
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for (w, A, x, b) in bits:
+            oracle.gemv(w.dtype, A, x, b, nthreads=cores)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 50:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    step_bytes = sum(w.qmin_bytes for w in head)
+    return {"value": round(step_bytes / dt / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the full step ({HEADLINE_DESC}), {reps} repetitions, fp64 C, OpenMP over rows",
+            "ms_per_step": round(dt * 1e3, 3)}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle timed on the host cores, on a bounded sample of the step."""
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    cores = host_cores()
+    head = [W.BY_NAME[n] for n in W.HEADLINE]
+    # a sample: the first `rows` rows of each GEMV of the step (same K, same values)
+    full = [W.make_inputs(w) for w in head]
+
+    def sample(rows):
+        out = []
+        for w, inp in zip(head, full):
+            r = min(rows, w.M)
+            out.append((w, r, W.storage_bits(inp["A"][:r]), W.storage_bits(inp["x"]),
+                        W.storage_bits(inp["bias"][:r])))
+        return out
+
+    def step(smp):
+        for (w, r, A, x, b) in smp:
+            oracle.gemv(w.dtype, A, x, b, nthreads=cores)
+
+    rows = 1024
+    smp = sample(rows)
+    t0 = time.perf_counter()
+    step(smp)
+    one = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)  # the whole run within ~1.5 minutes
+    if one > 0:
+        rows = int(max(64, min(16384, rows * budget / one)))
+    smp = sample(rows)
+    for _ in range(args.warmup):
+        step(smp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(smp)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    sbytes = sum(W.qmin_bytes(w.dtype, r, w.K, w.B) for (w, r, *_rest) in smp)
+    value = sbytes / dt / 1e9
+    desc = f"first {rows} rows of each of the 3 GEMVs of the step ({HEADLINE_DESC})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": HEADLINE_DESC, "M": 16384, "K": [16, 32, 4096], "B": 1, "bias": True,
+                   "dtype": "f32", "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+"""Python binding of libgemv (ctypes): argument marshalling only.
+
+The names and argument order are those of ``include/gemv.h``:
+
+    gemv_f32 (A, x, bias, y, M, K, B, stream=None)
+    gemv_f16 (A, x, bias, y, M, K, B, stream=None)
+    gemv_bf16(A, x, bias, y, M, K, B, stream=None)
+    gemv_w8  (A, row_scale, x, bias, y, M, K, B, stream=None)
+
+Buffers may be torch CUDA tensors (checked for device, contiguity, element size
+and minimum length before the call) or raw device addresses (ints, unchecked).
+``bias`` may be None.  ``stream`` may be None (torch's current stream), a
+``torch.cuda.Stream`` or a raw ``cudaStream_t`` value.  Every computation runs in
+the CUDA library; a status other than GEMV_SUCCESS raises ``GemvError``.  There is
+no fallback: without ``libgemv.so`` (build it with ``build()``) nothing runs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB as LIB_PATH, build
+
+__all__ = [
+    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "GemvError", "Plan", "plan_for",
+    "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
+    "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH",
+]
+
+SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3}
+KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
+           "split_k": 4, "batched": 5, "scalar": 6}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
+                ("rows_per_warp", ctypes.c_int), ("splits", ctypes.c_int), ("nb", ctypes.c_int),
+                ("threads", ctypes.c_int), ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
+        return d
+
+
+class GemvError(RuntimeError):
+    def __init__(self, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = status_string(status)
+        if status == ERR_CUDA:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgemv.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run decode_linear_layers_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for n in ("gemv_f32", "gemv_f16", "gemv_bf16"):
+            f = getattr(L, n)
+            f.argtypes = [vp, vp, vp, vp, i64, i64, ci, vp]
+            f.restype = ci
+        L.gemv_w8.argtypes = [vp, vp, vp, vp, vp, i64, i64, ci, vp]
+        L.gemv_w8.restype = ci
+        L.gemv_status_string.argtypes = [ci]
+        L.gemv_status_string.restype = ctypes.c_char_p
+        L.gemv_last_cuda_error.argtypes = []
+        L.gemv_last_cuda_error.restype = ci
+        L.gemv_launch_count.argtypes = []
+        L.gemv_launch_count.restype = ctypes.c_uint64
+        L.gemv_plan_for.argtypes = [ci, i64, i64, ci, ci, ci, ctypes.POINTER(Plan)]
+        L.gemv_plan_for.restype = ci
+        L.gemv_test_force_kernel.argtypes = [ci, ci]
+        L.gemv_test_force_kernel.restype = ci
+        L.gemv_test_last_plan.argtypes = [ctypes.POINTER(Plan)]
+        L.gemv_test_last_plan.restype = ci
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gemv_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return int(lib().gemv_last_cuda_error())
+
+
+def launch_count() -> int:
+    return int(lib().gemv_launch_count())
+
+
+def plan_for(dtype: str, M: int, K: int, B: int, aligned16: bool = True, num_sms: int = 152) -> dict:
+    p = Plan()
+    st = lib().gemv_plan_for(DTYPE_CODES[dtype], int(M), int(K), int(B), int(bool(aligned16)),
+                             int(num_sms), ctypes.byref(p))
+    if st != SUCCESS:
+        raise GemvError(st)
+    return p.as_dict()
+
+
+def force_kernel(kernel, param: int = 0) -> None:
+    """TEST ONLY: force a kernel family ("auto" restores dispatch)."""
+    k = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    st = lib().gemv_test_force_kernel(k, int(param))
+    if st != SUCCESS:
+        raise GemvError(st)
+
+
+def last_plan() -> dict:
+    """TEST ONLY: the plan of this thread's last successful call."""
+    p = Plan()
+    st = lib().gemv_test_last_plan(ctypes.byref(p))
+    if st != SUCCESS:
+        raise GemvError(st)
+    return p.as_dict()
+
+
+# ------------------------------------------------------------------ marshalling
+def _addr(t, elem_size: int, min_elems: int, what: str):
+    """Device address of a tensor (checked) or of a raw int pointer (unchecked)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{what} must be a CUDA tensor or a device address")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.element_size() != elem_size:
+        raise ValueError(f"{what}: element size {t.element_size()} != {elem_size}")
+    if t.numel() < min_elems:
+        raise ValueError(f"{what}: {t.numel()} elements < {min_elems} needed")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int) -> None:
+    if st != SUCCESS:
+        raise GemvError(st, last_cuda_error() if st == ERR_CUDA else 0)
+
+
+def _sizes(M, K, B):
+    M, K, B = int(M), int(K), int(B)
+    if min(M, K, B) < 0:
+        return M, K, B, 0, 0, 0  # let the library report the bad size
+    return M, K, B, M * K, B * K, B * M
+
+
+def _float_gemv(name, esize, A, x, bias, y, M, K, B, stream):
+    M, K, B, na, nx, ny = _sizes(M, K, B)
+    args = (_addr(A, esize, na, "A"), _addr(x, esize, nx, "x"),
+            _addr(bias, esize, M if bias is not None else 0, "bias"),
+            _addr(y, esize, ny, "y"))
+    _check(getattr(lib(), name)(*args, M, K, B, _stream(stream)))
+
+
+def gemv_f32(A, x, bias, y, M, K, B, stream=None) -> None:
+    """y[b, m] = sum_k A[m, k] x[b, k] (+ bias[m]); fp32 storage and accumulation."""
+    _float_gemv("gemv_f32", 4, A, x, bias, y, M, K, B, stream)
+
+
+def gemv_f16(A, x, bias, y, M, K, B, stream=None) -> None:
+    """fp16 storage (torch.float16), fp32 accumulation, fp16 output."""
+    _float_gemv("gemv_f16", 2, A, x, bias, y, M, K, B, stream)
+
+
+def gemv_bf16(A, x, bias, y, M, K, B, stream=None) -> None:
+    """bf16 storage (torch.bfloat16), fp32 accumulation, bf16 output."""
+    _float_gemv("gemv_bf16", 2, A, x, bias, y, M, K, B, stream)
+
+
+def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
+    """int8 A with fp32 row_scale; bf16 x, bias and y; fp32 accumulation."""
+    M, K, B, na, nx, ny = _sizes(M, K, B)
+    args = (_addr(A, 1, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, 2, nx, "x"),
+            _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
+    _check(lib().gemv_w8(*args, M, K, B, _stream(stream)))

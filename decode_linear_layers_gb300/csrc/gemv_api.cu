@@ -1,0 +1,185 @@
+// C-ABI entry points of libgemv: argument checks, dispatch, launch.
+//
+// The closest interface on the source pages is lesson 3's C launch function
+// (A, x, bias, y, M, N, stream) in "GEMV and row-level parallelism", which
+// returns nothing and checks nothing; this boundary keeps its shape (plain device
+// pointers, sizes, a stream) and adds B, status codes, host-side validation
+// (the NPU MatMul post, section 3.1: parameter and shape checks before any
+// kernel) and the per-shape kernel choice of gemv_plan.cpp.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/gemv.h"
+#include "gemv_launch.cuh"
+#include "gemv_plan.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local gemv_plan_t t_last_plan = {};
+thread_local bool t_have_plan = false;
+
+std::atomic<uint64_t> g_launches{0};
+int g_force_kernel = GEMV_KERNEL_AUTO;  // test-only override (not thread-safe)
+int g_force_param = 0;
+
+constexpr int kMaxDevices = 256;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+gemv_status_t cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return GEMV_ERR_CUDA;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
+
+// [p, p + n) and [q, q + m) share a byte.
+bool overlaps(const void *p, int64_t n, const void *q, int64_t m) {
+  if (p == nullptr || q == nullptr || n <= 0 || m <= 0) return false;
+  const uintptr_t a0 = (uintptr_t)p, a1 = a0 + (uintptr_t)n;
+  const uintptr_t b0 = (uintptr_t)q, b1 = b0 + (uintptr_t)m;
+  return a0 < b1 && b0 < a1;
+}
+
+bool aligned(const void *p, int bytes) { return ((uintptr_t)p % (uintptr_t)bytes) == 0; }
+
+gemv_status_t sm_count(int *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < kMaxDevices) {
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *out = v;
+      return GEMV_SUCCESS;
+    }
+  }
+  int v = 0;
+  e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(v, std::memory_order_relaxed);
+  *out = v;
+  return GEMV_SUCCESS;
+}
+
+typedef cudaError_t (*launch_fn)(const gemv_plan_t &, const gemv::Args &, float *, cudaStream_t);
+
+gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, const void *bias,
+                  void *y, int64_t M, int64_t K, int B, gemv_stream_t stream_in) {
+  if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
+  if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
+  if (M == 0 || B == 0) return GEMV_SUCCESS;
+  const int sa = gemv::elem_bytes_a(dtype), sx = gemv::elem_bytes_x(dtype);
+  const int sy = sx;
+  int64_t a_bytes, x_bytes, y_bytes, mk, bk, bm;
+  if (!mul_ok(M, K, &mk) || !mul_ok(mk, sa, &a_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (!mul_ok(B, K, &bk) || !mul_ok(bk, sx, &x_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (!mul_ok(B, M, &bm) || !mul_ok(bm, sy, &y_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (y == nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (K > 0 && (A == nullptr || x == nullptr)) return GEMV_ERR_INVALID_VALUE;
+  if (dtype == GEMV_DTYPE_W8 && scale == nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (!aligned(A, sa) || !aligned(x, sx) || !aligned(y, sy) || !aligned(bias, sx) ||
+      !aligned(scale, 4))
+    return GEMV_ERR_INVALID_VALUE;
+  if (overlaps(y, y_bytes, A, a_bytes) || overlaps(y, y_bytes, x, x_bytes) ||
+      overlaps(y, y_bytes, bias, M * sx) || overlaps(y, y_bytes, scale, M * 4))
+    return GEMV_ERR_INVALID_VALUE;
+
+  int sms = 0;
+  gemv_status_t st = sm_count(&sms);
+  if (st != GEMV_SUCCESS) return st;
+  const bool al16 = aligned(A, 16) && aligned(x, 16);
+  gemv_plan_t p;
+  st = gemv::plan(dtype, M, K, B, al16, sms, g_force_kernel, g_force_param, &p);
+  if (st != GEMV_SUCCESS) return st;
+
+  gemv::Args args;
+  args.A = A;
+  args.x = x;
+  args.bias = bias;
+  args.scale = scale;
+  args.y = y;
+  args.M = M;
+  args.K = K;
+  args.B = B;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_in);
+
+  launch_fn fn = dtype == GEMV_DTYPE_F32    ? gemv::launch_f32
+                 : dtype == GEMV_DTYPE_F16  ? gemv::launch_f16
+                 : dtype == GEMV_DTYPE_BF16 ? gemv::launch_bf16
+                                            : gemv::launch_w8;
+  float *ws = nullptr;
+  if (p.kernel == GEMV_KERNEL_SPLIT_K) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), (size_t)p.workspace_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  cudaError_t e = fn(p, args, ws, s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (ws != nullptr) {
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(p.kernel == GEMV_KERNEL_SPLIT_K ? 2 : 1, std::memory_order_relaxed);
+  t_last_plan = p;
+  t_have_plan = true;
+  return GEMV_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float *y, int64_t M,
+                       int64_t K, int B, gemv_stream_t stream) {
+  return run(GEMV_DTYPE_F32, A, nullptr, x, bias, y, M, K, B, stream);
+}
+
+gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, const uint16_t *bias, uint16_t *y,
+                       int64_t M, int64_t K, int B, gemv_stream_t stream) {
+  return run(GEMV_DTYPE_F16, A, nullptr, x, bias, y, M, K, B, stream);
+}
+
+gemv_status_t gemv_bf16(const uint16_t *A, const uint16_t *x, const uint16_t *bias, uint16_t *y,
+                        int64_t M, int64_t K, int B, gemv_stream_t stream) {
+  return run(GEMV_DTYPE_BF16, A, nullptr, x, bias, y, M, K, B, stream);
+}
+
+gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x,
+                      const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
+                      gemv_stream_t stream) {
+  return run(GEMV_DTYPE_W8, A, row_scale, x, bias, y, M, K, B, stream);
+}
+
+const char *gemv_status_string(gemv_status_t s) {
+  switch (s) {
+    case GEMV_SUCCESS: return "GEMV_SUCCESS";
+    case GEMV_ERR_INVALID_VALUE: return "GEMV_ERR_INVALID_VALUE";
+    case GEMV_ERR_UNSUPPORTED: return "GEMV_ERR_UNSUPPORTED";
+    case GEMV_ERR_CUDA: return "GEMV_ERR_CUDA";
+    default: return "GEMV_ERR_UNKNOWN";
+  }
+}
+
+int gemv_last_cuda_error(void) { return t_last_cuda_error; }
+
+uint64_t gemv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+gemv_status_t gemv_test_force_kernel(int kernel, int param) {
+  if (kernel < GEMV_KERNEL_AUTO || kernel > GEMV_KERNEL_SCALAR || param < 0)
+    return GEMV_ERR_INVALID_VALUE;
+  g_force_kernel = kernel;
+  g_force_param = kernel == GEMV_KERNEL_AUTO ? 0 : param;
+  return GEMV_SUCCESS;
+}
+
+gemv_status_t gemv_test_last_plan(gemv_plan_t *plan) {
+  if (plan == nullptr || !t_have_plan) return GEMV_ERR_INVALID_VALUE;
+  *plan = t_last_plan;
+  return GEMV_SUCCESS;
+}
+
+}  // extern "C"

@@ -1,0 +1,445 @@
+// Device code for libgemv: y[b][m] = s_m * sum_k A[m][k] * x[b][k] + bias[m].
+//
+// Everything here streams A once from HBM and is bound by HBM bandwidth (one
+// multiply-add per A element per vector: "16-sgemv" notes, closing summary;
+// lesson 3 "GEMV and row-level parallelism", section 1).  The kernels differ only
+// in how many threads share one output row:
+//
+//   k_rowteam   TPR = 1..32 lanes per row.  TPR < 32: several rows per warp for
+//               short rows (the notes' K = 16 kernel, generalised); TPR = 32: one
+//               warp per row with 16-byte loads (the notes' float4 kernel).  The
+//               VEC = false instance loads single elements for unaligned rows.
+//   k_blockrow  all 256 threads of a CTA on one row (lesson 3's block-per-row
+//               kernel), optionally over one K slice of it (split-K pass 1).
+//   k_splitk_reduce  split-K pass 2: sums the slices in slice order.
+//   k_batched   B > 1 vectors: x[0..B) staged once per CTA in shared memory by
+//               cp.async, each warp carries R rows so one x read feeds R rows.
+//
+// All reductions are fixed trees (xor butterflies, shared memory in warp order,
+// slices in index order): no atomics, bitwise-reproducible results.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gemv {
+
+constexpr int kThreads = 256;  // every kernel runs 8 warps per CTA
+constexpr int kWarps = kThreads / 32;
+
+struct Args {
+  const void *A;
+  const void *x;
+  const void *bias;     // nullptr: no bias
+  const float *scale;   // w8 row scale, nullptr otherwise
+  void *y;
+  int64_t M, K;
+  int B;
+};
+
+// ------------------------------------------------------------------ memory access
+// A is read exactly once: skip L1 and mark the L2 lines evict-first so x, y and
+// the rest of the working set stay cached.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void *ptr, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr), "l"(pol));
+  return r;
+}
+
+// x is re-read by every row: the read-only path, cached in L1.
+__device__ __forceinline__ uint4 ld_x16(const void *ptr) {
+  return __ldg(reinterpret_cast<const uint4 *>(ptr));
+}
+
+// --------------------------------------------------------------- element decoding
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t w) {
+  __half2 h = *reinterpret_cast<const __half2 *>(&w);
+  return __half22float2(h);
+}
+
+// int8 -> fp32 without a conversion instruction: with u = q + 128 (the byte with
+// its top bit flipped), the float whose bits are 0x4B0000uu is 2^23 + u exactly,
+// so subtracting 2^23 + 128 leaves q exactly.  PRMT builds the bits.
+template <int J>
+__device__ __forceinline__ float s8_to_f32(uint32_t flipped) {
+  return __uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7540 + J)) - 8388736.0f;
+}
+
+// ------------------------------------------------------------------- dtype traits
+// Each trait decodes one 16-byte chunk of A (VEC elements) against the matching
+// XCH x 16 bytes of one x vector and accumulates into two fp32 partial sums (even
+// and odd elements), in element order.
+struct OpF32 {
+  using TA = float;
+  using TX = float;
+  static constexpr int VEC = 4;
+  static constexpr int XCH = 1;
+  __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
+    e = fmaf(__uint_as_float(a.x), __uint_as_float(xv[0].x), e);
+    o = fmaf(__uint_as_float(a.y), __uint_as_float(xv[0].y), o);
+    e = fmaf(__uint_as_float(a.z), __uint_as_float(xv[0].z), e);
+    o = fmaf(__uint_as_float(a.w), __uint_as_float(xv[0].w), o);
+  }
+  __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
+    return __ldg(reinterpret_cast<const float *>(A) + i);
+  }
+  __device__ static __forceinline__ float x_elem(const void *x, int64_t i) {
+    return __ldg(reinterpret_cast<const float *>(x) + i);
+  }
+  __device__ static __forceinline__ void store(void *y, int64_t i, float v) {
+    reinterpret_cast<float *>(y)[i] = v;
+  }
+};
+
+struct OpBF16 {
+  using TA = __nv_bfloat16;
+  using TX = __nv_bfloat16;
+  static constexpr int VEC = 8;
+  static constexpr int XCH = 1;
+  __device__ static __forceinline__ void pair(float &e, float &o, uint32_t a, uint32_t x) {
+    e = fmaf(bf16_lo(a), bf16_lo(x), e);
+    o = fmaf(bf16_hi(a), bf16_hi(x), o);
+  }
+  __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
+    pair(e, o, a.x, xv[0].x);
+    pair(e, o, a.y, xv[0].y);
+    pair(e, o, a.z, xv[0].z);
+    pair(e, o, a.w, xv[0].w);
+  }
+  __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
+    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(A) + i));
+  }
+  __device__ static __forceinline__ float x_elem(const void *x, int64_t i) {
+    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(x) + i));
+  }
+  __device__ static __forceinline__ void store(void *y, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+struct OpF16 {
+  using TA = __half;
+  using TX = __half;
+  static constexpr int VEC = 8;
+  static constexpr int XCH = 1;
+  __device__ static __forceinline__ void pair(float &e, float &o, uint32_t a, uint32_t x) {
+    float2 fa = f16x2_to_f2(a), fx = f16x2_to_f2(x);
+    e = fmaf(fa.x, fx.x, e);
+    o = fmaf(fa.y, fx.y, o);
+  }
+  __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
+    pair(e, o, a.x, xv[0].x);
+    pair(e, o, a.y, xv[0].y);
+    pair(e, o, a.z, xv[0].z);
+    pair(e, o, a.w, xv[0].w);
+  }
+  __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
+    return __half2float(__ldg(reinterpret_cast<const __half *>(A) + i));
+  }
+  __device__ static __forceinline__ float x_elem(const void *x, int64_t i) {
+    return __half2float(__ldg(reinterpret_cast<const __half *>(x) + i));
+  }
+  __device__ static __forceinline__ void store(void *y, int64_t i, float v) {
+    reinterpret_cast<__half *>(y)[i] = __float2half_rn(v);
+  }
+};
+
+// int8 weights, bf16 activations: 16 weights per 16-byte chunk meet 32 bytes of x.
+struct OpW8 {
+  using TA = int8_t;
+  using TX = __nv_bfloat16;
+  static constexpr int VEC = 16;
+  static constexpr int XCH = 2;
+  __device__ static __forceinline__ void word(float &e, float &o, uint32_t a, uint32_t x01,
+                                              uint32_t x23) {
+    const uint32_t f = a ^ 0x80808080u;
+    e = fmaf(s8_to_f32<0>(f), bf16_lo(x01), e);
+    o = fmaf(s8_to_f32<1>(f), bf16_hi(x01), o);
+    e = fmaf(s8_to_f32<2>(f), bf16_lo(x23), e);
+    o = fmaf(s8_to_f32<3>(f), bf16_hi(x23), o);
+  }
+  __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
+    word(e, o, a.x, xv[0].x, xv[0].y);
+    word(e, o, a.y, xv[0].z, xv[0].w);
+    word(e, o, a.z, xv[1].x, xv[1].y);
+    word(e, o, a.w, xv[1].z, xv[1].w);
+  }
+  __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
+    return (float)__ldg(reinterpret_cast<const signed char *>(A) + i);
+  }
+  __device__ static __forceinline__ float x_elem(const void *x, int64_t i) {
+    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(x) + i));
+  }
+  __device__ static __forceinline__ void store(void *y, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+// bias is stored in the output type: fp32 for OpF32, otherwise the x type.
+template <class Op>
+__device__ __forceinline__ float bias_at(const void *bias, int64_t m) {
+  return Op::x_elem(bias, m);
+}
+
+// y = s_m * acc + bias[m], rounded once to the output type (lesson 3's epilogue:
+// bias added in fp32 after the reduction, NULL allowed).
+template <class Op>
+__device__ __forceinline__ void epilogue_store(const Args &a, int b, int64_t m, float acc) {
+  float v = acc;
+  if (a.scale != nullptr) v *= __ldg(a.scale + m);
+  if (a.bias != nullptr) v += bias_at<Op>(a.bias, m);
+  Op::store(a.y, (int64_t)b * a.M + m, v);
+}
+
+// Butterfly over WIDTH lanes: every lane of each WIDTH-lane group ends with the
+// group's sum, groups never mix (xor offsets < WIDTH stay inside the group).
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int off = WIDTH / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// ------------------------------------------------------------------ k_rowteam
+// TPR lanes per row, kThreads / TPR rows per CTA per pass, grid-stride over row
+// groups.  Lanes of a row take 16-byte chunks TPR apart (so a warp's loads are
+// contiguous), U chunks issued before any is consumed.  All 32 lanes of a warp
+// reach the butterfly, with rows past M contributing zeros.
+template <class Op, int TPR, int NB, int U, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_rowteam(const Args a) {
+  constexpr int TEAMS = kThreads / TPR;
+  const int sub = threadIdx.x & (TPR - 1);
+  const int team = threadIdx.x / TPR;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  const uint64_t pol = evict_first_policy();
+  constexpr int XB = Op::XCH * 16;  // bytes of one x vector per A chunk
+
+  for (int64_t base = (int64_t)blockIdx.x * TEAMS; base < M; base += (int64_t)gridDim.x * TEAMS) {
+    const int64_t row = base + team;
+    const bool live = row < M;
+    float e[NB], o[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
+
+    if (VEC) {
+      const int64_t nch = live ? K / Op::VEC : 0;
+      const char *arow = reinterpret_cast<const char *>(a.A) + row * K * (int64_t)sizeof(typename Op::TA);
+      const char *xb0 = reinterpret_cast<const char *>(a.x);
+      const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
+      for (int64_t c0 = sub; c0 < nch; c0 += (int64_t)TPR * U) {
+        uint4 av[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + (int64_t)u * TPR;
+          av[u] = (c < nch) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + (int64_t)u * TPR;
+          if (c < nch) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              if (b < B) {
+                uint4 xv[Op::XCH];
+#pragma unroll
+                for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
+                Op::dot(e[b], o[b], av[u], xv);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      const int64_t kend = live ? K : 0;
+      for (int64_t k = sub; k < kend; k += TPR) {
+        const float av = Op::a_elem(a.A, row * K + k);
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+          if (b < B) e[b] = fmaf(av, Op::x_elem(a.x, (int64_t)b * K + k), e[b]);
+      }
+    }
+
+#pragma unroll
+    for (int b = 0; b < NB; ++b) e[b] = group_sum<TPR>(e[b] + o[b]);
+    if (live && sub == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (b < B) epilogue_store<Op>(a, b, row, e[b]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ k_blockrow
+// One CTA per row (grid-stride over rows); blockIdx.y selects a K slice when the
+// row is split.  Partial sums: warp butterflies, then warp 0 adds the 8 warp
+// totals in warp order.  splits == 1 finishes the row here; otherwise the slice
+// total goes to partial[(slice * B + b) * M + row] for k_splitk_reduce.
+template <class Op, int NB, int U>
+__global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *partial,
+                                                       int64_t chunks_per_split) {
+  __shared__ float red[NB][kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  const uint64_t pol = evict_first_policy();
+  constexpr int XB = Op::XCH * 16;
+  const int64_t nch_all = K / Op::VEC;
+  const int64_t c_lo = (int64_t)blockIdx.y * chunks_per_split;
+  const int64_t c_hi = min(nch_all, c_lo + chunks_per_split);
+  const char *xb0 = reinterpret_cast<const char *>(a.x);
+  const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
+
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const char *arow = reinterpret_cast<const char *>(a.A) + row * K * (int64_t)sizeof(typename Op::TA);
+    float e[NB], o[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
+    for (int64_t c0 = c_lo + tid; c0 < c_hi; c0 += (int64_t)kThreads * U) {
+      uint4 av[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + (int64_t)u * kThreads;
+        av[u] = (c < c_hi) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + (int64_t)u * kThreads;
+        if (c < c_hi) {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (b < B) {
+              uint4 xv[Op::XCH];
+#pragma unroll
+              for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
+              Op::dot(e[b], o[b], av[u], xv);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float w = group_sum<32>(e[b] + o[b]);
+      if (lane == 0) red[b][warp] = w;
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < B && lane == 0) {
+          float s = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) s += red[b][w];
+          if (partial == nullptr) {
+            epilogue_store<Op>(a, b, row, s);
+          } else {
+            partial[((int64_t)blockIdx.y * B + b) * M + row] = s;
+          }
+        }
+      }
+    }
+    __syncthreads();  // red[] is reused by the next row
+  }
+}
+
+// Split-K pass 2: one thread per (b, m); slices summed in index order.
+template <class Op>
+__global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const float *partial,
+                                                            int splits) {
+  const int64_t M = a.M;
+  const int64_t total = M * a.B;
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * kThreads) {
+    const int b = (int)(i / M);
+    const int64_t m = i - (int64_t)b * M;
+    float s = 0.f;
+    for (int j = 0; j < splits; ++j) s += partial[((int64_t)j * a.B + b) * M + m];
+    epilogue_store<Op>(a, b, m, s);
+  }
+}
+
+// ------------------------------------------------------------------ k_batched
+// x[0..B) (B*K elements, a multiple of 16 bytes) is copied once per CTA into
+// shared memory with cp.async; warps then stream R rows at a time, each lane
+// taking 16-byte chunks 32 apart, so every x chunk read from shared memory feeds
+// R rows.  Requires B*K*sizeof(TX) <= the dynamic shared memory given.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+template <class Op, int NB, int R>
+__global__ void __launch_bounds__(kThreads) k_batched(const Args a) {
+  extern __shared__ __align__(16) unsigned char xs[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  constexpr int XB = Op::XCH * 16;
+  const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);  // bytes per x vector
+  {
+    const int64_t n16 = (xstride * B) / 16;
+    const char *src = reinterpret_cast<const char *>(a.x);
+    for (int64_t i = tid; i < n16; i += kThreads) cp_async16(xs + i * 16, src + i * 16);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
+  const uint64_t pol = evict_first_policy();
+  const int64_t nch = K / Op::VEC;
+  const int64_t rows_per_pass = (int64_t)gridDim.x * kWarps * R;
+
+  for (int64_t r0 = ((int64_t)blockIdx.x * kWarps + warp) * R; r0 < M; r0 += rows_per_pass) {
+    float e[R][NB], o[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) e[r][b] = o[r][b] = 0.f;
+    const char *arow[R];
+    bool live[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      live[r] = (r0 + r) < M;
+      arow[r] = reinterpret_cast<const char *>(a.A) +
+                (live[r] ? r0 + r : r0) * K * (int64_t)sizeof(typename Op::TA);
+    }
+    for (int64_t c = lane; c < nch; c += 32) {
+      uint4 av[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) av[r] = live[r] ? ld_stream16(arow[r] + c * 16, pol) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < B) {
+          uint4 xv[Op::XCH];
+#pragma unroll
+          for (int h = 0; h < Op::XCH; ++h)
+            xv[h] = *reinterpret_cast<const uint4 *>(xs + b * xstride + c * XB + h * 16);
+#pragma unroll
+          for (int r = 0; r < R; ++r) Op::dot(e[r][b], o[r][b], av[r], xv);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const float s = group_sum<32>(e[r][b] + o[r][b]);
+        if (lane == 0 && b < B && live[r]) epilogue_store<Op>(a, b, r0 + r, s);
+      }
+    }
+  }
+}
+
+}  // namespace gemv

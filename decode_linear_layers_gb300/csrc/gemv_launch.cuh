@@ -1,0 +1,99 @@
+// Plan -> kernel instantiation.  Included once per storage type (gemv_<dtype>.cu),
+// so the four types compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gemv_kernels.cuh"
+#include "gemv_plan.h"
+
+namespace gemv {
+
+// Unroll depth (16-byte chunks in flight per lane before the first is used).
+constexpr int kUnrollWarpRow = 4;
+constexpr int kUnrollBlockRow = 4;
+
+template <class Op, int NB>
+cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  const dim3 grid((unsigned)p.grid), block(kThreads);
+  if (p.kernel == GEMV_KERNEL_SCALAR) {
+    switch (p.lanes_per_row) {
+      case 4: k_rowteam<Op, 4, NB, 1, false><<<grid, block, 0, s>>>(a); break;
+      default: k_rowteam<Op, 32, NB, 1, false><<<grid, block, 0, s>>>(a); break;
+    }
+    return cudaSuccess;
+  }
+  switch (p.lanes_per_row) {
+    case 1: k_rowteam<Op, 1, NB, 1, true><<<grid, block, 0, s>>>(a); break;
+    case 2: k_rowteam<Op, 2, NB, 1, true><<<grid, block, 0, s>>>(a); break;
+    case 4: k_rowteam<Op, 4, NB, 1, true><<<grid, block, 0, s>>>(a); break;
+    case 8: k_rowteam<Op, 8, NB, 1, true><<<grid, block, 0, s>>>(a); break;
+    case 16: k_rowteam<Op, 16, NB, 1, true><<<grid, block, 0, s>>>(a); break;
+    case 32: k_rowteam<Op, 32, NB, kUnrollWarpRow, true><<<grid, block, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+template <class Op, int NB, int R>
+cudaError_t launch_batched_r(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  auto kern = k_batched<Op, NB, R>;
+  if (p.smem_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<dim3((unsigned)p.grid), dim3(kThreads), (size_t)p.smem_bytes, s>>>(a);
+  return cudaSuccess;
+}
+
+template <class Op, int NB>
+cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
+  switch (p.kernel) {
+    case GEMV_KERNEL_ROWS_PER_WARP:
+    case GEMV_KERNEL_WARP_PER_ROW:
+    case GEMV_KERNEL_SCALAR:
+      return launch_rowteam<Op, NB>(p, a, s);
+    case GEMV_KERNEL_BLOCK_PER_ROW:
+      k_blockrow<Op, NB, kUnrollBlockRow><<<dim3((unsigned)p.grid, 1), dim3(kThreads), 0, s>>>(
+          a, nullptr, a.K / Op::VEC);
+      return cudaSuccess;
+    case GEMV_KERNEL_SPLIT_K: {
+      const int64_t nch = a.K / Op::VEC;
+      const int64_t per = (nch + p.splits - 1) / p.splits;
+      k_blockrow<Op, NB, kUnrollBlockRow><<<dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kThreads), 0, s>>>(
+          a, ws, per);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      const int64_t total = a.M * a.B;
+      int64_t g = (total + kThreads - 1) / kThreads;
+      if (g > 65535) g = 65535;
+      k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
+      return cudaSuccess;
+    }
+    case GEMV_KERNEL_BATCHED:
+      if (p.rows_per_warp == 2) return launch_batched_r<Op, NB, 2>(p, a, s);
+      return launch_batched_r<Op, NB, 4>(p, a, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+template <class Op>
+cudaError_t launch(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
+  switch (p.nb) {
+    case 1: return launch_nb<Op, 1>(p, a, ws, s);
+    case 2: return launch_nb<Op, 2>(p, a, ws, s);
+    case 4: return launch_nb<Op, 4>(p, a, ws, s);
+    case 8: return launch_nb<Op, 8>(p, a, ws, s);
+    case 16: return launch_nb<Op, 16>(p, a, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Defined in gemv_f32.cu, gemv_f16.cu, gemv_bf16.cu, gemv_w8.cu.
+cudaError_t launch_f32(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
+cudaError_t launch_f16(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
+cudaError_t launch_bf16(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
+cudaError_t launch_w8(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
+
+}  // namespace gemv

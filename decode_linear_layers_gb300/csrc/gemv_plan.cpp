@@ -1,0 +1,189 @@
+// Host-side shape dispatcher for libgemv (no CUDA calls; unit-tested on the CPU).
+//
+// The one design axis of a GEMV is how many threads share an output row ("16-sgemv"
+// notes, design-space summary: elements per thread x rows per warp = 32; a short
+// row wastes lanes, few rows leave SMs idle).  Lesson 3 "GEMV and row-level
+// parallelism", section 4, gives the same rule by row length: a warp per row for
+// short rows, a CTA per row for long ones; the NPU MatMul post, sections 1.3 and
+// 3.4, asks for the kernel to be picked from (M, N, K, dtype, hardware) at run time.
+//
+// Rules used here (per call, from dtype, M, K, B, alignment and the SM count):
+//   rows not 16-byte aligned            -> SCALAR (element loads)
+//   row <= 16 chunks of 16 bytes        -> ROWS_PER_WARP, lanes = next pow2 of chunks
+//   B > 1 and x[0..B) fits in smem      -> BATCHED (x staged once per CTA)
+//   at least 16 rows per SM, or <= 4 KB -> WARP_PER_ROW
+//   at least 2 rows per SM              -> BLOCK_PER_ROW
+//   fewer rows                          -> SPLIT_K over enough K slices to give
+//                                          every SM about four CTAs
+#include <stdint.h>
+
+#include "../../include/gemv.h"
+#include "gemv_plan.h"
+
+namespace gemv {
+
+namespace {
+
+int next_pow2(int64_t v) {
+  int p = 1;
+  while (p < v && p < (1 << 30)) p <<= 1;
+  return p;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+int elem_bytes_a(int dtype) {
+  switch (dtype) {
+    case GEMV_DTYPE_F32: return 4;
+    case GEMV_DTYPE_F16:
+    case GEMV_DTYPE_BF16: return 2;
+    default: return 1;
+  }
+}
+
+int elem_bytes_x(int dtype) { return dtype == GEMV_DTYPE_F32 ? 4 : 2; }
+
+int rows_per_warp_for(int nb) { return nb >= 16 ? 2 : 4; }
+
+static bool rowteam_lanes_ok(int l) { return l == 1 || l == 2 || l == 4 || l == 8 || l == 16; }
+
+gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
+                   int force_kernel, int force_param, gemv_plan_t *out) {
+  if (out == nullptr || num_sms < 1) return GEMV_ERR_INVALID_VALUE;
+  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W8) return GEMV_ERR_INVALID_VALUE;
+  if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
+  if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
+  gemv_plan_t p = {};
+  p.kernel = GEMV_KERNEL_AUTO;
+  p.splits = 1;
+  p.threads = kPlanThreads;
+  if (M == 0 || B == 0) {
+    *out = p;
+    return GEMV_SUCCESS;
+  }
+  const int sa = elem_bytes_a(dtype), sx = elem_bytes_x(dtype);
+  const int vec = 16 / sa;
+  const bool vec_ok = aligned16 && (K % vec == 0);
+  const int64_t nch = vec_ok ? K / vec : 0;
+  const int64_t xbytes = (int64_t)B * K * sx;
+  p.nb = next_pow2(B);
+
+  int kernel = GEMV_KERNEL_AUTO;
+  int param = 0;
+  if (force_kernel != GEMV_KERNEL_AUTO) {
+    bool ok = false;
+    switch (force_kernel) {
+      case GEMV_KERNEL_ROWS_PER_WARP:
+        ok = vec_ok && (force_param == 0 || rowteam_lanes_ok(force_param));
+        break;
+      case GEMV_KERNEL_WARP_PER_ROW:
+      case GEMV_KERNEL_BLOCK_PER_ROW:
+        ok = vec_ok;
+        break;
+      case GEMV_KERNEL_SPLIT_K:
+        ok = vec_ok && nch >= 2 && force_param >= 0;
+        break;
+      case GEMV_KERNEL_BATCHED:
+        ok = vec_ok && xbytes <= kBatchedSmemMax &&
+             (force_param == 0 || force_param == 2 || force_param == 4);
+        break;
+      case GEMV_KERNEL_SCALAR:
+        ok = force_param == 0 || force_param == 4 || force_param == 32;
+        break;
+      default:
+        ok = false;
+    }
+    if (ok) {
+      kernel = force_kernel;
+      param = force_param;
+    }
+  }
+
+  if (kernel == GEMV_KERNEL_AUTO) {
+    if (!vec_ok) {
+      kernel = GEMV_KERNEL_SCALAR;
+    } else if (nch <= 16) {
+      kernel = GEMV_KERNEL_ROWS_PER_WARP;
+    } else if (B > 1 && xbytes <= kBatchedSmemMax && nch >= 32) {
+      kernel = GEMV_KERNEL_BATCHED;
+    } else if (M >= (int64_t)num_sms * 16 || nch <= kPlanThreads) {
+      kernel = GEMV_KERNEL_WARP_PER_ROW;  // many rows, or rows of at most 4 KB
+    } else if (M >= (int64_t)num_sms * 2 || nch < 2 * kPlanThreads) {
+      kernel = GEMV_KERNEL_BLOCK_PER_ROW;
+    } else {
+      kernel = GEMV_KERNEL_SPLIT_K;
+    }
+  }
+
+  p.kernel = kernel;
+  switch (kernel) {
+    case GEMV_KERNEL_ROWS_PER_WARP: {
+      int lanes = param != 0 ? param : next_pow2(nch < 1 ? 1 : nch);
+      if (lanes > 16) lanes = 16;
+      p.lanes_per_row = lanes;
+      const int64_t groups = ceil_div(M, kPlanThreads / lanes);
+      p.grid = groups < (int64_t)num_sms * 32 ? groups : (int64_t)num_sms * 32;
+      break;
+    }
+    case GEMV_KERNEL_WARP_PER_ROW: {
+      p.lanes_per_row = 32;
+      const int64_t groups = ceil_div(M, kPlanThreads / 32);
+      p.grid = groups < (int64_t)num_sms * 32 ? groups : (int64_t)num_sms * 32;
+      break;
+    }
+    case GEMV_KERNEL_SCALAR: {
+      int lanes = param != 0 ? param : (K <= 4 ? 4 : 32);
+      p.lanes_per_row = lanes;
+      const int64_t groups = ceil_div(M, kPlanThreads / lanes);
+      p.grid = groups < (int64_t)num_sms * 32 ? groups : (int64_t)num_sms * 32;
+      break;
+    }
+    case GEMV_KERNEL_BLOCK_PER_ROW: {
+      p.grid = M < (int64_t)num_sms * 16 ? M : (int64_t)num_sms * 16;
+      break;
+    }
+    case GEMV_KERNEL_SPLIT_K: {
+      int64_t s = param;
+      if (s <= 0) {
+        s = ceil_div((int64_t)num_sms * 4, M);
+        const int64_t cap = nch / kPlanThreads;  // at least one chunk per thread
+        if (s > cap) s = cap;
+        if (s < 2) s = 2;
+      }
+      if (s > nch) s = nch;
+      if (s > 65535) s = 65535;
+      const int64_t per = ceil_div(nch, s);
+      s = ceil_div(nch, per);  // no empty slices
+      p.splits = (int)s;
+      p.grid = M < (int64_t)num_sms * 16 ? M : (int64_t)num_sms * 16;
+      p.workspace_bytes = s * (int64_t)B * M * 4;
+      break;
+    }
+    case GEMV_KERNEL_BATCHED: {
+      const int r = param != 0 ? param : rows_per_warp_for(p.nb);
+      p.rows_per_warp = r;
+      p.smem_bytes = (int)xbytes;
+      const int64_t groups = ceil_div(M, (int64_t)(kPlanThreads / 32) * r);
+      // x is staged once per CTA, so the grid is persistent: a few CTAs per SM.
+      int64_t per_sm = (int64_t)(kSmemPerSm / (xbytes + 1024));
+      if (per_sm < 1) per_sm = 1;
+      if (per_sm > 2) per_sm = 2;
+      const int64_t cap = per_sm * num_sms;
+      p.grid = groups < cap ? groups : cap;
+      break;
+    }
+    default:
+      return GEMV_ERR_INVALID_VALUE;
+  }
+  *out = p;
+  return GEMV_SUCCESS;
+}
+
+}  // namespace gemv
+
+extern "C" gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B,
+                                       int aligned16, int num_sms, gemv_plan_t *plan) {
+  return gemv::plan((int)dtype, M, K, B, aligned16 != 0, num_sms, GEMV_KERNEL_AUTO, 0, plan);
+}

@@ -1,0 +1,24 @@
+// Internal interface between the C-ABI entry points, the dispatcher and the
+// per-dtype launch units.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/gemv.h"
+
+namespace gemv {
+
+constexpr int kPlanThreads = 256;
+// Largest x[0..B) the batched kernel stages in shared memory.
+constexpr int64_t kBatchedSmemMax = 200 * 1024;
+// Shared memory one SM can give to resident CTAs (sm_100-class: 228 KB).
+constexpr int64_t kSmemPerSm = 228 * 1024;
+
+int elem_bytes_a(int dtype);
+int elem_bytes_x(int dtype);
+int rows_per_warp_for(int nb);
+
+gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
+                   int force_kernel, int force_param, gemv_plan_t *out);
+
+}  // namespace gemv

@@ -1,0 +1,165 @@
+/*
+ * libgemv — dense matrix-vector products for LLM decode on NVIDIA GB300 (sm_103a).
+ *
+ * Every entry point computes, for b in [0, B) and m in [0, M):
+ *
+ *     y[b][m] = s_m * sum_{k=0}^{K-1} A[m][k] * x[b][k]  (+ bias[m])
+ *
+ * with the sum accumulated in fp32 and the result rounded once (round to nearest
+ * even) to the output type.  s_m is the per-row weight scale of gemv_w8 and is 1
+ * for the other entry points.
+ *
+ * Where the operation is defined:
+ *   - "16-sgemv" CUDA study notes, problem definition: y[m] = sum_k A[m][k] x[k],
+ *     A is M x K row-major, one dot product per output row;
+ *   - lesson 3 "GEMV and row-level parallelism", section 1 (y = A x + bias) and
+ *     section 3 (bias may be absent: a NULL bias adds nothing);
+ *   - the GEMM/GEMV arithmetic-intensity glossary page: decode batches of M = 1
+ *     and M = 16 activation rows against one weight, fp32 accumulation for 16-bit
+ *     storage types;
+ *   - the NPU MatMul operator post, section 1.2: quantised MatMul with int8
+ *     weights, 16-bit activations, an fp32 accumulator and a write-back to the
+ *     target dtype; section 4.2: a per-channel (here per-row) weight scale.
+ *
+ * Layout (all row-major, contiguous, no leading-dimension arguments):
+ *   A    M x K     row m starts at A + m*K
+ *   x    B x K     vector b starts at x + b*K
+ *   y    B x M     output row b starts at y + b*M
+ *   bias M         may be NULL
+ *   row_scale M    gemv_w8 only, fp32, required
+ * 16-bit floating point values are passed as their IEEE binary16 / bfloat16 bit
+ * patterns (uint16_t).
+ *
+ * Ownership and memory: every pointer is caller-owned DEVICE memory on the
+ * current CUDA device.  A, x, bias and row_scale are only read; y is only written
+ * and must not overlap any input (checked on the host).  The library keeps no
+ * pointer after the call returns.  Only the split-K path uses scratch memory: it
+ * takes it from the stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
+ * caller's stream), so nothing is allocated or freed synchronously.
+ *
+ * Execution: asynchronous on `stream` (NULL = the legacy default stream).  The
+ * call validates its arguments, picks a kernel from (dtype, M, K, B, alignment)
+ * and enqueues one kernel (two on the split-K path).  It never synchronises the
+ * host with the device.  Results are bitwise identical from call to call for the
+ * same arguments on the same device.
+ *
+ * Errors: the return value.  GEMV_ERR_INVALID_VALUE for negative sizes, NULL
+ * pointers where data is needed, pointers not aligned to their element size,
+ * sizes whose byte counts overflow int64, or y overlapping an input;
+ * GEMV_ERR_UNSUPPORTED for B > 16; GEMV_ERR_CUDA when a CUDA call fails (the
+ * cudaError_t is kept per thread, see gemv_last_cuda_error).  Nothing is enqueued
+ * when an argument check fails.
+ *
+ * Degenerate sizes: M == 0 or B == 0 does nothing and returns GEMV_SUCCESS.
+ * K == 0 is the empty sum: y = bias (or 0), and A and x may then be NULL.
+ */
+#ifndef LIBGEMV_GEMV_H
+#define LIBGEMV_GEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as the CUDA runtime's cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *gemv_stream_t;
+
+typedef enum gemv_status {
+  GEMV_SUCCESS = 0,
+  GEMV_ERR_INVALID_VALUE = 1,
+  GEMV_ERR_UNSUPPORTED = 2,
+  GEMV_ERR_CUDA = 3
+} gemv_status_t;
+
+/* Storage kinds, as used by gemv_plan_for. */
+typedef enum gemv_dtype {
+  GEMV_DTYPE_F32 = 0,  /* A, x, bias, y: fp32 */
+  GEMV_DTYPE_F16 = 1,  /* A, x, bias, y: IEEE binary16 */
+  GEMV_DTYPE_BF16 = 2, /* A, x, bias, y: bfloat16 */
+  GEMV_DTYPE_W8 = 3    /* A: int8 + fp32 row scale; x, bias, y: bfloat16 */
+} gemv_dtype_t;
+
+/* Maximum number of decode vectors per call. */
+#define GEMV_MAX_BATCH 16
+
+/* fp32: A M x K, x B x K, y B x M.  The "16-sgemv" notes' SGEMV plus the lesson's bias. */
+gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float *y,
+                       int64_t M, int64_t K, int B, gemv_stream_t stream);
+
+/* fp16 storage, fp32 accumulation, fp16 output (arithmetic-intensity page's fp16 x @ w). */
+gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
+                       uint16_t *y, int64_t M, int64_t K, int B, gemv_stream_t stream);
+
+/* bf16 storage, fp32 accumulation, bf16 output. */
+gemv_status_t gemv_bf16(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
+                        uint16_t *y, int64_t M, int64_t K, int B, gemv_stream_t stream);
+
+/* Weight-only int8: A int8 M x K with row_scale[m] (fp32); x, bias, y bf16.
+ * y[b][m] = row_scale[m] * sum_k A[m][k] x[b][k] + bias[m]; the int8 values are
+ * widened to fp32 in registers (NPU MatMul post, sections 1.2 and 5.2). */
+gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x,
+                      const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
+                      gemv_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *gemv_status_string(gemv_status_t status);
+
+/* The cudaError_t of this thread's last GEMV_ERR_CUDA (0 if none). */
+int gemv_last_cuda_error(void);
+
+/* Kernels launched by this process so far (all threads, all devices). */
+uint64_t gemv_launch_count(void);
+
+/* ------------------------------------------------------------------ dispatcher */
+
+/* Kernel families.  The threads given to one output row are the design axis
+ * ("16-sgemv" notes, design-space summary: elements per thread x rows per warp =
+ * 32; lesson 3 section 4: warp per row for short rows, block per row for long
+ * ones). */
+typedef enum gemv_kernel {
+  GEMV_KERNEL_AUTO = 0,
+  GEMV_KERNEL_ROWS_PER_WARP = 1, /* 1..16 lanes per row, several rows per warp (short K) */
+  GEMV_KERNEL_WARP_PER_ROW = 2,  /* one warp per row, 16-byte coalesced loads */
+  GEMV_KERNEL_BLOCK_PER_ROW = 3, /* one CTA per row, shared-memory reduction */
+  GEMV_KERNEL_SPLIT_K = 4,       /* CTAs over K slices + fixed-order second pass */
+  GEMV_KERNEL_BATCHED = 5,       /* x[0..B) staged in shared memory, R rows per warp */
+  GEMV_KERNEL_SCALAR = 6         /* element loads, for rows that are not 16-byte aligned */
+} gemv_kernel_t;
+
+typedef struct gemv_plan {
+  int kernel;              /* gemv_kernel_t */
+  int lanes_per_row;       /* ROWS_PER_WARP / WARP_PER_ROW / SCALAR: threads per row */
+  int rows_per_warp;       /* BATCHED: rows one warp carries at once */
+  int splits;              /* SPLIT_K: number of K slices (1 otherwise) */
+  int nb;                  /* vector count the kernel is built for (>= B, power of 2) */
+  int threads;             /* threads per CTA */
+  int64_t grid;            /* CTAs of the first (or only) kernel */
+  int smem_bytes;          /* dynamic shared memory per CTA */
+  int64_t workspace_bytes; /* split-K partial sums (stream-ordered pool) */
+} gemv_plan_t;
+
+/* Host-only: the plan the entry points would use on a device with `num_sms` SMs.
+ * `aligned16` says whether A and x start on 16-byte boundaries.  Launches nothing,
+ * touches no device.  Returns GEMV_ERR_INVALID_VALUE / GEMV_ERR_UNSUPPORTED for
+ * arguments the entry points would reject; for M == 0 or B == 0 the plan has
+ * kernel = GEMV_KERNEL_AUTO and grid = 0. */
+gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int aligned16,
+                            int num_sms, gemv_plan_t *plan);
+
+/* TEST ONLY — not thread-safe.  Make every later call use `kernel` with `param`
+ * (lanes_per_row, rows_per_warp or splits; 0 = the dispatcher's choice) when the
+ * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  A forced kernel
+ * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
+ * falls back to the dispatcher's choice. */
+gemv_status_t gemv_test_force_kernel(int kernel, int param);
+
+/* TEST ONLY — the plan of this thread's last successful launch. */
+gemv_status_t gemv_test_last_plan(gemv_plan_t *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBGEMV_GEMV_H */

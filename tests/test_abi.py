@@ -1,0 +1,204 @@
+"""libgemv on the host, without a GPU: exports, argument checks, dispatcher rules.
+
+No test here makes a call that passes validation, so nothing reaches a device:
+every call either returns before any CUDA work or is a host-only function.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import decode_linear_layers_gb300 as g
+from decode_linear_layers_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemv.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_status_string",
+              "gemv_last_cuda_error", "gemv_plan_for"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported():
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    L = ctypes.CDLL(g.LIB_PATH)
+    for n in declared_functions():
+        assert getattr(L, n) is not None
+
+
+def test_header_compiles_as_c():
+    src = '#include "gemv.h"\nint main(void){ gemv_plan_t p; return (int)sizeof(p) > 0 ? 0 : 1; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-", "-fsyntax-only"], input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings():
+    assert g.status_string(0) == "GEMV_SUCCESS"
+    assert g.status_string(1) == "GEMV_ERR_INVALID_VALUE"
+    assert g.status_string(2) == "GEMV_ERR_UNSUPPORTED"
+    assert g.status_string(3) == "GEMV_ERR_CUDA"
+    assert g.status_string(99) == "GEMV_ERR_UNKNOWN"
+
+
+# --------------------------------------------------------- argument validation
+# Fake addresses: every call below must be rejected before any device work.
+P = 1 << 32
+
+
+def call(fn, *a):
+    L = g.lib()
+    return getattr(L, fn)(*a)
+
+
+def test_negative_sizes_and_big_batch():
+    for fn in ("gemv_f32", "gemv_f16", "gemv_bf16"):
+        assert call(fn, P, P + 4096, None, P + 8192, -1, 4, 1, None) == 1
+        assert call(fn, P, P + 4096, None, P + 8192, 4, -1, 1, None) == 1
+        assert call(fn, P, P + 4096, None, P + 8192, 4, 4, -1, None) == 1
+        assert call(fn, P, P + 4096, None, P + 8192, 4, 4, 17, None) == 2
+    assert g.lib().gemv_w8(P, P + 64, P + 4096, None, P + 8192, 4, 4, 17, None) == 2
+
+
+def test_empty_problems_succeed_without_device():
+    # M == 0 or B == 0: nothing to do, no device touched
+    assert call("gemv_f32", None, None, None, None, 0, 5, 1, None) == 0
+    assert call("gemv_bf16", None, None, None, None, 7, 5, 0, None) == 0
+    assert g.lib().gemv_w8(None, None, None, None, None, 0, 3, 2, None) == 0
+
+
+def test_null_pointers():
+    assert call("gemv_f32", P, P + 4096, None, None, 4, 4, 1, None) == 1      # y
+    assert call("gemv_f32", None, P + 4096, None, P + 8192, 4, 4, 1, None) == 1  # A with K > 0
+    assert call("gemv_f32", P, None, None, P + 8192, 4, 4, 1, None) == 1      # x with K > 0
+    assert g.lib().gemv_w8(P, None, P + 4096, None, P + 8192, 4, 16, 1, None) == 1  # scale
+
+
+def test_misaligned_pointers():
+    assert call("gemv_f32", P + 2, P + 4096, None, P + 8192, 4, 4, 1, None) == 1
+    assert call("gemv_f32", P, P + 4097, None, P + 8192, 4, 4, 1, None) == 1
+    assert call("gemv_f32", P, P + 4096, P + 6, P + 8192, 4, 4, 1, None) == 1
+    assert call("gemv_f32", P, P + 4096, None, P + 8193, 4, 4, 1, None) == 1
+    assert call("gemv_bf16", P + 1, P + 4096, None, P + 8192, 4, 4, 1, None) == 1
+    assert g.lib().gemv_w8(P + 1, P + 66, P + 4096, None, P + 8192, 4, 16, 1, None) == 1
+
+
+def test_overlapping_output():
+    # y inside A, y over x, y over bias, y over the w8 scale
+    assert call("gemv_f32", P, P + 4096, None, P + 16, 4, 4, 1, None) == 1
+    assert call("gemv_f32", P, P + 4096, None, P + 4100, 4, 4, 1, None) == 1
+    assert call("gemv_f32", P, P + 4096, P + 8192, P + 8196, 4, 4, 1, None) == 1
+    assert g.lib().gemv_w8(P, P + 8192, P + 4096, None, P + 8192, 4, 16, 1, None) == 1
+    # touching but not overlapping is fine up to the device step; not called here
+
+
+def test_size_overflow():
+    big = 1 << 62
+    assert call("gemv_f32", P, P + 4096, None, P + 8192, big, 16, 1, None) == 1
+    assert call("gemv_f32", P, P + 4096, None, P + 8192, 16, big, 1, None) == 1
+
+
+def test_force_kernel_validation():
+    with pytest.raises(g.GemvError):
+        g.force_kernel(99)
+    with pytest.raises(g.GemvError):
+        g.force_kernel("split_k", -1)
+    g.force_kernel("auto")
+
+
+# ------------------------------------------------------------- dispatcher rules
+def test_plan_config_shapes():
+    K = g.KERNELS
+    assert g.plan_for("f32", 1024, 128, 1)["kernel"] == K["warp_per_row"]
+    p = g.plan_for("f32", 16384, 16, 1)
+    assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 4
+    p = g.plan_for("f32", 16384, 32, 1)
+    assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 8
+    assert g.plan_for("f32", 16384, 4096, 1)["kernel"] == K["warp_per_row"]
+    assert g.plan_for("f16", 4096, 4096, 1)["kernel"] == K["warp_per_row"]
+    p = g.plan_for("f16", 4096, 4096, 16)
+    assert p["kernel"] == K["batched"] and p["nb"] == 16 and p["smem_bytes"] == 16 * 4096 * 2
+    for M, Kd in ((14336, 4096), (4096, 14336), (128256, 4096)):
+        assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["warp_per_row"]
+    assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["warp_per_row"]
+    p = g.plan_for("w8", 8192, 8192, 4)
+    assert p["kernel"] == K["batched"] and p["smem_bytes"] == 4 * 8192 * 2
+
+
+def test_plan_small_k_lanes():
+    # K <= 16 chunks of 16 bytes: lanes per row = next power of two of the chunks
+    for dt, vec in (("f32", 4), ("f16", 8), ("bf16", 8), ("w8", 16)):
+        for chunks, lanes in ((1, 1), (2, 2), (3, 4), (5, 8), (9, 16), (16, 16)):
+            p = g.plan_for(dt, 1000, chunks * vec, 1)
+            assert p["kernel"] == g.KERNELS["rows_per_warp"], (dt, chunks)
+            assert p["lanes_per_row"] == lanes, (dt, chunks)
+            assert p["grid"] == min(-(-1000 // (256 // lanes)), 152 * 32)
+
+
+def test_plan_unaligned_goes_scalar():
+    assert g.plan_for("f32", 100, 4096, 1, aligned16=False)["kernel"] == g.KERNELS["scalar"]
+    assert g.plan_for("f32", 100, 4095, 1)["kernel"] == g.KERNELS["scalar"]   # K % 4 != 0
+    assert g.plan_for("w8", 100, 4104, 1)["kernel"] == g.KERNELS["scalar"]    # K % 16 != 0
+    p = g.plan_for("f16", 100, 3, 1)
+    assert p["kernel"] == g.KERNELS["scalar"] and p["lanes_per_row"] == 4
+
+
+def test_plan_few_rows_long_k():
+    p = g.plan_for("bf16", 8, 1 << 20, 1)
+    assert p["kernel"] == g.KERNELS["split_k"]
+    assert p["splits"] >= 2
+    assert p["workspace_bytes"] == p["splits"] * 1 * 8 * 4
+    nch = (1 << 20) // 8
+    per = -(-nch // p["splits"])
+    assert (p["splits"] - 1) * per < nch  # no empty slice
+    p = g.plan_for("bf16", 600, 1 << 16, 1)   # 2..16 rows per SM: a CTA per row
+    assert p["kernel"] == g.KERNELS["block_per_row"] and p["grid"] == 600
+
+
+def test_plan_batch_too_big_for_smem():
+    # 16 vectors of 16384 bf16 = 512 KB of x: not staged, warp per row instead
+    p = g.plan_for("bf16", 8192, 16384, 16)
+    assert p["kernel"] == g.KERNELS["warp_per_row"] and p["nb"] == 16
+
+
+def test_plan_nb_rounding_and_degenerate():
+    for B, nb in ((1, 1), (2, 2), (3, 4), (5, 8), (9, 16), (16, 16)):
+        assert g.plan_for("f32", 4096, 4096, B)["nb"] == nb
+    p = g.plan_for("f32", 0, 10, 1)
+    assert p["kernel"] == 0 and p["grid"] == 0
+    p = g.plan_for("f32", 10, 0, 1)   # K = 0: epilogue only
+    assert p["kernel"] == g.KERNELS["rows_per_warp"] and p["lanes_per_row"] == 1
+    with pytest.raises(g.GemvError):
+        g.plan_for("f32", 10, 10, 17)
+    with pytest.raises(g.GemvError):
+        g.plan_for("f32", -1, 10, 1)
+
+
+def test_plan_grid_never_exceeds_cap():
+    for M in (1, 7, 100, 5000, 10 ** 6, 10 ** 8):
+        for Kd in (16, 128, 4096):
+            for B in (1, 4, 16):
+                p = g.plan_for("bf16", M, Kd, B, num_sms=152)
+                assert 1 <= p["grid"] <= max(M, 152 * 32)
