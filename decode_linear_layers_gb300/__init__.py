@@ -30,13 +30,15 @@ __all__ = [
 SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3}
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
-           "split_k": 4, "batched": 5, "scalar": 6}
+           "split_k": 4, "batched": 5, "scalar": 6, "stream": 7}
+X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32"}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
-                ("rows_per_warp", ctypes.c_int), ("splits", ctypes.c_int), ("nb", ctypes.c_int),
+                ("rows_per_warp", ctypes.c_int), ("splits", ctypes.c_int), ("unroll", ctypes.c_int),
+                ("x_staging", ctypes.c_int), ("nb", ctypes.c_int),
                 ("threads", ctypes.c_int), ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_int64)]
 

@@ -1,19 +1,24 @@
 // Device code for libgemv: y[b][m] = s_m * sum_k A[m][k] * x[b][k] + bias[m].
 //
-// Everything here streams A once from HBM and is bound by HBM bandwidth (one
-// multiply-add per A element per vector: "16-sgemv" notes, closing summary;
-// lesson 3 "GEMV and row-level parallelism", section 1).  The kernels differ only
-// in how many threads share one output row:
+// Everything here streams A once from HBM and is bound by HBM bandwidth, or for
+// many vectors by the fp32 FMA rate (one multiply-add per A element per vector:
+// "16-sgemv" notes, closing summary; lesson 3 "GEMV and row-level parallelism",
+// section 1).  The kernels differ in how many threads share one output row and in
+// where x lives:
 //
-//   k_rowteam   TPR = 1..32 lanes per row.  TPR < 32: several rows per warp for
-//               short rows (the notes' K = 16 kernel, generalised); TPR = 32: one
-//               warp per row with 16-byte loads (the notes' float4 kernel).  The
-//               VEC = false instance loads single elements for unaligned rows.
+//   k_rowteam   TPR = 1..32 lanes per row, x through L1.  TPR < 32: several rows
+//               per warp for short rows (the notes' K = 16 kernel, generalised);
+//               TPR = 32: one warp per row with 16-byte loads (the notes' float4
+//               kernel), non-persistent grid for very tall matrices.  VEC = false
+//               loads single elements for rows that are not 16-byte aligned.
+//   k_stream    B = 1: persistent warps, one row at a time per warp, loads
+//               double-buffered across row boundaries, x in shared memory.
 //   k_blockrow  all 256 threads of a CTA on one row (lesson 3's block-per-row
 //               kernel), optionally over one K slice of it (split-K pass 1).
 //   k_splitk_reduce  split-K pass 2: sums the slices in slice order.
-//   k_batched   B > 1 vectors: x[0..B) staged once per CTA in shared memory by
-//               cp.async, each warp carries R rows so one x read feeds R rows.
+//   k_batch_lo  2 <= B <= 4: x in shared memory (fp32 where it fits), R rows per
+//               warp, every widened A element meets all B vectors, packed FMAs.
+//   k_batched2  5 <= B <= 16: x in shared memory as stored, R rows per warp.
 //
 // All reductions are fixed trees (xor butterflies, shared memory in warp order,
 // slices in index order): no atomics, bitwise-reproducible results.
@@ -56,6 +61,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void *ptr, uint64_t pol) {
   return r;
 }
 
+// 16-byte global -> shared copy that bypasses registers (completed by
+// cp.async.wait_group).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
 // x is re-read by every row: the read-only path, cached in L1.
 __device__ __forceinline__ uint4 ld_x16(const void *ptr) {
   return __ldg(reinterpret_cast<const uint4 *>(ptr));
@@ -93,6 +105,21 @@ struct OpF32 {
     e = fmaf(__uint_as_float(a.z), __uint_as_float(xv[0].z), e);
     o = fmaf(__uint_as_float(a.w), __uint_as_float(xv[0].w), o);
   }
+  __device__ static __forceinline__ void dot1(float &acc, const uint4 &a, const uint4 *xv) {
+    acc = fmaf(__uint_as_float(a.x), __uint_as_float(xv[0].x), acc);
+    acc = fmaf(__uint_as_float(a.y), __uint_as_float(xv[0].y), acc);
+    acc = fmaf(__uint_as_float(a.z), __uint_as_float(xv[0].z), acc);
+    acc = fmaf(__uint_as_float(a.w), __uint_as_float(xv[0].w), acc);
+  }
+  __device__ static __forceinline__ void quad2(const uint4 &a, int, float2 &q01, float2 &q23) {
+    q01 = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+    q23 = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+  }
+  // x elements 4w .. 4w+3 of the chunk, from x stored as fp32 at p (16 bytes).
+  __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+  }
   __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
     return __ldg(reinterpret_cast<const float *>(A) + i);
   }
@@ -118,6 +145,29 @@ struct OpBF16 {
     pair(e, o, a.y, xv[0].y);
     pair(e, o, a.z, xv[0].z);
     pair(e, o, a.w, xv[0].w);
+  }
+  // acc += a.lo * x.lo + a.hi * x.hi with the mixed-precision FMA (bf16 inputs,
+  // fp32 accumulator): the bf16 product is exact in fp32, one rounding per FMA.
+  __device__ static __forceinline__ void pair1(float &acc, uint32_t a, uint32_t x) {
+    asm("{\n\t.reg .b16 al, ah, xl, xh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, xl, %0;\n\tfma.rn.f32.bf16 %0, ah, xh, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(x));
+  }
+  __device__ static __forceinline__ void dot1(float &acc, const uint4 &a, const uint4 *xv) {
+    pair1(acc, a.x, xv[0].x);
+    pair1(acc, a.y, xv[0].y);
+    pair1(acc, a.z, xv[0].z);
+    pair1(acc, a.w, xv[0].w);
+  }
+  __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
+    const uint32_t u0 = w ? a.z : a.x, u1 = w ? a.w : a.y;
+    q01 = make_float2(bf16_lo(u0), bf16_hi(u0));
+    q23 = make_float2(bf16_lo(u1), bf16_hi(u1));
+  }
+  // 4 bf16 x values (8 bytes at p) as fp32.
+  __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    q[0] = bf16_lo(v.x); q[1] = bf16_hi(v.x); q[2] = bf16_lo(v.y); q[3] = bf16_hi(v.y);
   }
   __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
     return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(A) + i));
@@ -145,6 +195,28 @@ struct OpF16 {
     pair(e, o, a.y, xv[0].y);
     pair(e, o, a.z, xv[0].z);
     pair(e, o, a.w, xv[0].w);
+  }
+  // acc += a.lo * x.lo + a.hi * x.hi with the mixed-precision FMA (fp16 inputs,
+  // fp32 accumulator): the fp16 product is exact in fp32, one rounding per FMA.
+  __device__ static __forceinline__ void pair1(float &acc, uint32_t a, uint32_t x) {
+    asm("{\n\t.reg .b16 al, ah, xl, xh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, xl, %0;\n\tfma.rn.f32.f16 %0, ah, xh, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(x));
+  }
+  __device__ static __forceinline__ void dot1(float &acc, const uint4 &a, const uint4 *xv) {
+    pair1(acc, a.x, xv[0].x);
+    pair1(acc, a.y, xv[0].y);
+    pair1(acc, a.z, xv[0].z);
+    pair1(acc, a.w, xv[0].w);
+  }
+  __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
+    q01 = f16x2_to_f2(w ? a.z : a.x);
+    q23 = f16x2_to_f2(w ? a.w : a.y);
+  }
+  __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    const float2 f0 = f16x2_to_f2(v.x), f1 = f16x2_to_f2(v.y);
+    q[0] = f0.x; q[1] = f0.y; q[2] = f1.x; q[3] = f1.y;
   }
   __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
     return __half2float(__ldg(reinterpret_cast<const __half *>(A) + i));
@@ -176,6 +248,33 @@ struct OpW8 {
     word(e, o, a.y, xv[0].z, xv[0].w);
     word(e, o, a.z, xv[1].x, xv[1].y);
     word(e, o, a.w, xv[1].z, xv[1].w);
+  }
+  __device__ static __forceinline__ void word1(float &acc, uint32_t a, uint32_t x01, uint32_t x23) {
+    const uint32_t f = a ^ 0x80808080u;
+    acc = fmaf(s8_to_f32<0>(f), bf16_lo(x01), acc);
+    acc = fmaf(s8_to_f32<1>(f), bf16_hi(x01), acc);
+    acc = fmaf(s8_to_f32<2>(f), bf16_lo(x23), acc);
+    acc = fmaf(s8_to_f32<3>(f), bf16_hi(x23), acc);
+  }
+  __device__ static __forceinline__ void dot1(float &acc, const uint4 &a, const uint4 *xv) {
+    word1(acc, a.x, xv[0].x, xv[0].y);
+    word1(acc, a.y, xv[0].z, xv[0].w);
+    word1(acc, a.z, xv[1].x, xv[1].y);
+    word1(acc, a.w, xv[1].z, xv[1].w);
+  }
+  // the same magic-number decode, two weights per packed subtraction
+  __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
+    const uint32_t u = w == 0 ? a.x : w == 1 ? a.y : w == 2 ? a.z : a.w;
+    const uint32_t f = u ^ 0x80808080u;
+    const float2 mg = make_float2(-8388736.0f, -8388736.0f);
+    q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7540)),
+                                 __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7541))), mg);
+    q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7542)),
+                                 __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7543))), mg);
+  }
+  __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(p);
+    q[0] = bf16_lo(v.x); q[1] = bf16_hi(v.x); q[2] = bf16_lo(v.y); q[3] = bf16_hi(v.y);
   }
   __device__ static __forceinline__ float a_elem(const void *A, int64_t i) {
     return (float)__ldg(reinterpret_cast<const signed char *>(A) + i);
@@ -372,41 +471,39 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
   }
 }
 
-// ------------------------------------------------------------------ k_batched
-// x[0..B) (B*K elements, a multiple of 16 bytes) is copied once per CTA into
-// shared memory with cp.async; warps then stream R rows at a time, each lane
-// taking 16-byte chunks 32 apart, so every x chunk read from shared memory feeds
-// R rows.  Requires B*K*sizeof(TX) <= the dynamic shared memory given.
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-
-template <class Op, int NB, int R>
-__global__ void __launch_bounds__(kThreads) k_batched(const Args a) {
+// ------------------------------------------------------------------ k_batched2
+// 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored; each
+// warp streams R rows at a time with U chunks per row in flight per lane; every x
+// chunk read from shared memory feeds R rows.  One fp32 accumulator per
+// (row, vector); mixed-precision FMAs (16-bit operands, fp32 accumulator) for the
+// 16-bit types.
+template <class Op, int NB, int R, int U, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
+  constexpr int WARPS = THREADS / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t M = a.M, K = a.K;
   const int B = a.B;
-  constexpr int XB = Op::XCH * 16;
-  const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);  // bytes per x vector
+  constexpr int XB = Op::XCH * 16;  // smem bytes of x per A chunk
+  const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
   {
     const int64_t n16 = (xstride * B) / 16;
     const char *src = reinterpret_cast<const char *>(a.x);
-    for (int64_t i = tid; i < n16; i += kThreads) cp_async16(xs + i * 16, src + i * 16);
+    for (int64_t i = tid; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     __syncthreads();
   }
   const uint64_t pol = evict_first_policy();
   const int64_t nch = K / Op::VEC;
-  const int64_t rows_per_pass = (int64_t)gridDim.x * kWarps * R;
-
-  for (int64_t r0 = ((int64_t)blockIdx.x * kWarps + warp) * R; r0 < M; r0 += rows_per_pass) {
-    float e[R][NB], o[R][NB];
+  const int64_t groups = (M + R - 1) / R;
+  // row groups of R rows dealt to CTAs round-robin: every SM gets an equal share
+  for (int64_t g = blockIdx.x + (int64_t)gridDim.x * warp; g < groups; g += (int64_t)gridDim.x * WARPS) {
+    const int64_t r0 = g * R;
+    float acc[R][NB];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) e[r][b] = o[r][b] = 0.f;
+      for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
     const char *arow[R];
     bool live[R];
 #pragma unroll
@@ -415,19 +512,30 @@ __global__ void __launch_bounds__(kThreads) k_batched(const Args a) {
       arow[r] = reinterpret_cast<const char *>(a.A) +
                 (live[r] ? r0 + r : r0) * K * (int64_t)sizeof(typename Op::TA);
     }
-    for (int64_t c = lane; c < nch; c += 32) {
-      uint4 av[R];
+    for (int64_t c0 = lane; c0 < nch; c0 += 32 * U) {
+      uint4 av[U][R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) av[r] = live[r] ? ld_stream16(arow[r] + c * 16, pol) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + 32 * u;
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (b < B) {
-          uint4 xv[Op::XCH];
+        for (int r = 0; r < R; ++r)
+          av[u][r] = (live[r] && c < nch) ? ld_stream16(arow[r] + c * 16, pol) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-          for (int h = 0; h < Op::XCH; ++h)
-            xv[h] = *reinterpret_cast<const uint4 *>(xs + b * xstride + c * XB + h * 16);
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + 32 * u;
+        if (c < nch) {
 #pragma unroll
-          for (int r = 0; r < R; ++r) Op::dot(e[r][b], o[r][b], av[r], xv);
+          for (int b = 0; b < NB; ++b) {
+            if (b < B) {
+              const unsigned char *xp = xs + b * xstride + c * XB;
+              uint4 xv[Op::XCH];
+#pragma unroll
+              for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
+#pragma unroll
+              for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], av[u][r], xv);
+            }
+          }
         }
       }
     }
@@ -435,10 +543,201 @@ __global__ void __launch_bounds__(kThreads) k_batched(const Args a) {
     for (int r = 0; r < R; ++r) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        const float s = group_sum<32>(e[r][b] + o[r][b]);
+        const float s = group_sum<32>(acc[r][b]);
         if (lane == 0 && b < B && live[r]) epilogue_store<Op>(a, b, r0 + r, s);
       }
     }
+  }
+}
+
+// ------------------------------------------------------------------ k_stream
+// B = 1, rows of at least one chunk per lane: persistent warps, one row at a time
+// per warp, U chunks per lane in flight, double-buffered across row boundaries
+// (the next row's first loads are issued before the current row is reduced), so
+// a warp never waits on an empty pipeline between rows.  Rows are dealt to CTAs
+// round-robin so that every SM gets an equal share.  x is read through L1, or
+// from shared memory (XS) where the CTA copies it once.
+template <class Op, int U, int THREADS, bool XS>
+__global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
+  extern __shared__ __align__(16) unsigned char xs[];
+  constexpr int WARPS = THREADS / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t M = a.M, K = a.K;
+  constexpr int XB = Op::XCH * 16;
+  if (XS) {
+    const int64_t n16 = K * (int64_t)sizeof(typename Op::TX) / 16;
+    const char *src = reinterpret_cast<const char *>(a.x);
+    for (int64_t i = threadIdx.x; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
+  const unsigned char *xb = XS ? xs : reinterpret_cast<const unsigned char *>(a.x);
+  const uint64_t pol = evict_first_policy();
+  const int64_t nch = K / Op::VEC;
+  const int64_t rstride = (int64_t)gridDim.x * WARPS;
+  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const char *A = reinterpret_cast<const char *>(a.A);
+
+  // `row` and `base` (first chunk of the current load group) are the same in all
+  // lanes of a warp, so every lane leaves a row at the same step.
+  int64_t row = blockIdx.x + (int64_t)gridDim.x * warp;
+  int64_t base = 0;
+  uint4 buf[U];
+  // prologue: first group of the first row
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t c = base + lane + 32 * u;
+    buf[u] = (row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+  }
+  while (row < M) {
+    float e = 0.f, o = 0.f;
+    for (;;) {
+      uint4 cur[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = buf[u];
+      const int64_t cc = base + lane;
+      // next group: same row, or the first group of this warp's next row
+      int64_t nrow = row;
+      base += 32 * U;
+      if (base >= nch) { nrow = row + rstride; base = 0; }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = base + lane + 32 * u;
+        buf[u] = (nrow < M && c < nch) ? ld_stream16(A + nrow * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = cc + 32 * u;
+        if (c < nch) {
+          uint4 xv[Op::XCH];
+#pragma unroll
+          for (int h = 0; h < Op::XCH; ++h)
+            xv[h] = XS ? *reinterpret_cast<const uint4 *>(xb + c * XB + h * 16) : ld_x16(xb + c * XB + h * 16);
+          Op::dot(e, o, cur[u], xv);
+        }
+      }
+      if (nrow != row) break;
+    }
+    const float s = group_sum<32>(e + o);
+    if (lane == 0) epilogue_store<Op>(a, 0, row, s);
+    row += rstride;
+  }
+}
+
+// ------------------------------------------------------------------ k_batch_lo
+// 2 <= B <= 4 (NB in {1, 2, 4}).  x[0..B) staged once per CTA in shared memory,
+// fp32 when XF32, laid out as [b][quad w][chunk c][4] so that the lanes of a warp
+// (consecutive chunks) read consecutive words: no bank conflicts.  Each warp
+// carries R rows; every A element is widened once and meets all B vectors; every
+// x value feeds R rows.  (even, odd) accumulator pairs take packed FMAs.  The
+// loads of the next chunk group (possibly of the next row group) are in flight
+// while the current one is used, and are issued before x is staged.
+template <class Op, int NB, int R, int THREADS, bool XF32>
+__global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
+  extern __shared__ __align__(16) unsigned char xs[];
+  constexpr int WARPS = THREADS / 32;
+  constexpr int QW = Op::VEC / 4;
+  constexpr int SX = (int)sizeof(typename Op::TX);
+  constexpr int XE = XF32 ? 4 : SX;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  const uint64_t pol = evict_first_policy();
+  const int64_t nch = K / Op::VEC;
+  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const char *A = reinterpret_cast<const char *>(a.A);
+  const int64_t groups = (M + R - 1) / R;
+  const int64_t gstride = (int64_t)gridDim.x * WARPS;
+
+  int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
+  int64_t base = 0;  // same in every lane of the warp
+  uint4 nxt[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t row = g * R + r, c = base + lane;
+    nxt[r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+  }
+  {  // stage x: 4-element groups, [b][w][c][4] (no runtime division)
+    const unsigned char *src = reinterpret_cast<const unsigned char *>(a.x);
+    for (int b = 0; b < B; ++b)
+    for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
+      const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
+      unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
+      const unsigned char *sp = src + ((int64_t)b * K + k0) * SX;
+      if (SX == 4) {
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sp);
+      } else if (XF32) {
+        float q[4];
+        Op::xquad(sp, q);
+        *reinterpret_cast<float4 *>(dst) = make_float4(q[0], q[1], q[2], q[3]);
+      } else {
+        *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(sp);
+      }
+    }
+    __syncthreads();
+  }
+
+  while (g < groups) {
+    float2 acc[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    int64_t ng;
+    for (;;) {
+      uint4 cur[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+      const int64_t cc = base + lane;
+      ng = g;
+      base += 32;
+      if (base >= nch) { ng = g + gstride; base = 0; }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t row = ng * R + r, c = base + lane;
+        nxt[r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+      }
+      if (cc < nch) {
+#pragma unroll
+        for (int w = 0; w < QW; ++w) {
+          float2 q01[R], q23[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) Op::quad2(cur[r], w, q01[r], q23[r]);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (b < B) {
+              const unsigned char *xp = xs + (((b * QW + w) * nch + cc) * 4) * XE;
+              float2 x01, x23;
+              if (XE == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(xp);
+                x01 = make_float2(v.x, v.y);
+                x23 = make_float2(v.z, v.w);
+              } else {
+                float q[4];
+                Op::xquad(xp, q);
+                x01 = make_float2(q[0], q[1]);
+                x23 = make_float2(q[2], q[3]);
+              }
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                acc[r][b] = __ffma2_rn(q01[r], x01, acc[r][b]);
+                acc[r][b] = __ffma2_rn(q23[r], x23, acc[r][b]);
+              }
+            }
+          }
+        }
+      }
+      if (ng != g) break;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const float s = group_sum<32>(acc[r][b].x + acc[r][b].y);
+        if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
+      }
+    }
+    g = ng;
   }
 }
 

@@ -9,9 +9,12 @@
 
 namespace gemv {
 
-// Unroll depth (16-byte chunks in flight per lane before the first is used).
-constexpr int kUnrollWarpRow = 4;
-constexpr int kUnrollBlockRow = 4;
+// Dynamic shared memory above 48 KB has to be allowed per kernel.
+template <typename Kern>
+cudaError_t allow_smem(Kern kern, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
 
 template <class Op, int NB>
 cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
@@ -35,14 +38,44 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
   return cudaSuccess;
 }
 
-template <class Op, int NB, int R>
-cudaError_t launch_batched_r(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
-  auto kern = k_batched<Op, NB, R>;
-  if (p.smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+template <class Op, int NB>
+cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  constexpr int T = kBatchedThreads;
+  const dim3 grid((unsigned)p.grid), block(T);
+  if constexpr (NB <= 4) {
+    // B <= 4: x in shared memory (fp32 where it fits), R = 2 or 4 rows per warp
+    auto run = [&](auto kern) -> cudaError_t {
+      cudaError_t e = allow_smem(kern, p.smem_bytes);
+      if (e != cudaSuccess) return e;
+      kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
+      return cudaSuccess;
+    };
+    const bool f32x = p.x_staging == GEMV_X_SMEM_FP32;
+    if (p.rows_per_warp == 2)
+      return f32x ? run(k_batch_lo<Op, NB, 2, T, true>) : run(k_batch_lo<Op, NB, 2, T, false>);
+    return f32x ? run(k_batch_lo<Op, NB, 4, T, true>) : run(k_batch_lo<Op, NB, 4, T, false>);
+  } else {
+    auto kern = k_batched2<Op, NB, 2, 2, T>;
+    cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
+    kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
+    return cudaSuccess;
   }
-  kern<<<dim3((unsigned)p.grid), dim3(kThreads), (size_t)p.smem_bytes, s>>>(a);
+}
+
+template <class Op>
+cudaError_t launch_stream(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  constexpr int T = kStreamThreads;
+  const dim3 grid((unsigned)p.grid), block(T);
+  if (p.x_staging == GEMV_X_SMEM) {
+    auto kern = p.unroll == 2 ? k_stream<Op, 2, T, true> : k_stream<Op, 4, T, true>;
+    cudaError_t e = allow_smem(kern, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
+  } else {
+    auto kern = p.unroll == 2 ? k_stream<Op, 2, T, false> : k_stream<Op, 4, T, false>;
+    kern<<<grid, block, 0, s>>>(a);
+  }
   return cudaSuccess;
 }
 
@@ -71,8 +104,10 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
       return cudaSuccess;
     }
     case GEMV_KERNEL_BATCHED:
-      if (p.rows_per_warp == 2) return launch_batched_r<Op, NB, 2>(p, a, s);
-      return launch_batched_r<Op, NB, 4>(p, a, s);
+      return launch_batched<Op, NB>(p, a, s);
+    case GEMV_KERNEL_STREAM:
+      if constexpr (NB == 1) return launch_stream<Op>(p, a, s);
+      return cudaErrorInvalidValue;
     default:
       return cudaErrorInvalidValue;
   }

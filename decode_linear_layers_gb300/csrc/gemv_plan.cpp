@@ -7,14 +7,17 @@
 // short rows, a CTA per row for long ones; the NPU MatMul post, sections 1.3 and
 // 3.4, asks for the kernel to be picked from (M, N, K, dtype, hardware) at run time.
 //
-// Rules used here (per call, from dtype, M, K, B, alignment and the SM count):
-//   rows not 16-byte aligned            -> SCALAR (element loads)
-//   row <= 16 chunks of 16 bytes        -> ROWS_PER_WARP, lanes = next pow2 of chunks
-//   B > 1 and x[0..B) fits in smem      -> BATCHED (x staged once per CTA)
-//   at least 16 rows per SM, or <= 4 KB -> WARP_PER_ROW
-//   at least 2 rows per SM              -> BLOCK_PER_ROW
-//   fewer rows                          -> SPLIT_K over enough K slices to give
-//                                          every SM about four CTAs
+// Rules used here (per call, from dtype, M, K, B, alignment and the SM count;
+// the thresholds come from timing every kernel on the GB300 configurations):
+//   rows not 16-byte aligned              -> SCALAR (element loads)
+//   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
+//   B >= 2 and x[0..B) fits in smem       -> BATCHED
+//   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
+//   B == 1 and at least 16 rows per SM    -> STREAM (persistent warps)
+//   at least 16 rows per SM, or <= 4 KB   -> WARP_PER_ROW
+//   at least 2 rows per SM                -> BLOCK_PER_ROW
+//   fewer rows                            -> SPLIT_K over enough K slices to give
+//                                            every SM about four CTAs
 #include <stdint.h>
 
 #include "../../include/gemv.h"
@@ -45,9 +48,14 @@ int elem_bytes_a(int dtype) {
 
 int elem_bytes_x(int dtype) { return dtype == GEMV_DTYPE_F32 ? 4 : 2; }
 
-int rows_per_warp_for(int nb) { return nb >= 16 ? 2 : 4; }
-
 static bool rowteam_lanes_ok(int l) { return l == 1 || l == 2 || l == 4 || l == 8 || l == 16; }
+
+// x staging of the batched kernels: B <= 4 prefers fp32 in shared memory.
+static int batched_staging(int nb, int64_t B, int64_t K, int sx) {
+  if (nb <= 4 && B * K * 4 <= kBatchedSmemMax) return GEMV_X_SMEM_FP32;
+  if (B * K * sx <= kBatchedSmemMax) return GEMV_X_SMEM;
+  return -1;
+}
 
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out) {
@@ -67,8 +75,8 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   const int vec = 16 / sa;
   const bool vec_ok = aligned16 && (K % vec == 0);
   const int64_t nch = vec_ok ? K / vec : 0;
-  const int64_t xbytes = (int64_t)B * K * sx;
   p.nb = next_pow2(B);
+  const int bstage = batched_staging(p.nb, B, K, sx);
 
   int kernel = GEMV_KERNEL_AUTO;
   int param = 0;
@@ -86,8 +94,11 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         ok = vec_ok && nch >= 2 && force_param >= 0;
         break;
       case GEMV_KERNEL_BATCHED:
-        ok = vec_ok && xbytes <= kBatchedSmemMax &&
-             (force_param == 0 || force_param == 2 || force_param == 4);
+        ok = vec_ok && bstage >= 0 &&
+             (force_param == 0 || force_param == 2 || (force_param == 4 && p.nb <= 4));
+        break;
+      case GEMV_KERNEL_STREAM:
+        ok = vec_ok && B == 1;
         break;
       case GEMV_KERNEL_SCALAR:
         ok = force_param == 0 || force_param == 4 || force_param == 32;
@@ -106,8 +117,12 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       kernel = GEMV_KERNEL_SCALAR;
     } else if (nch <= 16) {
       kernel = GEMV_KERNEL_ROWS_PER_WARP;
-    } else if (B > 1 && xbytes <= kBatchedSmemMax && nch >= 32) {
+    } else if (B > 1 && bstage >= 0 && nch >= 32) {
       kernel = GEMV_KERNEL_BATCHED;
+    } else if (M >= 65536) {
+      kernel = GEMV_KERNEL_WARP_PER_ROW;
+    } else if (B == 1 && M >= (int64_t)num_sms * 16) {
+      kernel = GEMV_KERNEL_STREAM;
     } else if (M >= (int64_t)num_sms * 16 || nch <= kPlanThreads) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;  // many rows, or rows of at most 4 KB
     } else if (M >= (int64_t)num_sms * 2 || nch < 2 * kPlanThreads) {
@@ -118,6 +133,8 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   }
 
   p.kernel = kernel;
+  p.unroll = 1;
+  p.x_staging = GEMV_X_GLOBAL;
   switch (kernel) {
     case GEMV_KERNEL_ROWS_PER_WARP: {
       int lanes = param != 0 ? param : next_pow2(nch < 1 ? 1 : nch);
@@ -129,6 +146,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
     }
     case GEMV_KERNEL_WARP_PER_ROW: {
       p.lanes_per_row = 32;
+      p.unroll = kUnrollWarpRow;
       const int64_t groups = ceil_div(M, kPlanThreads / 32);
       p.grid = groups < (int64_t)num_sms * 32 ? groups : (int64_t)num_sms * 32;
       break;
@@ -141,6 +159,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       break;
     }
     case GEMV_KERNEL_BLOCK_PER_ROW: {
+      p.unroll = kUnrollBlockRow;
       p.grid = M < (int64_t)num_sms * 16 ? M : (int64_t)num_sms * 16;
       break;
     }
@@ -157,21 +176,38 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       const int64_t per = ceil_div(nch, s);
       s = ceil_div(nch, per);  // no empty slices
       p.splits = (int)s;
+      p.unroll = kUnrollBlockRow;
       p.grid = M < (int64_t)num_sms * 16 ? M : (int64_t)num_sms * 16;
       p.workspace_bytes = s * (int64_t)B * M * 4;
       break;
     }
     case GEMV_KERNEL_BATCHED: {
-      const int r = param != 0 ? param : rows_per_warp_for(p.nb);
+      // x is staged once per CTA, so the grid is persistent: one 512-thread CTA
+      // per SM; each warp carries R rows.
+      int r = param != 0 ? param : (p.nb <= 4 ? 4 : 2);
+      if (p.nb > 4) r = 2;
       p.rows_per_warp = r;
-      p.smem_bytes = (int)xbytes;
-      const int64_t groups = ceil_div(M, (int64_t)(kPlanThreads / 32) * r);
-      // x is staged once per CTA, so the grid is persistent: a few CTAs per SM.
-      int64_t per_sm = (int64_t)(kSmemPerSm / (xbytes + 1024));
-      if (per_sm < 1) per_sm = 1;
-      if (per_sm > 2) per_sm = 2;
-      const int64_t cap = per_sm * num_sms;
-      p.grid = groups < cap ? groups : cap;
+      p.threads = kBatchedThreads;
+      p.x_staging = p.nb <= 4 ? bstage : GEMV_X_SMEM;
+      p.unroll = p.nb <= 4 ? 1 : 2;
+      p.smem_bytes = (int)((int64_t)B * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
+      p.grid = num_sms;
+      break;
+    }
+    case GEMV_KERNEL_STREAM: {
+      // fp32 rows: x through L1, four CTAs per SM; 16-bit and int8 rows: x in
+      // shared memory (when it fits in 96 KB), two CTAs per SM, deeper unroll.
+      p.lanes_per_row = 32;
+      p.rows_per_warp = 1;
+      p.threads = kStreamThreads;
+      const bool f32 = dtype == GEMV_DTYPE_F32;
+      p.unroll = f32 ? 2 : 4;
+      p.x_staging = (!f32 && K * sx <= kStreamSmemMax) ? GEMV_X_SMEM : GEMV_X_GLOBAL;
+      p.smem_bytes = p.x_staging == GEMV_X_SMEM ? (int)(K * sx) : 0;
+      // Every CTA of the persistent grid is launched even when M needs fewer warps:
+      // rows are dealt to CTAs round-robin, so each SM gets an equal share.
+      const int64_t per_sm = f32 ? 4 : 2;
+      p.grid = per_sm * num_sms;
       break;
     }
     default:

@@ -13,10 +13,16 @@ constexpr int kPlanThreads = 256;
 constexpr int64_t kBatchedSmemMax = 200 * 1024;
 // Shared memory one SM can give to resident CTAs (sm_100-class: 228 KB).
 constexpr int64_t kSmemPerSm = 228 * 1024;
+// Largest x the streaming kernel copies into shared memory.
+constexpr int64_t kStreamSmemMax = 96 * 1024;
+constexpr int kBatchedThreads = 512;
+constexpr int kStreamThreads = 512;
+// 16-byte chunks in flight per lane: warp-per-row and block-per-row kernels.
+constexpr int kUnrollWarpRow = 4;
+constexpr int kUnrollBlockRow = 4;
 
 int elem_bytes_a(int dtype);
 int elem_bytes_x(int dtype);
-int rows_per_warp_for(int nb);
 
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out);

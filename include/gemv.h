@@ -124,15 +124,24 @@ typedef enum gemv_kernel {
   GEMV_KERNEL_WARP_PER_ROW = 2,  /* one warp per row, 16-byte coalesced loads */
   GEMV_KERNEL_BLOCK_PER_ROW = 3, /* one CTA per row, shared-memory reduction */
   GEMV_KERNEL_SPLIT_K = 4,       /* CTAs over K slices + fixed-order second pass */
-  GEMV_KERNEL_BATCHED = 5,       /* x[0..B) staged in shared memory, R rows per warp */
-  GEMV_KERNEL_SCALAR = 6         /* element loads, for rows that are not 16-byte aligned */
+  GEMV_KERNEL_BATCHED = 5,       /* B >= 2: x[0..B) in shared memory, R rows per warp */
+  GEMV_KERNEL_SCALAR = 6,        /* element loads, for rows that are not 16-byte aligned */
+  GEMV_KERNEL_STREAM = 7         /* B == 1: persistent warps, one row at a time per warp,
+                                    loads double-buffered across rows, x in shared memory */
 } gemv_kernel_t;
+
+/* Where a kernel reads x from (gemv_plan_t.x_staging). */
+#define GEMV_X_GLOBAL 0      /* through L1, from the caller's buffer */
+#define GEMV_X_SMEM 1        /* copied once per CTA into shared memory as stored */
+#define GEMV_X_SMEM_FP32 2   /* widened once per CTA into shared memory as fp32 */
 
 typedef struct gemv_plan {
   int kernel;              /* gemv_kernel_t */
   int lanes_per_row;       /* ROWS_PER_WARP / WARP_PER_ROW / SCALAR: threads per row */
   int rows_per_warp;       /* BATCHED: rows one warp carries at once */
   int splits;              /* SPLIT_K: number of K slices (1 otherwise) */
+  int unroll;              /* 16-byte chunks of A in flight per lane per step */
+  int x_staging;           /* GEMV_X_GLOBAL / GEMV_X_SMEM / GEMV_X_SMEM_FP32 */
   int nb;                  /* vector count the kernel is built for (>= B, power of 2) */
   int threads;             /* threads per CTA */
   int64_t grid;            /* CTAs of the first (or only) kernel */
@@ -150,7 +159,9 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
 
 /* TEST ONLY — not thread-safe.  Make every later call use `kernel` with `param`
  * (lanes_per_row, rows_per_warp or splits; 0 = the dispatcher's choice) when the
- * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  A forced kernel
+ * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  STREAM needs
+ * B == 1; BATCHED needs x[0..B) to fit in shared memory and takes rows_per_warp
+ * 2 or 4 for B <= 4 and 2 for B > 4.  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);

@@ -136,15 +136,42 @@ def test_plan_config_shapes():
     assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 4
     p = g.plan_for("f32", 16384, 32, 1)
     assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 8
-    assert g.plan_for("f32", 16384, 4096, 1)["kernel"] == K["warp_per_row"]
-    assert g.plan_for("f16", 4096, 4096, 1)["kernel"] == K["warp_per_row"]
+    p = g.plan_for("f32", 16384, 4096, 1)
+    assert p["kernel"] == K["stream"] and p["unroll"] == 2 and p["x_staging"] == 0
+    assert p["threads"] == 512 and p["grid"] == 4 * 152
+    p = g.plan_for("f16", 4096, 4096, 1)
+    assert p["kernel"] == K["stream"] and p["unroll"] == 4 and p["x_staging"] == 1
+    assert p["smem_bytes"] == 4096 * 2 and p["grid"] == 2 * 152
     p = g.plan_for("f16", 4096, 4096, 16)
-    assert p["kernel"] == K["batched"] and p["nb"] == 16 and p["smem_bytes"] == 16 * 4096 * 2
-    for M, Kd in ((14336, 4096), (4096, 14336), (128256, 4096)):
-        assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["warp_per_row"]
-    assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["warp_per_row"]
+    assert p["kernel"] == K["batched"] and p["nb"] == 16 and p["x_staging"] == 1
+    assert p["smem_bytes"] == 16 * 4096 * 2 and p["rows_per_warp"] == 2 and p["grid"] == 152
+    for M, Kd in ((14336, 4096), (4096, 14336)):
+        assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["stream"]
+    p = g.plan_for("bf16", 128256, 4096, 1)
+    assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
+    assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["stream"]
     p = g.plan_for("w8", 8192, 8192, 4)
-    assert p["kernel"] == K["batched"] and p["smem_bytes"] == 4 * 8192 * 2
+    assert p["kernel"] == K["batched"] and p["x_staging"] == 2 and p["rows_per_warp"] == 4
+    assert p["smem_bytes"] == 4 * 8192 * 4
+
+
+def test_plan_stream_needs_one_vector():
+    # more than one vector never goes to the one-row streaming kernel
+    for B in range(2, 17):
+        assert g.plan_for("bf16", 8192, 32768, B)["kernel"] != g.KERNELS["stream"]
+    # x larger than the streaming kernel's shared-memory budget is read through L1
+    p = g.plan_for("bf16", 8192, 65536, 1)
+    assert p["kernel"] == g.KERNELS["stream"] and p["x_staging"] == 0 and p["smem_bytes"] == 0
+
+
+def test_plan_batched_staging():
+    # fp32 x in shared memory for B <= 4 when it fits, as stored when only that fits
+    p = g.plan_for("bf16", 4096, 8192, 4)
+    assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4
+    p = g.plan_for("bf16", 4096, 16384, 4)
+    assert p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2
+    p = g.plan_for("bf16", 4096, 4096, 8)
+    assert p["x_staging"] == 1 and p["rows_per_warp"] == 2
 
 
 def test_plan_small_k_lanes():

@@ -52,7 +52,23 @@ SHAPES = [  # (M, K) with several tiles and ragged tails for each kernel family
 ]
 FORCED = [("rows_per_warp", 0), ("rows_per_warp", 1), ("rows_per_warp", 16),
           ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0), ("split_k", 3),
-          ("split_k", 7), ("batched", 2), ("batched", 4), ("scalar", 4), ("scalar", 32)]
+          ("split_k", 7), ("batched", 2), ("batched", 4), ("scalar", 4), ("scalar", 32),
+          ("stream", 0)]
+
+
+def forced_feasible(dtype, kernel, param, K, B):
+    """Mirror of the dispatcher's rules for honouring a forced kernel."""
+    sa = {"f32": 4, "f16": 2, "bf16": 2, "w8": 1}[dtype]
+    sx = 4 if dtype == "f32" else 2
+    nb = 1 << (B - 1).bit_length()
+    if kernel == "batched":
+        fits = (nb <= 4 and B * K * 4 <= 200 * 1024) or B * K * sx <= 200 * 1024
+        return fits and (param in (0, 2) or (param == 4 and nb <= 4))
+    if kernel == "split_k":
+        return K * sa // 16 >= 2
+    if kernel == "stream":
+        return B == 1
+    return True
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
@@ -75,10 +91,7 @@ def test_forced_kernel(dtype, kernel, param):
             y = U.run_gpu(dtype, d, M, K, B)
             plan = g.last_plan()
             g.force_kernel("auto")
-            sa = {"f32": 4, "f16": 2, "bf16": 2, "w8": 1}[dtype]
-            feasible = {"batched": B * K * (4 if dtype == "f32" else 2) <= 200 * 1024,
-                        "split_k": K * sa // 16 >= 2}.get(kernel, True)
-            if feasible:
+            if forced_feasible(dtype, kernel, param, K, B):
                 assert plan["kernel"] == g.KERNELS[kernel], (plan, kernel)
             U.assert_close(dtype, y, y_ref, absdot, with_rounding=True,
                            what=f"{dtype} {kernel}/{param} M={M} K={K} B={B} bias={bias}")
@@ -127,9 +140,10 @@ def test_unaligned_rows(dtype):
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
 def test_guard_bytes_untouched(dtype):
-    for kernel, param in (("auto", 0), ("split_k", 4), ("batched", 4), ("block_per_row", 0),
-                          ("rows_per_warp", 2), ("scalar", 32)):
-        M, K, B = 333, 256, 4
+    for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("batched", 4, 4), ("batched", 2, 9),
+                             ("block_per_row", 0, 4), ("rows_per_warp", 2, 4), ("scalar", 32, 4),
+                             ("stream", 0, 1), ("warp_per_row", 0, 3)):
+        M, K = 333, 256
         w = W.small(dtype, M, K, B, False, seed=400)
         d = U.to_device(W.make_inputs(w))
         n = B * M
@@ -219,9 +233,10 @@ def test_non_default_stream_and_launch_count():
 def test_exact_closed_forms_on_gpu(dtype):
     # A = 1, x = 1 gives y = K exactly (times the w8 scale) in every kernel family
     xk = P.xkind(dtype)
-    for kernel, param in (("auto", 0), ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 5),
-                          ("batched", 2), ("scalar", 32)):
-        M, K, B = 96, 4096, 2
+    for kernel, param, B in (("auto", 0, 2), ("warp_per_row", 0, 2), ("block_per_row", 0, 2),
+                             ("split_k", 5, 2), ("batched", 2, 2), ("batched", 2, 12), ("scalar", 32, 2),
+                             ("stream", 0, 1)):
+        M, K = 96, 4096
         A = torch.ones(M, K, dtype=torch.int8 if dtype == "w8" else U.out_dtype(dtype))
         x = torch.ones(B, K, dtype=U.out_dtype(xk if dtype != "w8" else "bf16"))
         scale = torch.full((M,), 0.5) if dtype == "w8" else None
