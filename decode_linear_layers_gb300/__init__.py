@@ -22,7 +22,7 @@ import os
 from .build import LIB as LIB_PATH, build
 
 __all__ = [
-    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "GemvError", "Plan", "plan_for",
+    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_bf16_splitk_noalloc", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
     "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH",
 ]
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             f.restype = ci
         L.gemv_w8.argtypes = [vp, vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_w8.restype = ci
+        L.gemv_bf16_splitk_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, ci, vp]
+        L.gemv_bf16_splitk_noalloc.restype = ci
         L.gemv_status_string.argtypes = [ci]
         L.gemv_status_string.restype = ctypes.c_char_p
         L.gemv_last_cuda_error.argtypes = []
@@ -197,3 +199,15 @@ def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
     args = (_addr(A, 1, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, 2, nx, "x"),
             _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
     _check(lib().gemv_w8(*args, M, K, B, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
+
+
+def gemv_bf16_splitk_noalloc(A, x, bias, y, M, K, B, stream=None) -> None:
+    """gemv_bf16 on the split-K path with its partial sums in the library's fixed
+    device array (no device allocation).  For callers that cannot allocate while
+    they run; calls that overlap on the GPU race on the shared array.  Raises
+    GemvError(GEMV_ERR_UNSUPPORTED) when splits x B x M x 4 bytes exceed
+    NOALLOC_SCRATCH_BYTES or the rows are not 16-byte aligned."""
+    _float_gemv("gemv_bf16_splitk_noalloc", 2, A, x, bias, y, M, K, B, stream)

@@ -131,6 +131,13 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
 
 }  // namespace
 
+namespace gemv {
+// For other entry points of the library (gemv_noalloc.cu): keep the per-thread
+// CUDA error and the launch counter in one place.
+void record_cuda_error(int e) { t_last_cuda_error = e; }
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace gemv
+
 extern "C" {
 
 gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float *y, int64_t M,

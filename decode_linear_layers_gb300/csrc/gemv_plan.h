@@ -24,6 +24,10 @@ constexpr int kUnrollBlockRow = 4;
 int elem_bytes_a(int dtype);
 int elem_bytes_x(int dtype);
 
+// Defined in gemv_api.cu.
+void record_cuda_error(int e);
+void count_launches(int n);
+
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out);
 

@@ -103,6 +103,26 @@ gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x
                       const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
                       gemv_stream_t stream);
 
+/* bf16 GEMV that allocates nothing.  The source pages have no counterpart: this is
+ * a service for callers that cannot allocate device memory while they run (memory
+ * reserved up front by their own allocator, real-time loops where an allocation
+ * could block or fail, hosts that forbid the CUDA allocator).  Same arguments and
+ * result as gemv_bf16, computed on the split-K path, whose partial sums live in a
+ * fixed device array of GEMV_NOALLOC_SCRATCH_BYTES inside the library (held on
+ * every GPU that loads the library until the process exits) instead of the
+ * stream-ordered pool.
+ *   - GEMV_ERR_UNSUPPORTED when the partial sums (splits x B x M x 4 bytes) would
+ *     not fit in that array, or when the split-K path cannot run (rows not 16-byte
+ *     aligned, fewer than two 16-byte chunks per row); nothing is launched then.
+ *   - All calls share the one array: calls whose kernels overlap on the GPU race
+ *     and give wrong results; order them on one stream.
+ *   - The first call on each device looks up the array's address (cudaGetSymbolAddress
+ *     with that device current); make it before any stream capture. */
+#define GEMV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+gemv_status_t gemv_bf16_splitk_noalloc(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
+                                       uint16_t *y, int64_t M, int64_t K, int B,
+                                       gemv_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gemv_status_string(gemv_status_t status);
 
