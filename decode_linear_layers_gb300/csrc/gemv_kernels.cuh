@@ -164,6 +164,13 @@ struct OpBF16 {
     q01 = make_float2(bf16_lo(u0), bf16_hi(u0));
     q23 = make_float2(bf16_lo(u1), bf16_hi(u1));
   }
+  // 8 x values (16 bytes of bf16) as 4 fp32 pairs.
+  __device__ static __forceinline__ void xpairs8(const uint4 &v, float2 (&p)[4]) {
+    p[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+    p[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    p[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+    p[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+  }
   // 4 bf16 x values (8 bytes at p) as fp32.
   __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
     const uint2 v = *reinterpret_cast<const uint2 *>(p);
@@ -212,6 +219,13 @@ struct OpF16 {
   __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
     q01 = f16x2_to_f2(w ? a.z : a.x);
     q23 = f16x2_to_f2(w ? a.w : a.y);
+  }
+  // 8 x values (16 bytes of fp16) as 4 fp32 pairs.
+  __device__ static __forceinline__ void xpairs8(const uint4 &v, float2 (&p)[4]) {
+    p[0] = f16x2_to_f2(v.x);
+    p[1] = f16x2_to_f2(v.y);
+    p[2] = f16x2_to_f2(v.z);
+    p[3] = f16x2_to_f2(v.w);
   }
   __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
     const uint2 v = *reinterpret_cast<const uint2 *>(p);
@@ -272,6 +286,13 @@ struct OpW8 {
     q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7542)),
                                  __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7543))), mg);
   }
+  // 8 x values (16 bytes of bf16) as 4 fp32 pairs.
+  __device__ static __forceinline__ void xpairs8(const uint4 &v, float2 (&p)[4]) {
+    p[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+    p[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    p[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+    p[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+  }
   __device__ static __forceinline__ void xquad(const unsigned char *p, float (&q)[4]) {
     const uint2 v = *reinterpret_cast<const uint2 *>(p);
     q[0] = bf16_lo(v.x); q[1] = bf16_hi(v.x); q[2] = bf16_lo(v.y); q[3] = bf16_hi(v.y);
@@ -317,9 +338,9 @@ __device__ __forceinline__ float group_sum(float v) {
 // groups.  Lanes of a row take 16-byte chunks TPR apart (so a warp's loads are
 // contiguous), U chunks issued before any is consumed.  All 32 lanes of a warp
 // reach the butterfly, with rows past M contributing zeros.
-template <class Op, int TPR, int NB, int U, bool VEC>
-__global__ void __launch_bounds__(kThreads) k_rowteam(const Args a) {
-  constexpr int TEAMS = kThreads / TPR;
+template <class Op, int TPR, int NB, int U, bool VEC, int THREADS = kThreads>
+__global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
+  constexpr int TEAMS = THREADS / TPR;
   const int sub = threadIdx.x & (TPR - 1);
   const int team = threadIdx.x / TPR;
   const int64_t M = a.M, K = a.K;
@@ -472,11 +493,12 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
 }
 
 // ------------------------------------------------------------------ k_batched2
-// 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored; each
-// warp streams R rows at a time with U chunks per row in flight per lane; every x
-// chunk read from shared memory feeds R rows.  One fp32 accumulator per
-// (row, vector); mixed-precision FMAs (16-bit operands, fp32 accumulator) for the
-// 16-bit types.
+// 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored, with
+// vectors B..NB-1 zero, so the inner loops run over all NB vectors without a
+// branch; each warp streams R rows at a time with U chunks per row in flight per
+// lane; every x chunk read from shared memory feeds R rows.  One fp32 accumulator
+// per (row, vector); mixed-precision FMAs (16-bit operands, fp32 accumulator) for
+// the 16-bit types.
 template <class Op, int NB, int R, int U, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
@@ -487,9 +509,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   constexpr int XB = Op::XCH * 16;  // smem bytes of x per A chunk
   const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
   {
-    const int64_t n16 = (xstride * B) / 16;
+    const int64_t n16 = (xstride * B) / 16, nz16 = (xstride * NB) / 16;
     const char *src = reinterpret_cast<const char *>(a.x);
     for (int64_t i = tid; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
+    for (int64_t i = n16 + tid; i < nz16; i += THREADS)
+      reinterpret_cast<uint4 *>(xs)[i] = make_uint4(0, 0, 0, 0);
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     __syncthreads();
   }
@@ -527,14 +551,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
         if (c < nch) {
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
-            if (b < B) {
-              const unsigned char *xp = xs + b * xstride + c * XB;
-              uint4 xv[Op::XCH];
+            const unsigned char *xp = xs + b * xstride + c * XB;
+            uint4 xv[Op::XCH];
 #pragma unroll
-              for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
+            for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
 #pragma unroll
-              for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], av[u][r], xv);
-            }
+            for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], av[u][r], xv);
           }
         }
       }
@@ -627,12 +649,14 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
 // ------------------------------------------------------------------ k_batch_lo
 // 2 <= B <= 4 (NB in {1, 2, 4}).  x[0..B) staged once per CTA in shared memory,
 // fp32 when XF32, laid out as [b][quad w][chunk c][4] so that the lanes of a warp
-// (consecutive chunks) read consecutive words: no bank conflicts.  Each warp
-// carries R rows; every A element is widened once and meets all B vectors; every
-// x value feeds R rows.  (even, odd) accumulator pairs take packed FMAs.  The
-// loads of the next chunk group (possibly of the next row group) are in flight
-// while the current one is used, and are issued before x is staged.
-template <class Op, int NB, int R, int THREADS, bool XF32>
+// (consecutive chunks) read consecutive words: no bank conflicts.  Vectors
+// B..NB-1 are zero, so the inner loops run over all NB vectors without a branch.  Each warp
+// carries R rows and takes U chunks of each per step; every A element is widened
+// once and meets all B vectors; every x value feeds R rows.  (even, odd)
+// accumulator pairs take packed FMAs.  The next step's loads (possibly of the next
+// row group) are in flight while the current step is used, and the first ones are
+// issued before x is staged.
+template <class Op, int NB, int R, int U, int THREADS, bool XF32>
 __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
@@ -650,30 +674,40 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
   const int64_t gstride = (int64_t)gridDim.x * WARPS;
 
   int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
-  int64_t base = 0;  // same in every lane of the warp
-  uint4 nxt[R];
+  int64_t base = 0;  // first chunk of the step, the same in every lane of the warp
+  uint4 nxt[U][R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int64_t row = g * R + r, c = base + lane;
-    nxt[r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
-  }
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t row = g * R + r, c = base + lane + 32 * u;
+      nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
+                                                     : make_uint4(0, 0, 0, 0);
+    }
   {  // stage x: 4-element groups, [b][w][c][4] (no runtime division)
     const unsigned char *src = reinterpret_cast<const unsigned char *>(a.x);
     for (int b = 0; b < B; ++b)
-    for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
-      const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
-      unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
-      const unsigned char *sp = src + ((int64_t)b * K + k0) * SX;
-      if (SX == 4) {
-        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sp);
-      } else if (XF32) {
-        float q[4];
-        Op::xquad(sp, q);
-        *reinterpret_cast<float4 *>(dst) = make_float4(q[0], q[1], q[2], q[3]);
-      } else {
-        *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(sp);
+      for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
+        const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
+        unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
+        const unsigned char *sp = src + ((int64_t)b * K + k0) * SX;
+        if (SX == 4) {
+          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sp);
+        } else if (XF32) {
+          float q[4];
+          Op::xquad(sp, q);
+          *reinterpret_cast<float4 *>(dst) = make_float4(q[0], q[1], q[2], q[3]);
+        } else {
+          *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(sp);
+        }
       }
-    }
+    for (int b = B; b < NB; ++b)
+      for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
+        const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
+        unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
+        if (XE == 4) *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        else *reinterpret_cast<uint2 *>(dst) = make_uint2(0, 0);
+      }
     __syncthreads();
   }
 
@@ -685,28 +719,35 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
       for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
     int64_t ng;
     for (;;) {
-      uint4 cur[R];
+      uint4 cur[U][R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) cur[r] = nxt[r];
-      const int64_t cc = base + lane;
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int r = 0; r < R; ++r) cur[u][r] = nxt[u][r];
+      const int64_t cb = base + lane;
       ng = g;
-      base += 32;
+      base += 32 * U;
       if (base >= nch) { ng = g + gstride; base = 0; }
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int64_t row = ng * R + r, c = base + lane;
-        nxt[r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
-      }
-      if (cc < nch) {
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int w = 0; w < QW; ++w) {
-          float2 q01[R], q23[R];
+        for (int r = 0; r < R; ++r) {
+          const int64_t row = ng * R + r, c = base + lane + 32 * u;
+          nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
+                                                          : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-          for (int r = 0; r < R; ++r) Op::quad2(cur[r], w, q01[r], q23[r]);
+      for (int u = 0; u < U; ++u) {
+        const int64_t cc = cb + 32 * u;
+        if (cc < nch) {
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (b < B) {
-              const unsigned char *xp = xs + (((b * QW + w) * nch + cc) * 4) * XE;
+          for (int w = 0; w < QW; ++w) {
+            float2 q01[R], q23[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) Op::quad2(cur[u][r], w, q01[r], q23[r]);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              const unsigned char *xp = xs + ((((int64_t)b * QW + w) * nch + cc) * 4) * XE;
               float2 x01, x23;
               if (XE == 4) {
                 const float4 v = *reinterpret_cast<const float4 *>(xp);

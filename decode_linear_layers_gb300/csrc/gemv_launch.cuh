@@ -50,10 +50,11 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
       kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
       return cudaSuccess;
     };
+    // R = 2 rows per warp with U = 2 chunks per step, or R = 4 with U = 1
     const bool f32x = p.x_staging == GEMV_X_SMEM_FP32;
     if (p.rows_per_warp == 2)
-      return f32x ? run(k_batch_lo<Op, NB, 2, T, true>) : run(k_batch_lo<Op, NB, 2, T, false>);
-    return f32x ? run(k_batch_lo<Op, NB, 4, T, true>) : run(k_batch_lo<Op, NB, 4, T, false>);
+      return f32x ? run(k_batch_lo<Op, NB, 2, 2, T, true>) : run(k_batch_lo<Op, NB, 2, 2, T, false>);
+    return f32x ? run(k_batch_lo<Op, NB, 4, 1, T, true>) : run(k_batch_lo<Op, NB, 4, 1, T, false>);
   } else {
     auto kern = k_batched2<Op, NB, 2, 2, T>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);

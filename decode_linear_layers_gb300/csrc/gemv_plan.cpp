@@ -50,10 +50,11 @@ int elem_bytes_x(int dtype) { return dtype == GEMV_DTYPE_F32 ? 4 : 2; }
 
 static bool rowteam_lanes_ok(int l) { return l == 1 || l == 2 || l == 4 || l == 8 || l == 16; }
 
-// x staging of the batched kernels: B <= 4 prefers fp32 in shared memory.
-static int batched_staging(int nb, int64_t B, int64_t K, int sx) {
-  if (nb <= 4 && B * K * 4 <= kBatchedSmemMax) return GEMV_X_SMEM_FP32;
-  if (B * K * sx <= kBatchedSmemMax) return GEMV_X_SMEM;
+// x staging of the batched kernels (NB vectors, the padded ones zero): B <= 4
+// prefers fp32 in shared memory.
+static int batched_staging(int nb, int64_t K, int sx) {
+  if (nb <= 4 && (int64_t)nb * K * 4 <= kBatchedSmemMax) return GEMV_X_SMEM_FP32;
+  if ((int64_t)nb * K * sx <= kBatchedSmemMax) return GEMV_X_SMEM;
   return -1;
 }
 
@@ -76,7 +77,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   const bool vec_ok = aligned16 && (K % vec == 0);
   const int64_t nch = vec_ok ? K / vec : 0;
   p.nb = next_pow2(B);
-  const int bstage = batched_staging(p.nb, B, K, sx);
+  const int bstage = batched_staging(p.nb, K, sx);
 
   int kernel = GEMV_KERNEL_AUTO;
   int param = 0;
@@ -184,13 +185,14 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
     case GEMV_KERNEL_BATCHED: {
       // x is staged once per CTA, so the grid is persistent: one 512-thread CTA
       // per SM; each warp carries R rows.
-      int r = param != 0 ? param : (p.nb <= 4 ? 4 : 2);
+      // x[0..NB) is staged (vectors B..NB-1 zero): the inner loops have no branch
+      int r = param != 0 ? param : 2;
       if (p.nb > 4) r = 2;
       p.rows_per_warp = r;
       p.threads = kBatchedThreads;
       p.x_staging = p.nb <= 4 ? bstage : GEMV_X_SMEM;
-      p.unroll = p.nb <= 4 ? 1 : 2;
-      p.smem_bytes = (int)((int64_t)B * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
+      p.unroll = r == 4 ? 1 : 2;
+      p.smem_bytes = (int)((int64_t)p.nb * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
       p.grid = num_sms;
       break;
     }

@@ -151,8 +151,8 @@ def test_plan_config_shapes():
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
     assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["stream"]
     p = g.plan_for("w8", 8192, 8192, 4)
-    assert p["kernel"] == K["batched"] and p["x_staging"] == 2 and p["rows_per_warp"] == 4
-    assert p["smem_bytes"] == 4 * 8192 * 4
+    assert p["kernel"] == K["batched"] and p["x_staging"] == 2 and p["rows_per_warp"] == 2
+    assert p["smem_bytes"] == 4 * 8192 * 4 and p["unroll"] == 2
 
 
 def test_plan_stream_needs_one_vector():
@@ -172,6 +172,9 @@ def test_plan_batched_staging():
     assert p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2
     p = g.plan_for("bf16", 4096, 4096, 8)
     assert p["x_staging"] == 1 and p["rows_per_warp"] == 2
+    # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
+    assert g.plan_for("bf16", 4096, 4096, 3)["smem_bytes"] == 4 * 4096 * 4
+    assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
 
 
 def test_plan_small_k_lanes():

@@ -62,7 +62,7 @@ def forced_feasible(dtype, kernel, param, K, B):
     sx = 4 if dtype == "f32" else 2
     nb = 1 << (B - 1).bit_length()
     if kernel == "batched":
-        fits = (nb <= 4 and B * K * 4 <= 200 * 1024) or B * K * sx <= 200 * 1024
+        fits = (nb <= 4 and nb * K * 4 <= 200 * 1024) or nb * K * sx <= 200 * 1024
         return fits and (param in (0, 2) or (param == 4 and nb <= 4))
     if kernel == "split_k":
         return K * sa // 16 >= 2
