@@ -59,6 +59,10 @@ def parse_args(argv=None):
     ap.add_argument("--only", default=None, help="sweep only these comma-separated configs")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-configuration sweep (e.g. under ncu); prints one JSON line")
+    ap.add_argument("--force", default=None,
+                    help="with --sweep-only: run every configuration on this kernel family where it "
+                         "applies (rows_per_warp, warp_per_row, block_per_row, split_k, batched, "
+                         "scalar, stream), through the library's test hook")
     return ap.parse_args(argv)
 
 
@@ -251,8 +255,13 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
 
     if args.sweep_only:
-        if rank == 0:
-            print(json.dumps({"sweep": sweep(args, torch, g, dev, flush, peak)}), flush=True)
+        if args.force:
+            g.force_kernel(args.force)
+        try:
+            if rank == 0:
+                print(json.dumps({"sweep": sweep(args, torch, g, dev, flush, peak)}), flush=True)
+        finally:
+            g.force_kernel("auto")
         return None
 
     head = [W.BY_NAME[n] for n in W.HEADLINE]

@@ -495,10 +495,11 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
 // ------------------------------------------------------------------ k_batched2
 // 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored, with
 // vectors B..NB-1 zero, so the inner loops run over all NB vectors without a
-// branch; each warp streams R rows at a time with U chunks per row in flight per
-// lane; every x chunk read from shared memory feeds R rows.  One fp32 accumulator
-// per (row, vector); mixed-precision FMAs (16-bit operands, fp32 accumulator) for
-// the 16-bit types.
+// branch.  Each warp carries R rows and takes U chunks of each per step; the
+// next step's loads (possibly of the warp's next row group) are in flight while
+// the current step is used.  Every x chunk read from shared memory feeds R rows.
+// One fp32 accumulator per (row, vector); mixed-precision FMAs (16-bit operands,
+// fp32 accumulator) for the 16-bit types.
 template <class Op, int NB, int R, int U, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
@@ -508,6 +509,25 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   const int B = a.B;
   constexpr int XB = Op::XCH * 16;  // smem bytes of x per A chunk
   const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
+  const uint64_t pol = evict_first_policy();
+  const int64_t nch = K / Op::VEC;
+  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const char *A = reinterpret_cast<const char *>(a.A);
+  const int64_t groups = (M + R - 1) / R;
+  const int64_t gstride = (int64_t)gridDim.x * WARPS;
+
+  // row groups of R rows dealt to CTAs round-robin: every SM gets an equal share
+  int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
+  int64_t base = 0;  // first chunk of the step, the same in every lane of the warp
+  uint4 nxt[U][R];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t row = g * R + r, c = base + lane + 32 * u;
+      nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
+                                                     : make_uint4(0, 0, 0, 0);
+    }
   {
     const int64_t n16 = (xstride * B) / 16, nz16 = (xstride * NB) / 16;
     const char *src = reinterpret_cast<const char *>(a.x);
@@ -517,37 +537,35 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     __syncthreads();
   }
-  const uint64_t pol = evict_first_policy();
-  const int64_t nch = K / Op::VEC;
-  const int64_t groups = (M + R - 1) / R;
-  // row groups of R rows dealt to CTAs round-robin: every SM gets an equal share
-  for (int64_t g = blockIdx.x + (int64_t)gridDim.x * warp; g < groups; g += (int64_t)gridDim.x * WARPS) {
-    const int64_t r0 = g * R;
+
+  while (g < groups) {
     float acc[R][NB];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
-    const char *arow[R];
-    bool live[R];
+    int64_t ng;
+    for (;;) {
+      uint4 cur[U][R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      live[r] = (r0 + r) < M;
-      arow[r] = reinterpret_cast<const char *>(a.A) +
-                (live[r] ? r0 + r : r0) * K * (int64_t)sizeof(typename Op::TA);
-    }
-    for (int64_t c0 = lane; c0 < nch; c0 += 32 * U) {
-      uint4 av[U][R];
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int r = 0; r < R; ++r) cur[u][r] = nxt[u][r];
+      const int64_t cb = base + lane;
+      ng = g;
+      base += 32 * U;
+      if (base >= nch) { ng = g + gstride; base = 0; }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int64_t row = ng * R + r, c = base + lane + 32 * u;
+          nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
+                                                          : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + 32 * u;
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          av[u][r] = (live[r] && c < nch) ? ld_stream16(arow[r] + c * 16, pol) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + 32 * u;
+        const int64_t c = cb + 32 * u;
         if (c < nch) {
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
@@ -556,19 +574,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 #pragma unroll
             for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
 #pragma unroll
-            for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], av[u][r], xv);
+            for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], cur[u][r], xv);
           }
         }
       }
+      if (ng != g) break;
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const float s = group_sum<32>(acc[r][b]);
-        if (lane == 0 && b < B && live[r]) epilogue_store<Op>(a, b, r0 + r, s);
+        if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
       }
     }
+    g = ng;
   }
 }
 
