@@ -14,6 +14,8 @@ events on the stream it runs on; the step time is the sum of the three.
                  and y copied back inside the timed region, every step
     cpu_baseline = the CPU oracle on the same step, on the host's cores
     sweep      = every configuration at its full size, timed the same way
+    decode_layer = a Llama-3-8B-shaped bf16 layer's four GEMVs, eager and from a
+                 CUDA graph
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs the same workload on its own GPU (replicas: the
@@ -362,6 +364,7 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_sweep:
         line["sweep"] = sweep(args, torch, g, dev, flush, peak)
+        line["decode_layer"] = decode_layer(args, torch, g, dev, flush, peak)
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(head, host_inputs)
     print(json.dumps(line), flush=True)
@@ -395,6 +398,65 @@ def sweep(args, torch, g, dev, flush, peak):
         del d, y
         torch.cuda.empty_cache()
     return out
+
+
+# A Llama-3-8B-shaped decode layer (bf16, one token): fused QKV, output
+# projection, fused gate+up, down projection.
+DECODE_LAYER = (("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096), ("down", 4096, 14336))
+
+
+def decode_layer(args, torch, g, dev, flush, peak, iters=20):
+    """The layer's four GEMVs back to back, eager and replayed from a CUDA graph.
+
+    L2 is flushed once before each layer (not between its GEMVs); the weights
+    (434 MB) do not fit in L2 anyway."""
+    ws = [W.Workload(f"bf16_{n}", "bf16", M, K, 1, False, ("normal", 0.02), ("normal", 1.0), seed=i)
+          for i, (n, M, K) in enumerate(DECODE_LAYER)]
+    items = []
+    for w in ws:
+        inp = W.make_inputs(w)
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        items.append((w, d, torch.empty((1, w.M), dtype=torch.bfloat16, device=dev)))
+    layer_bytes = sum(w.qmin_bytes for w in ws)
+
+    def run():
+        for (w, d, y) in items:
+            call_gemv(g, w, d, y)
+
+    def timed(fn):
+        out = []
+        for i in range(iters + 3):
+            l2_flush(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                out.append(e0.elapsed_time(e1))
+        return statistics.median(out)
+
+    eager_ms = timed(run)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    n0 = g.launch_count()
+    with torch.cuda.graph(graph):
+        run()
+    launches = g.launch_count() - n0
+    graph_ms = timed(graph.replay)
+    iso = time_gemvs(torch, g, items, flush, iters, 3)
+    iso_ms = sum(statistics.median(t) for t in iso)
+    return {"layer": "bf16 B=1: " + ", ".join(f"{n} {M}x{K}" for n, M, K in DECODE_LAYER),
+            "bytes": layer_bytes, "kernels": launches,
+            "eager_us": round(eager_ms * 1e3, 2), "graph_us": round(graph_ms * 1e3, 2),
+            "isolated_sum_us": round(iso_ms * 1e3, 2),
+            "eager_gbs": round(layer_bytes / (eager_ms * 1e-3) / 1e9, 1),
+            "graph_gbs": round(layer_bytes / (graph_ms * 1e-3) / 1e9, 1),
+            "graph_frac_of_peak": round(layer_bytes / (graph_ms * 1e-3) / 1e9 / peak, 4)}
 
 
 def cpu_baseline(head, host_inputs, budget_s=10.0):
