@@ -22,12 +22,14 @@ import os
 from .build import LIB as LIB_PATH, build
 
 __all__ = [
-    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_bf16_splitk_noalloc", "GemvError", "Plan", "plan_for",
+    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_bf16_splitk_noalloc", "gemv_ex",
+    "gemv_swiglu", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
     "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH",
 ]
 
 SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+ACT_NONE, ACT_SILU = 0, 1
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3}
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
            "split_k": 4, "batched": 5, "scalar": 6, "stream": 7}
@@ -77,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.gemv_w8.restype = ci
         L.gemv_bf16_splitk_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_bf16_splitk_noalloc.restype = ci
+        L.gemv_ex.argtypes = [ci, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, vp]
+        L.gemv_ex.restype = ci
+        L.gemv_swiglu.argtypes = [ci, vp, vp, vp, vp, vp, i64, i64, ci, vp]
+        L.gemv_swiglu.restype = ci
         L.gemv_status_string.argtypes = [ci]
         L.gemv_status_string.restype = ctypes.c_char_p
         L.gemv_last_cuda_error.argtypes = []
@@ -211,3 +217,30 @@ def gemv_bf16_splitk_noalloc(A, x, bias, y, M, K, B, stream=None) -> None:
     GemvError(GEMV_ERR_UNSUPPORTED) when splits x B x M x 4 bytes exceed
     NOALLOC_SCRATCH_BYTES or the rows are not 16-byte aligned."""
     _float_gemv("gemv_bf16_splitk_noalloc", 2, A, x, bias, y, M, K, B, stream)
+
+
+_ESIZE = {"f32": (4, 4), "f16": (2, 2), "bf16": (2, 2), "w8": (1, 2)}   # (A, x/bias/y)
+
+
+def gemv_ex(dtype, A, row_scale, x, bias, residual, y, M, K, B, act=ACT_NONE, stream=None) -> None:
+    """y = act(s_m * sum_k A x + bias) + residual, one launch, any storage type.
+
+    row_scale: w8 only (else None).  residual: (B, M) in y's type, None, or y itself
+    (in place)."""
+    M, K, B, na, nx, ny = _sizes(M, K, B)
+    sa, sx = _ESIZE[dtype]
+    args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, sx, nx, "x"),
+            _addr(bias, sx, M if bias is not None else 0, "bias"),
+            _addr(residual, sx, ny if residual is not None else 0, "residual"), _addr(y, sx, ny, "y"))
+    _check(lib().gemv_ex(DTYPE_CODES[dtype], *args, M, K, B, int(act), _stream(stream)))
+
+
+def gemv_swiglu(dtype, A, row_scale, x, bias, y, I, K, B, stream=None) -> None:
+    """y[b][m] = silu(gate_m) * up_m over A = [gate rows; up rows] (2I x K)."""
+    I, K, B = int(I), int(K), int(B)
+    M2 = 2 * I if I >= 0 else 0
+    sa, sx = _ESIZE[dtype]
+    args = (_addr(A, sa, max(0, M2 * K), "A"), _addr(row_scale, 4, M2, "row_scale"),
+            _addr(x, sx, max(0, B * K), "x"), _addr(bias, sx, M2 if bias is not None else 0, "bias"),
+            _addr(y, sx, max(0, B * I), "y"))
+    _check(lib().gemv_swiglu(DTYPE_CODES[dtype], *args, I, K, B, _stream(stream)))

@@ -67,25 +67,33 @@ gemv_status_t sm_count(int *out) {
 
 typedef cudaError_t (*launch_fn)(const gemv_plan_t &, const gemv::Args &, float *, cudaStream_t);
 
+// M counts the rows of A.  swiglu: y has M / 2 entries per vector (M even).
 gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, const void *bias,
-                  void *y, int64_t M, int64_t K, int B, gemv_stream_t stream_in) {
+                  const void *residual, void *y, int64_t M, int64_t K, int B, int act, bool swiglu,
+                  gemv_stream_t stream_in) {
   if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
+  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W8) return GEMV_ERR_INVALID_VALUE;
+  if (act != GEMV_ACT_NONE && act != GEMV_ACT_SILU) return GEMV_ERR_INVALID_VALUE;
   if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
   if (M == 0 || B == 0) return GEMV_SUCCESS;
   const int sa = gemv::elem_bytes_a(dtype), sx = gemv::elem_bytes_x(dtype);
   const int sy = sx;
+  const int64_t ym = swiglu ? M / 2 : M;  // outputs per vector
   int64_t a_bytes, x_bytes, y_bytes, mk, bk, bm;
   if (!mul_ok(M, K, &mk) || !mul_ok(mk, sa, &a_bytes)) return GEMV_ERR_INVALID_VALUE;
   if (!mul_ok(B, K, &bk) || !mul_ok(bk, sx, &x_bytes)) return GEMV_ERR_INVALID_VALUE;
-  if (!mul_ok(B, M, &bm) || !mul_ok(bm, sy, &y_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (!mul_ok(B, ym, &bm) || !mul_ok(bm, sy, &y_bytes)) return GEMV_ERR_INVALID_VALUE;
   if (y == nullptr) return GEMV_ERR_INVALID_VALUE;
   if (K > 0 && (A == nullptr || x == nullptr)) return GEMV_ERR_INVALID_VALUE;
   if (dtype == GEMV_DTYPE_W8 && scale == nullptr) return GEMV_ERR_INVALID_VALUE;
   if (!aligned(A, sa) || !aligned(x, sx) || !aligned(y, sy) || !aligned(bias, sx) ||
-      !aligned(scale, 4))
+      !aligned(scale, 4) || !aligned(residual, sy))
     return GEMV_ERR_INVALID_VALUE;
   if (overlaps(y, y_bytes, A, a_bytes) || overlaps(y, y_bytes, x, x_bytes) ||
       overlaps(y, y_bytes, bias, M * sx) || overlaps(y, y_bytes, scale, M * 4))
+    return GEMV_ERR_INVALID_VALUE;
+  // the residual may be y itself (in-place y += A x), but not a shifted view of it
+  if (residual != nullptr && residual != y && overlaps(y, y_bytes, residual, y_bytes))
     return GEMV_ERR_INVALID_VALUE;
 
   int sms = 0;
@@ -93,8 +101,17 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   if (st != GEMV_SUCCESS) return st;
   const bool al16 = aligned(A, 16) && aligned(x, 16);
   gemv_plan_t p;
-  st = gemv::plan(dtype, M, K, B, al16, sms, g_force_kernel, g_force_param, &p);
-  if (st != GEMV_SUCCESS) return st;
+  if (swiglu) {
+    // one vector: the streaming kernel walks gate/up row pairs; more: the batched
+    // kernels carry each pair as their R = 2 rows
+    const int want = B == 1 ? GEMV_KERNEL_STREAM : GEMV_KERNEL_BATCHED;
+    st = gemv::plan(dtype, M, K, B, al16, sms, want, B == 1 ? 0 : 2, &p);
+    if (st != GEMV_SUCCESS) return st;
+    if (p.kernel != want) return GEMV_ERR_UNSUPPORTED;
+  } else {
+    st = gemv::plan(dtype, M, K, B, al16, sms, g_force_kernel, g_force_param, &p);
+    if (st != GEMV_SUCCESS) return st;
+  }
 
   gemv::Args args;
   args.A = A;
@@ -105,6 +122,9 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   args.M = M;
   args.K = K;
   args.B = B;
+  args.residual = residual;
+  args.act = act;
+  args.half = swiglu ? M / 2 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_in);
 
   launch_fn fn = dtype == GEMV_DTYPE_F32    ? gemv::launch_f32
@@ -142,23 +162,40 @@ extern "C" {
 
 gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float *y, int64_t M,
                        int64_t K, int B, gemv_stream_t stream) {
-  return run(GEMV_DTYPE_F32, A, nullptr, x, bias, y, M, K, B, stream);
+  return run(GEMV_DTYPE_F32, A, nullptr, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
 }
 
 gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, const uint16_t *bias, uint16_t *y,
                        int64_t M, int64_t K, int B, gemv_stream_t stream) {
-  return run(GEMV_DTYPE_F16, A, nullptr, x, bias, y, M, K, B, stream);
+  return run(GEMV_DTYPE_F16, A, nullptr, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
 }
 
 gemv_status_t gemv_bf16(const uint16_t *A, const uint16_t *x, const uint16_t *bias, uint16_t *y,
                         int64_t M, int64_t K, int B, gemv_stream_t stream) {
-  return run(GEMV_DTYPE_BF16, A, nullptr, x, bias, y, M, K, B, stream);
+  return run(GEMV_DTYPE_BF16, A, nullptr, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
 }
 
 gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x,
                       const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
                       gemv_stream_t stream) {
-  return run(GEMV_DTYPE_W8, A, row_scale, x, bias, y, M, K, B, stream);
+  return run(GEMV_DTYPE_W8, A, row_scale, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
+}
+
+gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
+                      const void *bias, const void *residual, void *y, int64_t M, int64_t K, int B,
+                      gemv_activation_t act, gemv_stream_t stream) {
+  if (dtype != GEMV_DTYPE_W8 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
+  return run((int)dtype, A, row_scale, x, bias, residual, y, M, K, B, (int)act, false, stream);
+}
+
+gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
+                          const void *bias, void *y, int64_t I, int64_t K, int B,
+                          gemv_stream_t stream) {
+  if (I < 0) return GEMV_ERR_INVALID_VALUE;
+  if (dtype != GEMV_DTYPE_W8 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
+  int64_t m2;
+  if (!mul_ok(I, 2, &m2)) return GEMV_ERR_INVALID_VALUE;
+  return run((int)dtype, A, row_scale, x, bias, nullptr, y, m2, K, B, GEMV_ACT_NONE, true, stream);
 }
 
 const char *gemv_status_string(gemv_status_t s) {

@@ -42,6 +42,12 @@ struct Args {
   void *y;
   int64_t M, K;
   int B;
+  // fused epilogue (all kernels): activation, then residual[b][m] (y's type, B x M,
+  // may be y itself).  SwiGLU (half > 0): A is [gate rows 0..half-1; up rows
+  // half..2*half-1], M = 2*half, and y[b][m] = silu(gate_m) * up_m is B x half.
+  const void *residual = nullptr;
+  int act = 0;          // 0: none, 1: SiLU
+  int64_t half = 0;
 };
 
 // ------------------------------------------------------------------ memory access
@@ -314,14 +320,38 @@ __device__ __forceinline__ float bias_at(const void *bias, int64_t m) {
   return Op::x_elem(bias, m);
 }
 
-// y = s_m * acc + bias[m], rounded once to the output type (lesson 3's epilogue:
-// bias added in fp32 after the reduction, NULL allowed).
+// SiLU(v) = v / (1 + e^-v), in fp32 with the CUDA math library's expf.
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
+
+// Row m of vector b before any activation: s_m * acc + bias[m].
 template <class Op>
-__device__ __forceinline__ void epilogue_store(const Args &a, int b, int64_t m, float acc) {
+__device__ __forceinline__ float row_value(const Args &a, int64_t m, float acc) {
   float v = acc;
   if (a.scale != nullptr) v *= __ldg(a.scale + m);
   if (a.bias != nullptr) v += bias_at<Op>(a.bias, m);
-  Op::store(a.y, (int64_t)b * a.M + m, v);
+  return v;
+}
+
+// y = act(s_m * acc + bias[m]) + residual[b][m], rounded once to the output type
+// (lesson 3's epilogue adds the bias in fp32 after the reduction, NULL allowed;
+// the NPU MatMul post, section 5.1, fuses bias, activation and residual into the
+// MatMul instead of separate passes over y).
+template <class Op>
+__device__ __forceinline__ void epilogue_store(const Args &a, int b, int64_t m, float acc) {
+  float v = row_value<Op>(a, m, acc);
+  if (a.act == 1) v = silu(v);
+  const int64_t i = (int64_t)b * a.M + m;
+  if (a.residual != nullptr) v += Op::x_elem(a.residual, i);
+  Op::store(a.y, i, v);
+}
+
+// SwiGLU output m of vector b from the gate row m and the up row m + half.
+template <class Op>
+__device__ __forceinline__ void epilogue_swiglu(const Args &a, int b, int64_t m, float acc_gate,
+                                                float acc_up) {
+  const float g = row_value<Op>(a, m, acc_gate);
+  const float u = row_value<Op>(a, m + a.half, acc_up);
+  Op::store(a.y, (int64_t)b * a.half + m, silu(g) * u);
 }
 
 // Butterfly over WIDTH lanes: every lane of each WIDTH-lane group ends with the
@@ -500,8 +530,9 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
 // the current step is used.  Every x chunk read from shared memory feeds R rows.
 // One fp32 accumulator per (row, vector); mixed-precision FMAs (16-bit operands,
 // fp32 accumulator) for the 16-bit types.
-template <class Op, int NB, int R, int U, int THREADS>
+template <class Op, int NB, int R, int U, int THREADS, bool SW = false>
 __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
+  static_assert(!SW || R == 2, "SwiGLU pairs the gate and up row of one output");
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -513,7 +544,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   const int64_t nch = K / Op::VEC;
   const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
   const char *A = reinterpret_cast<const char *>(a.A);
-  const int64_t groups = (M + R - 1) / R;
+  // row r of group g: g * R + r, or with SW the gate row g and the up row g + half
+  const int64_t groups = SW ? a.half : (M + R - 1) / R;
+  auto row_of = [&](int64_t gg, int r) -> int64_t { return SW ? gg + r * a.half : gg * R + r; };
   const int64_t gstride = (int64_t)gridDim.x * WARPS;
 
   // row groups of R rows dealt to CTAs round-robin: every SM gets an equal share
@@ -524,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   for (int u = 0; u < U; ++u)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int64_t row = g * R + r, c = base + lane + 32 * u;
+      const int64_t row = row_of(g, r), c = base + lane + 32 * u;
       nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
                                                      : make_uint4(0, 0, 0, 0);
     }
@@ -559,7 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const int64_t row = ng * R + r, c = base + lane + 32 * u;
+          const int64_t row = row_of(ng, r), c = base + lane + 32 * u;
           nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
                                                           : make_uint4(0, 0, 0, 0);
         }
@@ -580,12 +613,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       }
       if (ng != g) break;
     }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
+    if constexpr (SW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        const float s = group_sum<32>(acc[r][b]);
-        if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
+        const float s0 = group_sum<32>(acc[0][b]);
+        const float s1 = group_sum<32>(acc[1][b]);
+        if (lane == 0 && b < B) epilogue_swiglu<Op>(a, b, g, s0, s1);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float s = group_sum<32>(acc[r][b]);
+          if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
+        }
       }
     }
     g = ng;
@@ -599,7 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 // a warp never waits on an empty pipeline between rows.  Rows are dealt to CTAs
 // round-robin so that every SM gets an equal share.  x is read through L1, or
 // from shared memory (XS) where the CTA copies it once.
-template <class Op, int U, int THREADS, bool XS>
+template <class Op, int U, int THREADS, bool XS, bool SW = false>
 __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
@@ -621,17 +663,30 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
   const char *A = reinterpret_cast<const char *>(a.A);
 
   // `row` and `base` (first chunk of the current load group) are the same in all
-  // lanes of a warp, so every lane leaves a row at the same step.
+  // lanes of a warp, so every lane leaves a row at the same step.  With SW
+  // (M = 2 * half) the warp walks pairs: gate row p, then up row p + half, then
+  // gate row p + rstride; once the next pair index reaches half, the row becomes
+  // M, which ends the loop.
+  const int64_t half = a.half;
+  auto next_row = [&](int64_t r) -> int64_t {
+    if (!SW) return r + rstride;
+    if (r < half) return r + half;                 // gate -> its up row
+    const int64_t np = r - half + rstride;         // up -> next pair's gate row
+    return np < half ? np : M;
+  };
+  auto row_live = [&](int64_t r) -> bool { return r < M; };
   int64_t row = blockIdx.x + (int64_t)gridDim.x * warp;
+  if (SW && row >= half) row = M;  // a pair index past the last pair: no work
   int64_t base = 0;
+  float gate_sum = 0.f;
   uint4 buf[U];
   // prologue: first group of the first row
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int64_t c = base + lane + 32 * u;
-    buf[u] = (row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+    buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
   }
-  while (row < M) {
+  while (row_live(row)) {
     float e = 0.f, o = 0.f;
     for (;;) {
       uint4 cur[U];
@@ -641,11 +696,11 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
       // next group: same row, or the first group of this warp's next row
       int64_t nrow = row;
       base += 32 * U;
-      if (base >= nch) { nrow = row + rstride; base = 0; }
+      if (base >= nch) { nrow = next_row(row); base = 0; }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = base + lane + 32 * u;
-        buf[u] = (nrow < M && c < nch) ? ld_stream16(A + nrow * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+        buf[u] = (row_live(nrow) && c < nch) ? ld_stream16(A + nrow * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -661,8 +716,13 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
       if (nrow != row) break;
     }
     const float s = group_sum<32>(e + o);
-    if (lane == 0) epilogue_store<Op>(a, 0, row, s);
-    row += rstride;
+    if (SW) {
+      if (row < half) gate_sum = s;
+      else if (lane == 0) epilogue_swiglu<Op>(a, 0, row - half, gate_sum, s);
+    } else if (lane == 0) {
+      epilogue_store<Op>(a, 0, row, s);
+    }
+    row = next_row(row);
   }
 }
 
@@ -676,8 +736,9 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
 // accumulator pairs take packed FMAs.  The next step's loads (possibly of the next
 // row group) are in flight while the current step is used, and the first ones are
 // issued before x is staged.
-template <class Op, int NB, int R, int U, int THREADS, bool XF32>
+template <class Op, int NB, int R, int U, int THREADS, bool XF32, bool SW = false>
 __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
+  static_assert(!SW || R == 2, "SwiGLU pairs the gate and up row of one output");
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
   constexpr int QW = Op::VEC / 4;
@@ -690,7 +751,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
   const int64_t nch = K / Op::VEC;
   const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
   const char *A = reinterpret_cast<const char *>(a.A);
-  const int64_t groups = (M + R - 1) / R;
+  // row r of group g: g * R + r, or with SW the gate row g and the up row g + half
+  const int64_t groups = SW ? a.half : (M + R - 1) / R;
+  auto row_of = [&](int64_t gg, int r) -> int64_t { return SW ? gg + r * a.half : gg * R + r; };
   const int64_t gstride = (int64_t)gridDim.x * WARPS;
 
   int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
@@ -700,7 +763,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
   for (int u = 0; u < U; ++u)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int64_t row = g * R + r, c = base + lane + 32 * u;
+      const int64_t row = row_of(g, r), c = base + lane + 32 * u;
       nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
                                                      : make_uint4(0, 0, 0, 0);
     }
@@ -752,7 +815,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const int64_t row = ng * R + r, c = base + lane + 32 * u;
+          const int64_t row = row_of(ng, r), c = base + lane + 32 * u;
           nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
                                                           : make_uint4(0, 0, 0, 0);
         }
@@ -790,12 +853,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
       }
       if (ng != g) break;
     }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
+    if constexpr (SW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        const float s = group_sum<32>(acc[r][b].x + acc[r][b].y);
-        if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
+        const float s0 = group_sum<32>(acc[0][b].x + acc[0][b].y);
+        const float s1 = group_sum<32>(acc[1][b].x + acc[1][b].y);
+        if (lane == 0 && b < B) epilogue_swiglu<Op>(a, b, g, s0, s1);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float s = group_sum<32>(acc[r][b].x + acc[r][b].y);
+          if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
+        }
       }
     }
     g = ng;

@@ -50,13 +50,16 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
       kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
       return cudaSuccess;
     };
-    // R = 2 rows per warp with U = 2 chunks per step, or R = 4 with U = 1
+    // R = 2 rows per warp with U = 2 chunks per step, or R = 4 with U = 1;
+    // SwiGLU (a.half > 0) pairs each gate row with its up row (R = 2)
     const bool f32x = p.x_staging == GEMV_X_SMEM_FP32;
+    if (a.half > 0)
+      return f32x ? run(k_batch_lo<Op, NB, 2, 2, T, true, true>) : run(k_batch_lo<Op, NB, 2, 2, T, false, true>);
     if (p.rows_per_warp == 2)
       return f32x ? run(k_batch_lo<Op, NB, 2, 2, T, true>) : run(k_batch_lo<Op, NB, 2, 2, T, false>);
     return f32x ? run(k_batch_lo<Op, NB, 4, 1, T, true>) : run(k_batch_lo<Op, NB, 4, 1, T, false>);
   } else {
-    auto kern = k_batched2<Op, NB, 2, 2, T>;
+    auto kern = a.half > 0 ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
@@ -68,13 +71,16 @@ template <class Op>
 cudaError_t launch_stream(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
   constexpr int T = kStreamThreads;
   const dim3 grid((unsigned)p.grid), block(T);
+  const bool sw = a.half > 0;  // SwiGLU row pairs
   if (p.x_staging == GEMV_X_SMEM) {
-    auto kern = p.unroll == 2 ? k_stream<Op, 2, T, true> : k_stream<Op, 4, T, true>;
+    auto kern = sw ? k_stream<Op, 4, T, true, true>
+                   : (p.unroll == 2 ? k_stream<Op, 2, T, true> : k_stream<Op, 4, T, true>);
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
   } else {
-    auto kern = p.unroll == 2 ? k_stream<Op, 2, T, false> : k_stream<Op, 4, T, false>;
+    auto kern = sw ? (p.unroll == 2 ? k_stream<Op, 2, T, false, true> : k_stream<Op, 4, T, false, true>)
+                   : (p.unroll == 2 ? k_stream<Op, 2, T, false> : k_stream<Op, 4, T, false>);
     kern<<<grid, block, 0, s>>>(a);
   }
   return cudaSuccess;

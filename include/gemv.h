@@ -123,6 +123,38 @@ gemv_status_t gemv_bf16_splitk_noalloc(const uint16_t *A, const uint16_t *x, con
                                        uint16_t *y, int64_t M, int64_t K, int B,
                                        gemv_stream_t stream);
 
+/* ------------------------------------------------------- fused epilogues */
+
+/* Activation applied after the bias (NPU MatMul post, section 5.1: fuse the bias,
+ * the activation and the residual into the MatMul rather than running separate
+ * passes over y). */
+typedef enum gemv_activation {
+  GEMV_ACT_NONE = 0,
+  GEMV_ACT_SILU = 1 /* silu(v) = v / (1 + e^-v), fp32 */
+} gemv_activation_t;
+
+/* y[b][m] = act(s_m * sum_k A[m][k] x[b][k] + bias[m]) + residual[b][m]
+ * Any storage type (`dtype`); row_scale only (and required) for GEMV_DTYPE_W8,
+ * NULL otherwise.  residual is B x M in y's type, may be NULL, and may be y itself
+ * (in place: y += act(A x + bias)); it must not otherwise overlap y.  The kernel
+ * choice, layouts and errors are those of the plain entry points. */
+gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
+                      const void *bias, const void *residual, void *y, int64_t M, int64_t K, int B,
+                      gemv_activation_t act, gemv_stream_t stream);
+
+/* SwiGLU over a concatenated gate/up projection: A is 2I x K, rows 0..I-1 the gate
+ * and rows I..2I-1 the up projection (bias and row_scale, when given, have 2I
+ * entries in the same order); y is B x I:
+ *     y[b][m] = silu(g) * u,  g = s_m A[m] x[b] + bias[m],
+ *                             u = s_{m+I} A[m+I] x[b] + bias[m+I].
+ * One launch; the gate and up sums of an output meet in registers, so the 2I
+ * intermediate values never reach memory.  Needs 16-byte aligned rows with at least
+ * one 16-byte chunk per lane of a warp, and for B > 1 x[0..B) small enough to stage
+ * in shared memory; otherwise GEMV_ERR_UNSUPPORTED and nothing is launched. */
+gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
+                          const void *bias, void *y, int64_t I, int64_t K, int B,
+                          gemv_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gemv_status_string(gemv_status_t status);
 

@@ -61,6 +61,14 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode.restype = ctypes.c_int
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
+        L.oracle_silu.argtypes = [ctypes.c_double]
+        L.oracle_silu.restype = ctypes.c_double
+        L.oracle_gemv_ex.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int,
+                                     vp, vp, vp, ctypes.c_int]
+        L.oracle_gemv_ex.restype = ctypes.c_int
+        L.oracle_swiglu.argtypes = [ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp,
+                                    ctypes.c_int]
+        L.oracle_swiglu.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -108,6 +116,63 @@ def gemv(dtype: str, A, x, bias=None, scale=None, nthreads: int = 1):
     if rc != 0:
         raise ValueError("oracle_gemv rejected its arguments")
     return y, absdot
+
+
+def silu(v: float) -> float:
+    """The oracle's SiLU, v / (1 + e^-v), in double."""
+    return float(lib().oracle_silu(float(v)))
+
+
+def gemv_ex(dtype: str, A, x, bias=None, scale=None, residual=None, act: int = 0, nthreads: int = 1):
+    """GEMV with the fused epilogue: y = act(s_m * sum_k A x + bias) + residual.
+
+    act: 0 none, 1 SiLU.  residual: (B, M) in y's storage type (like x) or None.
+    Returns (y, pre, absdot): y after the epilogue, pre the value before the
+    activation, absdot = sum_k |s_m A x|; all float64 (B, M).
+    """
+    code = KIND[dtype]
+    A = _storage(A, code)
+    xcode = KIND["bf16"] if dtype == "w8" else code
+    x = _storage(x, xcode)
+    bias = _storage(bias, xcode)
+    residual = _storage(residual, xcode)
+    if scale is not None:
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M, K = A.shape
+    B = x.shape[0]
+    if residual is not None and residual.shape != (B, M):
+        raise ValueError("residual must be (B, M)")
+    y = np.empty((B, M)); pre = np.empty((B, M)); ad = np.empty((B, M))
+    rc = lib().oracle_gemv_ex(code, _ptr(A), _ptr(scale), _ptr(x), _ptr(bias), _ptr(residual), M, K, B,
+                              int(act), _ptr(y), _ptr(pre), _ptr(ad), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gemv_ex rejected its arguments")
+    return y, pre, ad
+
+
+def swiglu(dtype: str, A, x, bias=None, scale=None, nthreads: int = 1):
+    """SwiGLU over A = [gate rows; up rows] (2I x K): y = silu(gate) * up.
+
+    Returns (y, gate, up, absdot_gate, absdot_up), all float64 (B, I).
+    """
+    code = KIND[dtype]
+    A = _storage(A, code)
+    xcode = KIND["bf16"] if dtype == "w8" else code
+    x = _storage(x, xcode)
+    bias = _storage(bias, xcode)
+    if scale is not None:
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+    M2, K = A.shape
+    if M2 % 2:
+        raise ValueError("A must have an even number of rows (gate then up)")
+    I = M2 // 2
+    B = x.shape[0]
+    out = [np.empty((B, I)) for _ in range(5)]
+    rc = lib().oracle_swiglu(code, _ptr(A), _ptr(scale), _ptr(x), _ptr(bias), I, K, B,
+                             *[_ptr(o) for o in out], int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_swiglu rejected its arguments")
+    return tuple(out)
 
 
 def decode(kind: str, bits) -> np.ndarray:

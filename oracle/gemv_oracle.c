@@ -25,12 +25,19 @@
  * The companion output absdot[b][m] = sum_k |s_m * A[m][k] * x[b][k]| is the scale
  * against which the GPU's fp32-accumulation error is judged.
  *
+ * Fused epilogues (the NPU MatMul post, section 5.1: bias, activation and residual
+ * fused into the MatMul) are the same rows followed by the elementwise step, in
+ * fp64: oracle_gemv_ex applies act() and adds residual[b][m]; oracle_swiglu takes
+ * rows 0..I-1 of A as the gate and rows I..2I-1 as the up projection and returns
+ * silu(gate_m) * up_m, with silu(v) = v / (1 + e^-v).
+ *
  * Build: gcc -O2 -fPIC -shared -ffp-contract=off -fopenmp (no fast-math, so each
  * double operation rounds once, as written).
  */
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifdef _OPENMP
@@ -142,4 +149,59 @@ int oracle_max_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* SiLU in double: v / (1 + e^-v). */
+double oracle_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/*
+ * y[b][m] = act(row value) + residual[b][m], act 0 = none, 1 = SiLU; residual is
+ * B x M in y's storage type (decoded like x) or NULL.  pre[b][m] (may be NULL) gets
+ * the value before the activation; absdot as in oracle_gemv.
+ */
+int oracle_gemv_ex(int dtype, const void *A, const float *scale, const void *x, const void *bias,
+                   const void *residual, int64_t M, int64_t K, int64_t B, int act, double *y,
+                   double *pre, double *absdot, int nthreads) {
+  if (act != 0 && act != 1) return -1;
+  int rc = oracle_gemv(dtype, A, scale, x, bias, M, K, B, y, absdot, nthreads);
+  if (rc != 0) return rc;
+  for (int64_t i = 0; i < M * B; ++i) {
+    double v = y[i];
+    if (pre != NULL) pre[i] = v;
+    if (act == 1) v = oracle_silu(v);
+    if (residual != NULL) v += load_x(dtype, residual, (size_t)i);
+    y[i] = v;
+  }
+  return 0;
+}
+
+/*
+ * SwiGLU: A is 2I x K (gate rows, then up rows), bias and scale 2I long (or NULL /
+ * unused).  y[b][m] = silu(g) * u with g and u the rows m and m + I of vector b.
+ * gate, up, absdot_gate, absdot_up: B x I each (may be NULL).
+ */
+int oracle_swiglu(int dtype, const void *A, const float *scale, const void *x, const void *bias,
+                  int64_t I, int64_t K, int64_t B, double *y, double *gate, double *up,
+                  double *absdot_gate, double *absdot_up, int nthreads) {
+  if (I < 0 || B < 0) return -1;
+  if (I == 0 || B == 0) return 0;
+  double *full = (double *)malloc(sizeof(double) * (size_t)(2 * I * B));
+  double *fabsd = (double *)malloc(sizeof(double) * (size_t)(2 * I * B));
+  if (full == NULL || fabsd == NULL) { free(full); free(fabsd); return -1; }
+  int rc = oracle_gemv(dtype, A, scale, x, bias, 2 * I, K, B, full, fabsd, nthreads);
+  if (rc == 0) {
+    for (int64_t b = 0; b < B; ++b) {
+      for (int64_t m = 0; m < I; ++m) {
+        const double g = full[b * 2 * I + m], u = full[b * 2 * I + m + I];
+        y[b * I + m] = oracle_silu(g) * u;
+        if (gate != NULL) gate[b * I + m] = g;
+        if (up != NULL) up[b * I + m] = u;
+        if (absdot_gate != NULL) absdot_gate[b * I + m] = fabsd[b * 2 * I + m];
+        if (absdot_up != NULL) absdot_up[b * I + m] = fabsd[b * 2 * I + m + I];
+      }
+    }
+  }
+  free(full);
+  free(fabsd);
+  return rc;
 }

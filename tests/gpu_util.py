@@ -80,3 +80,38 @@ def assert_close(dtype: str, y: torch.Tensor, y_ref: np.ndarray, absdot: np.ndar
             f"{what}: {int(bad.sum())} of {bad.size} outputs out of tolerance; worst err "
             f"{err[i]:.3e} > bound {bound[fin][i]:.3e} (got {got[fin][i]!r}, ref {y_ref[fin][i]!r})")
     return float((err / bound[fin]).max()) if err.size else 0.0
+
+
+SILU_LIP = 1.1  # max |d silu / dv| is 1.0998 (at v ~ 2.40)
+F32_SLACK = 4e-7  # fp32 expf and division in the GPU's silu, relative
+
+
+def assert_close_ex(dtype, y, y_ref, absdot, act: int, what: str = ""):
+    """Fused epilogue: the GEMV bound through SiLU's Lipschitz constant, plus the
+    output rounding and the fp32 activation's own rounding."""
+    rel, ab = TOL[dtype]
+    bound = (SILU_LIP if act else 1.0) * (rel * absdot + ab)
+    bound = bound + (U_OUT[dtype] + F32_SLACK) * np.abs(y_ref)
+    _compare(y, y_ref, bound, what)
+
+
+def assert_close_swiglu(dtype, y, y_ref, gate, up, adg, adu, what: str = ""):
+    """silu(g) * u with g, u each within the GEMV bound: |d| <= L tg (|u| + tu) + |silu(g)| tu."""
+    rel, ab = TOL[dtype]
+    tg, tu = rel * adg + ab, rel * adu + ab
+    sg = gate / (1.0 + np.exp(-gate))
+    bound = SILU_LIP * tg * (np.abs(up) + tu) + np.abs(sg) * tu
+    bound = bound + (U_OUT[dtype] + F32_SLACK) * np.abs(y_ref)
+    _compare(y, y_ref, bound, what)
+
+
+def _compare(y, y_ref, bound, what):
+    got = y.detach().double().cpu().numpy().reshape(y_ref.shape)
+    assert np.array_equal(np.isnan(got), np.isnan(y_ref)), f"{what}: NaN positions differ"
+    fin = np.isfinite(y_ref)
+    err = np.abs(got[fin] - y_ref[fin])
+    bad = err > bound[fin]
+    if bad.any():
+        i = int(np.argmax(err - bound[fin]))
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} out of tolerance; worst err "
+                             f"{err[i]:.3e} > bound {bound[fin][i]:.3e} (got {got[fin][i]!r}, ref {y_ref[fin][i]!r})")

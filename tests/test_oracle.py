@@ -168,3 +168,74 @@ def test_planted_mistake_is_caught(name):
         except (AssertionError, IndexError, ValueError):
             failed.append(pin.__name__)
     assert failed, f"no pin catches the planted mistake {name}"
+
+
+# ------------------------------------------------------------ fused epilogues
+# SiLU, the residual add and SwiGLU are pinned against an independent logistic
+# function (scipy.special.expit), exact identities and closed forms.
+def test_silu_closed_forms():
+    import math
+    from scipy.special import expit
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(math.log(3.0)) == pytest.approx(0.75 * math.log(3.0), rel=1e-15)
+    for v in (-30.0, -3.5, -1.0, -1e-3, 1e-3, 0.5, 2.0, 7.25, 40.0):
+        assert oracle.silu(v) - oracle.silu(-v) == pytest.approx(v, rel=1e-14, abs=1e-300)
+        assert oracle.silu(v) == pytest.approx(v * expit(v), rel=1e-14)
+    assert oracle.silu(100.0) == 100.0
+    assert abs(oracle.silu(-100.0)) < 1e-40
+
+
+def test_gemv_ex_is_gemv_then_elementwise():
+    from scipy.special import expit
+    rng = np.random.default_rng(20)
+    for dtype in P.DTYPES:
+        M, K, B = 7, 11, 3
+        A, x, bb, sc = P.tiny_inputs(rng, dtype, M, K, B, True)
+        y0, ad0 = oracle.gemv(dtype, A, x, bb, sc)
+        y, pre, ad = oracle.gemv_ex(dtype, A, x, bb, sc, act=0)
+        assert np.array_equal(y, y0) and np.array_equal(pre, y0) and np.array_equal(ad, ad0)
+        y, pre, _ = oracle.gemv_ex(dtype, A, x, bb, sc, act=1)
+        assert np.array_equal(pre, y0)
+        np.testing.assert_allclose(y, y0 * expit(y0), rtol=1e-14, atol=1e-300)
+        # residual in y's storage type: small integers make the sum exact
+        xk = P.xkind(dtype)
+        rv = rng.integers(-9, 10, size=(B, M)).astype(np.float64)
+        r = P.encode(xk, rv)
+        y, _, _ = oracle.gemv_ex(dtype, A, x, bb, sc, residual=r, act=0)
+        assert np.array_equal(y, y0 + rv)
+
+
+def test_swiglu_on_permutations():
+    """A = [P; Q] with permutation matrices: gate = P x, up = Q x, exactly; the
+    first I rows are the gate (swapping the halves gives silu(Q x) * P x)."""
+    from scipy.special import expit
+    rng = np.random.default_rng(21)
+    for dtype in P.DTYPES:
+        I = 6
+        p1, p2 = rng.permutation(I), rng.permutation(I)
+        Pm, Qm = np.zeros((I, I)), np.zeros((I, I))
+        Pm[np.arange(I), p1] = 1.0
+        Qm[np.arange(I), p2] = 1.0
+        A = P.encode(dtype, np.vstack([Pm, Qm]))
+        _, x, _, _ = P.tiny_inputs(rng, dtype, I, I, 2, False)
+        sc = np.ones(2 * I, dtype=np.float32) if dtype == "w8" else None
+        xd = P.decode_any(P.xkind(dtype), x)
+        y, g, u, adg, adu = oracle.swiglu(dtype, A, x, scale=sc)
+        assert np.array_equal(g, xd[:, p1]) and np.array_equal(u, xd[:, p2])
+        np.testing.assert_allclose(y, xd[:, p1] * expit(xd[:, p1]) * xd[:, p2], rtol=1e-14, atol=1e-300)
+        assert np.array_equal(adg, np.abs(xd[:, p1])) and np.array_equal(adu, np.abs(xd[:, p2]))
+        A2 = P.encode(dtype, np.vstack([Qm, Pm]))
+        y2, *_ = oracle.swiglu(dtype, A2, x, scale=sc)
+        np.testing.assert_allclose(y2, xd[:, p2] * expit(xd[:, p2]) * xd[:, p1], rtol=1e-14, atol=1e-300)
+
+
+def test_swiglu_bias_and_scale_follow_rows():
+    # bias/scale entries 0..I-1 belong to the gate rows, I..2I-1 to the up rows
+    I, K = 3, 4
+    A = P.encode("w8", np.ones((2 * I, K)))
+    x = P.enc_bf16_exact([[1.0, 1.0, 1.0, 1.0]])
+    sc = np.array([1, 2, 3, 0.5, 0.25, 2], dtype=np.float32)
+    bb = P.enc_bf16_exact([0, 1, 2, 3, 4, 5])
+    y, g, u, _, _ = oracle.swiglu("w8", A, x, bias=bb, scale=sc)
+    assert np.array_equal(g[0], [4 * 1 + 0, 4 * 2 + 1, 4 * 3 + 2])
+    assert np.array_equal(u[0], [4 * 0.5 + 3, 4 * 0.25 + 4, 4 * 2 + 5])
