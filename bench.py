@@ -15,7 +15,8 @@ events on the stream it runs on; the step time is the sum of the three.
     cpu_baseline = the CPU oracle on the same step, on the host's cores
     sweep      = every configuration at its full size, timed the same way
     decode_layer = a Llama-3-8B-shaped bf16 layer's four GEMVs, eager and from a
-                 CUDA graph
+                 CUDA graph, and again with the residual adds and SwiGLU fused
+                 into the GEMV epilogues
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs the same workload on its own GPU (replicas: the
@@ -450,13 +451,51 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
     graph_ms = timed(graph.replay)
     iso = time_gemvs(torch, g, items, flush, iters, 3)
     iso_ms = sum(statistics.median(t) for t in iso)
+    fused = decode_layer_fused(torch, g, dev, items, timed)
     return {"layer": "bf16 B=1: " + ", ".join(f"{n} {M}x{K}" for n, M, K in DECODE_LAYER),
             "bytes": layer_bytes, "kernels": launches,
             "eager_us": round(eager_ms * 1e3, 2), "graph_us": round(graph_ms * 1e3, 2),
             "isolated_sum_us": round(iso_ms * 1e3, 2),
             "eager_gbs": round(layer_bytes / (eager_ms * 1e-3) / 1e9, 1),
             "graph_gbs": round(layer_bytes / (graph_ms * 1e-3) / 1e9, 1),
-            "graph_frac_of_peak": round(layer_bytes / (graph_ms * 1e-3) / 1e9 / peak, 4)}
+            "graph_frac_of_peak": round(layer_bytes / (graph_ms * 1e-3) / 1e9 / peak, 4),
+            "fused": dict(fused, graph_frac_of_peak=round(fused["graph_gbs"] / peak, 4))}
+
+
+def decode_layer_fused(torch, g, dev, items, timed):
+    """The same layer with its elementwise steps in the GEMV epilogues: the output
+    and down projections add the residual stream h in place (gemv_ex), and gate_up
+    stores silu(gate) * up (gemv_swiglu, I = 14336), which the down projection then
+    reads as its x.  Unfused, these steps would be three more kernels."""
+    (wq, dq, yq), (wo, do, yo), (wg, dg, _), (wd, dd, yd) = items
+    I = wg.M // 2
+    h_o = torch.zeros((1, wo.M), dtype=torch.bfloat16, device=dev)
+    h_d = torch.zeros((1, wd.M), dtype=torch.bfloat16, device=dev)
+    act = torch.empty((1, I), dtype=torch.bfloat16, device=dev)
+
+    def run():
+        g.gemv_bf16(dq["A"], dq["x"], None, yq, wq.M, wq.K, 1)
+        g.gemv_ex("bf16", do["A"], None, do["x"], None, h_o, h_o, wo.M, wo.K, 1)
+        g.gemv_swiglu("bf16", dg["A"], None, dg["x"], None, act, I, wg.K, 1)
+        g.gemv_ex("bf16", dd["A"], None, act, None, h_d, h_d, wd.M, wd.K, 1)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    n0 = g.launch_count()
+    with torch.cuda.graph(graph):
+        run()
+    launches = g.launch_count() - n0
+    ms = timed(graph.replay)
+    # Q_min of the fused layer: the weights, each x once, each y once, residuals read
+    nbytes = (wq.qmin_bytes + wo.qmin_bytes + 2 * wo.M + wg.M * wg.K * 2 + wg.K * 2 + I * 2
+              + wd.qmin_bytes + 2 * wd.M)
+    return {"epilogues": "o, down: + residual in place; gate_up: silu(gate) * up",
+            "bytes": nbytes, "kernels": launches, "graph_us": round(ms * 1e3, 2),
+            "graph_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
 def cpu_baseline(head, host_inputs, budget_s=10.0):
