@@ -336,13 +336,57 @@ __device__ __forceinline__ float row_value(const Args &a, int64_t m, float acc) 
 // (lesson 3's epilogue adds the bias in fp32 after the reduction, NULL allowed;
 // the NPU MatMul post, section 5.1, fuses bias, activation and residual into the
 // MatMul instead of separate passes over y).
+// The residual may be y itself (in place): a plain, coherent load, not the
+// read-only path.
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <class Op>
+__device__ __forceinline__ float residual_at(const void *r, int64_t i) {
+  return to_f32(reinterpret_cast<const typename Op::TX *>(r)[i]);
+}
+
+// act(v) + res, rounded once to the output type, stored at y[i].
+template <class Op>
+__device__ __forceinline__ void store_act_res(const Args &a, int64_t i, float v, float res) {
+  if (a.act == 1) v = silu(v);
+  if (a.residual != nullptr) v += res;
+  Op::store(a.y, i, v);
+}
+
 template <class Op>
 __device__ __forceinline__ void epilogue_store(const Args &a, int b, int64_t m, float acc) {
-  float v = row_value<Op>(a, m, acc);
-  if (a.act == 1) v = silu(v);
   const int64_t i = (int64_t)b * a.M + m;
-  if (a.residual != nullptr) v += Op::x_elem(a.residual, i);
-  Op::store(a.y, i, v);
+  const float res = a.residual != nullptr ? residual_at<Op>(a.residual, i) : 0.f;
+  store_act_res<Op>(a, i, row_value<Op>(a, m, acc), res);
+}
+
+// A row's epilogue operands, loaded when the row's first A loads are issued so
+// that they arrive while the row streams instead of after its reduction: the
+// scale, the bias and (RES) vector 0's residual, all in registers.
+struct RowPre {
+  float s, bias, res;
+};
+
+template <class Op, bool RES>
+__device__ __forceinline__ RowPre row_pre(const Args &a, int64_t m, bool live) {
+  RowPre p{1.f, 0.f, 0.f};
+  if (live) {
+    if (a.scale != nullptr) p.s = __ldg(a.scale + m);
+    if (a.bias != nullptr) p.bias = bias_at<Op>(a.bias, m);
+    if (RES && a.residual != nullptr) p.res = residual_at<Op>(a.residual, m);
+  }
+  return p;
+}
+
+// s_m * acc + bias[m] from prefetched operands (the same operations as row_value).
+template <class Op>
+__device__ __forceinline__ float row_value_pre(const Args &a, const RowPre &p, float acc) {
+  float v = acc;
+  if (a.scale != nullptr) v *= p.s;
+  if (a.bias != nullptr) v += p.bias;
+  return v;
 }
 
 // SwiGLU output m of vector b from the gate row m and the up row m + half.
@@ -381,6 +425,7 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
   for (int64_t base = (int64_t)blockIdx.x * TEAMS; base < M; base += (int64_t)gridDim.x * TEAMS) {
     const int64_t row = base + team;
     const bool live = row < M;
+    const RowPre pre = row_pre<Op, NB == 1>(a, row, live);
     float e[NB], o[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
@@ -427,8 +472,13 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
     for (int b = 0; b < NB; ++b) e[b] = group_sum<TPR>(e[b] + o[b]);
     if (live && sub == 0) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
-        if (b < B) epilogue_store<Op>(a, b, row, e[b]);
+      for (int b = 0; b < NB; ++b) {
+        if (b < B) {
+          const int64_t i = (int64_t)b * M + row;
+          const float res = NB == 1 ? pre.res : (a.residual != nullptr ? residual_at<Op>(a.residual, i) : 0.f);
+          store_act_res<Op>(a, i, row_value_pre<Op>(a, pre, e[b]), res);
+        }
+      }
     }
   }
 }
@@ -641,8 +691,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 // a warp never waits on an empty pipeline between rows.  Rows are dealt to CTAs
 // round-robin so that every SM gets an equal share.  x is read through L1, or
 // from shared memory (XS) where the CTA copies it once.
+// CTAs per SM the stream plan launches (4 for fp32 rows, 2 otherwise): the
+// register budget must let them all be resident.
+template <class Op>
+constexpr int stream_ctas_per_sm() { return sizeof(typename Op::TA) == 4 ? 4 : 2; }
+
 template <class Op, int U, int THREADS, bool XS, bool SW = false>
-__global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
+__global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -678,13 +733,36 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
   int64_t row = blockIdx.x + (int64_t)gridDim.x * warp;
   if (SW && row >= half) row = M;  // a pair index past the last pair: no work
   int64_t base = 0;
-  float gate_sum = 0.f;
+  float gate_val = 0.f;
   uint4 buf[U];
   // prologue: first group of the first row
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int64_t c = base + lane + 32 * u;
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+  }
+  // The epilogue operands of the CTA's first THREADS rows (pairs with SW) are
+  // staged in shared memory while those loads are in flight, so that no row waits
+  // on a bias, scale or residual load after its reduction.  The j-th row of warp w
+  // is unit t = w + WARPS * j of the CTA: row (or pair) blockIdx.x + gridDim.x * t.
+  __shared__ float ops[4][THREADS];
+  const bool staged = a.bias != nullptr || a.scale != nullptr || a.residual != nullptr;
+  if (staged) {
+    const int t = threadIdx.x;
+    const int64_t r = blockIdx.x + (int64_t)gridDim.x * t;
+    if (SW ? r < half : r < M) {
+      if (SW) {
+        ops[0][t] = a.bias != nullptr ? bias_at<Op>(a.bias, r) : 0.f;
+        ops[1][t] = a.scale != nullptr ? __ldg(a.scale + r) : 1.f;
+        ops[2][t] = a.bias != nullptr ? bias_at<Op>(a.bias, r + half) : 0.f;
+        ops[3][t] = a.scale != nullptr ? __ldg(a.scale + r + half) : 1.f;
+      } else {
+        ops[0][t] = a.bias != nullptr ? bias_at<Op>(a.bias, r) : 0.f;
+        ops[1][t] = a.scale != nullptr ? __ldg(a.scale + r) : 1.f;
+        ops[2][t] = a.residual != nullptr ? residual_at<Op>(a.residual, r) : 0.f;
+      }
+    }
+    __syncthreads();
   }
   while (row_live(row)) {
     float e = 0.f, o = 0.f;
@@ -693,7 +771,8 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
 #pragma unroll
       for (int u = 0; u < U; ++u) cur[u] = buf[u];
       const int64_t cc = base + lane;
-      // next group: same row, or the first group of this warp's next row
+      // next group: same row, or the first group of this warp's next row (whose
+      // epilogue operand is fetched with it)
       int64_t nrow = row;
       base += 32 * U;
       if (base >= nch) { nrow = next_row(row); base = 0; }
@@ -716,11 +795,21 @@ __global__ void __launch_bounds__(THREADS) k_stream(const Args a) {
       if (nrow != row) break;
     }
     const float s = group_sum<32>(e + o);
-    if (SW) {
-      if (row < half) gate_sum = s;
-      else if (lane == 0) epilogue_swiglu<Op>(a, 0, row - half, gate_sum, s);
-    } else if (lane == 0) {
-      epilogue_store<Op>(a, 0, row, s);
+    if (lane == 0) {
+      const bool up = SW && row >= half;
+      const int64_t t = ((up ? row - half : row) - blockIdx.x) / gridDim.x;  // unit index in the CTA
+      RowPre p{1.f, 0.f, 0.f};
+      if (staged && t < THREADS) {
+        p.bias = ops[up ? 2 : 0][t];
+        p.s = ops[up ? 3 : 1][t];
+        if (!SW) p.res = ops[2][t];
+      } else {
+        p = row_pre<Op, !SW>(a, row, true);
+      }
+      const float v = row_value_pre<Op>(a, p, s);
+      if (!SW) store_act_res<Op>(a, row, v, p.res);
+      else if (!up) gate_val = v;
+      else Op::store(a.y, row - half, silu(gate_val) * v);
     }
     row = next_row(row);
   }
