@@ -146,11 +146,15 @@ struct OpBF16 {
     e = fmaf(bf16_lo(a), bf16_lo(x), e);
     o = fmaf(bf16_hi(a), bf16_hi(x), o);
   }
+  // (e, o) as one fp32 pair, one packed FMA per word (same order as pair()).
   __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
-    pair(e, o, a.x, xv[0].x);
-    pair(e, o, a.y, xv[0].y);
-    pair(e, o, a.z, xv[0].z);
-    pair(e, o, a.w, xv[0].w);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, xw[4] = {xv[0].x, xv[0].y, xv[0].z, xv[0].w};
+    float2 acc = make_float2(e, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      acc = __ffma2_rn(make_float2(bf16_lo(aw[i]), bf16_hi(aw[i])), make_float2(bf16_lo(xw[i]), bf16_hi(xw[i])), acc);
+    e = acc.x;
+    o = acc.y;
   }
   // acc += a.lo * x.lo + a.hi * x.hi with the mixed-precision FMA (bf16 inputs,
   // fp32 accumulator): the bf16 product is exact in fp32, one rounding per FMA.
@@ -203,11 +207,14 @@ struct OpF16 {
     e = fmaf(fa.x, fx.x, e);
     o = fmaf(fa.y, fx.y, o);
   }
+  // (e, o) as one fp32 pair, one packed FMA per word (same order as pair()).
   __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
-    pair(e, o, a.x, xv[0].x);
-    pair(e, o, a.y, xv[0].y);
-    pair(e, o, a.z, xv[0].z);
-    pair(e, o, a.w, xv[0].w);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, xw[4] = {xv[0].x, xv[0].y, xv[0].z, xv[0].w};
+    float2 acc = make_float2(e, o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc = __ffma2_rn(f16x2_to_f2(aw[i]), f16x2_to_f2(xw[i]), acc);
+    e = acc.x;
+    o = acc.y;
   }
   // acc += a.lo * x.lo + a.hi * x.hi with the mixed-precision FMA (fp16 inputs,
   // fp32 accumulator): the fp16 product is exact in fp32, one rounding per FMA.
@@ -263,11 +270,21 @@ struct OpW8 {
     e = fmaf(s8_to_f32<2>(f), bf16_lo(x23), e);
     o = fmaf(s8_to_f32<3>(f), bf16_hi(x23), o);
   }
+  // (e, o) as one fp32 pair: each packed subtraction decodes two weights and each
+  // packed FMA adds two products, in the same order per accumulator as word().
   __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
-    word(e, o, a.x, xv[0].x, xv[0].y);
-    word(e, o, a.y, xv[0].z, xv[0].w);
-    word(e, o, a.z, xv[1].x, xv[1].y);
-    word(e, o, a.w, xv[1].z, xv[1].w);
+    float2 acc = make_float2(e, o);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float2 q01, q23;
+      quad2(a, w, q01, q23);
+      const uint32_t x01 = (w & 1) ? (w < 2 ? xv[0].z : xv[1].z) : (w < 2 ? xv[0].x : xv[1].x);
+      const uint32_t x23 = (w & 1) ? (w < 2 ? xv[0].w : xv[1].w) : (w < 2 ? xv[0].y : xv[1].y);
+      acc = __ffma2_rn(q01, make_float2(bf16_lo(x01), bf16_hi(x01)), acc);
+      acc = __ffma2_rn(q23, make_float2(bf16_lo(x23), bf16_hi(x23)), acc);
+    }
+    e = acc.x;
+    o = acc.y;
   }
   __device__ static __forceinline__ void word1(float &acc, uint32_t a, uint32_t x01, uint32_t x23) {
     const uint32_t f = a ^ 0x80808080u;
