@@ -13,7 +13,8 @@ events on the stream it runs on; the step time is the sum of the three.
     e2e        = the same metric with A, x, bias copied from pinned host memory
                  and y copied back inside the timed region, every step
     cpu_baseline = the CPU oracle on the same step, on the host's cores
-    sweep      = every configuration at its full size, timed the same way
+    sweep      = every configuration at its full size, timed the same way, plus
+                 the int4 (group-scaled) workloads
     decode_layer = a Llama-3-8B-shaped bf16 layer's four GEMVs, eager and from a
                  CUDA graph, and again with the residual adds and SwiGLU fused
                  into the GEMV epilogues
@@ -193,14 +194,15 @@ def gpu_id_for(torch, dev) -> str:
 
 # ------------------------------------------------------------------ our arm
 def call_gemv(g, w, d, y):
-    if w.dtype == "w8":
-        g.gemv_w8(d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
+    if w.dtype in ("w8", "w4"):
+        getattr(g, f"gemv_{w.dtype}")(d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
     else:
         getattr(g, f"gemv_{w.dtype}")(d["A"], d["x"], d["bias"], y, w.M, w.K, w.B)
 
 
 def out_dtype(torch, dtype):
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "w8": torch.bfloat16}[dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "w8": torch.bfloat16,
+            "w4": torch.bfloat16}[dtype]
 
 
 def l2_flush(flush):
@@ -375,9 +377,10 @@ def run_ours(args, rank, world, local_rank):
 
 
 def sweep(args, torch, g, dev, flush, peak):
-    """Every configuration at full size: µs, GB/s and fraction of peak."""
+    """Every configuration at full size (and the int4 workloads): µs, GB/s and
+    fraction of peak."""
     out = []
-    names = [w.name for w in W.CONFIGS]
+    names = [w.name for w in W.CONFIGS + W.W4_CONFIGS]
     if args.only:
         names = [n for n in names if n in args.only.split(",")]
     for n in names:

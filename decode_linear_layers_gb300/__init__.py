@@ -22,7 +22,7 @@ import os
 from .build import LIB as LIB_PATH, build
 
 __all__ = [
-    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_bf16_splitk_noalloc", "gemv_ex",
+    "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_w4", "gemv_bf16_splitk_noalloc", "gemv_ex",
     "gemv_swiglu", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
     "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH",
@@ -30,7 +30,8 @@ __all__ = [
 
 SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 ACT_NONE, ACT_SILU = 0, 1
-DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3, "w4": 4}
+W4_GROUP = 128  # elements of a row that share one int4 scale
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
            "split_k": 4, "batched": 5, "scalar": 6, "stream": 7}
 X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32"}
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
             f.restype = ci
         L.gemv_w8.argtypes = [vp, vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_w8.restype = ci
+        L.gemv_w4.argtypes = [vp, vp, vp, vp, vp, i64, i64, ci, vp]
+        L.gemv_w4.restype = ci
         L.gemv_bf16_splitk_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_bf16_splitk_noalloc.restype = ci
         L.gemv_ex.argtypes = [ci, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, vp]
@@ -210,6 +213,16 @@ def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
+def gemv_w4(A, group_scale, x, bias, y, M, K, B, stream=None) -> None:
+    """int4 A, two per byte (torch.uint8, M x K/2, even element in the low nibble),
+    with fp32 group_scale (M x K/W4_GROUP); bf16 x, bias and y; fp32 accumulation."""
+    M, K, B, _, nx, ny = _sizes(M, K, B)
+    na, ns = _a_count("w4", M, K)
+    args = (_addr(A, 1, na, "A"), _addr(group_scale, 4, ns, "group_scale"), _addr(x, 2, nx, "x"),
+            _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
+    _check(lib().gemv_w4(*args, M, K, B, _stream(stream)))
+
+
 def gemv_bf16_splitk_noalloc(A, x, bias, y, M, K, B, stream=None) -> None:
     """gemv_bf16 on the split-K path with its partial sums in the library's fixed
     device array (no device allocation).  For callers that cannot allocate while
@@ -219,7 +232,14 @@ def gemv_bf16_splitk_noalloc(A, x, bias, y, M, K, B, stream=None) -> None:
     _float_gemv("gemv_bf16_splitk_noalloc", 2, A, x, bias, y, M, K, B, stream)
 
 
-_ESIZE = {"f32": (4, 4), "f16": (2, 2), "bf16": (2, 2), "w8": (1, 2)}   # (A, x/bias/y)
+_ESIZE = {"f32": (4, 4), "f16": (2, 2), "bf16": (2, 2), "w8": (1, 2), "w4": (1, 2)}   # (A, x/bias/y)
+
+
+def _a_count(dtype, M, K):
+    """Elements of A's storage (bytes for int4, two values each) and of its scales."""
+    if dtype == "w4":
+        return max(0, M * K // 2), max(0, M * (K // W4_GROUP))
+    return max(0, M * K), max(0, M)
 
 
 def gemv_ex(dtype, A, row_scale, x, bias, residual, y, M, K, B, act=ACT_NONE, stream=None) -> None:
@@ -227,9 +247,10 @@ def gemv_ex(dtype, A, row_scale, x, bias, residual, y, M, K, B, act=ACT_NONE, st
 
     row_scale: w8 only (else None).  residual: (B, M) in y's type, None, or y itself
     (in place)."""
-    M, K, B, na, nx, ny = _sizes(M, K, B)
+    M, K, B, _, nx, ny = _sizes(M, K, B)
+    na, ns = _a_count(dtype, M, K)
     sa, sx = _ESIZE[dtype]
-    args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, sx, nx, "x"),
+    args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, ns, "row_scale"), _addr(x, sx, nx, "x"),
             _addr(bias, sx, M if bias is not None else 0, "bias"),
             _addr(residual, sx, ny if residual is not None else 0, "residual"), _addr(y, sx, ny, "y"))
     _check(lib().gemv_ex(DTYPE_CODES[dtype], *args, M, K, B, int(act), _stream(stream)))
@@ -240,7 +261,8 @@ def gemv_swiglu(dtype, A, row_scale, x, bias, y, I, K, B, stream=None) -> None:
     I, K, B = int(I), int(K), int(B)
     M2 = 2 * I if I >= 0 else 0
     sa, sx = _ESIZE[dtype]
-    args = (_addr(A, sa, max(0, M2 * K), "A"), _addr(row_scale, 4, M2, "row_scale"),
+    na, ns = _a_count(dtype, M2, K)
+    args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, ns, "row_scale"),
             _addr(x, sx, max(0, B * K), "x"), _addr(bias, sx, M2 if bias is not None else 0, "bias"),
             _addr(y, sx, max(0, B * I), "y"))
     _check(lib().gemv_swiglu(DTYPE_CODES[dtype], *args, I, K, B, _stream(stream)))

@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libgemv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]
-SOURCES = ["gemv_api.cu", "gemv_plan.cpp", "gemv_f32.cu", "gemv_f16.cu", "gemv_bf16.cu", "gemv_w8.cu",
+SOURCES = ["gemv_api.cu", "gemv_plan.cpp", "gemv_f32.cu", "gemv_f16.cu", "gemv_bf16.cu", "gemv_w8.cu", "gemv_w4.cu",
            "gemv_noalloc.cu"]
 HEADERS = ["gemv_kernels.cuh", "gemv_launch.cuh", "gemv_plan.h"]
 

@@ -72,8 +72,10 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
                   const void *residual, void *y, int64_t M, int64_t K, int B, int act, bool swiglu,
                   gemv_stream_t stream_in) {
   if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
-  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W8) return GEMV_ERR_INVALID_VALUE;
+  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W4) return GEMV_ERR_INVALID_VALUE;
   if (act != GEMV_ACT_NONE && act != GEMV_ACT_SILU) return GEMV_ERR_INVALID_VALUE;
+  const bool w4 = dtype == GEMV_DTYPE_W4;
+  if (w4 && K % GEMV_W4_GROUP != 0) return GEMV_ERR_INVALID_VALUE;
   if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
   if (M == 0 || B == 0) return GEMV_SUCCESS;
   const int sa = gemv::elem_bytes_a(dtype), sx = gemv::elem_bytes_x(dtype);
@@ -81,16 +83,20 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   const int64_t ym = swiglu ? M / 2 : M;  // outputs per vector
   int64_t a_bytes, x_bytes, y_bytes, mk, bk, bm;
   if (!mul_ok(M, K, &mk) || !mul_ok(mk, sa, &a_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (w4) a_bytes /= 2;  // two int4 per byte
+  // scale entries: one per row (int8), one per group of a row (int4)
+  const int64_t s_count = w4 ? M * (K / GEMV_W4_GROUP) : M;
   if (!mul_ok(B, K, &bk) || !mul_ok(bk, sx, &x_bytes)) return GEMV_ERR_INVALID_VALUE;
   if (!mul_ok(B, ym, &bm) || !mul_ok(bm, sy, &y_bytes)) return GEMV_ERR_INVALID_VALUE;
   if (y == nullptr) return GEMV_ERR_INVALID_VALUE;
   if (K > 0 && (A == nullptr || x == nullptr)) return GEMV_ERR_INVALID_VALUE;
   if (dtype == GEMV_DTYPE_W8 && scale == nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (w4 && K > 0 && scale == nullptr) return GEMV_ERR_INVALID_VALUE;
   if (!aligned(A, sa) || !aligned(x, sx) || !aligned(y, sy) || !aligned(bias, sx) ||
       !aligned(scale, 4) || !aligned(residual, sy))
     return GEMV_ERR_INVALID_VALUE;
   if (overlaps(y, y_bytes, A, a_bytes) || overlaps(y, y_bytes, x, x_bytes) ||
-      overlaps(y, y_bytes, bias, M * sx) || overlaps(y, y_bytes, scale, M * 4))
+      overlaps(y, y_bytes, bias, M * sx) || overlaps(y, y_bytes, scale, s_count * 4))
     return GEMV_ERR_INVALID_VALUE;
   // the residual may be y itself (in-place y += A x), but not a shifted view of it
   if (residual != nullptr && residual != y && overlaps(y, y_bytes, residual, y_bytes))
@@ -117,7 +123,9 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   args.A = A;
   args.x = x;
   args.bias = bias;
-  args.scale = scale;
+  args.scale = w4 ? nullptr : scale;  // int4 scales are per group, applied per chunk
+  args.gscale = w4 ? scale : nullptr;
+  args.gshift = w4 ? 7 : 0;          // log2(GEMV_W4_GROUP)
   args.y = y;
   args.M = M;
   args.K = K;
@@ -130,7 +138,8 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   launch_fn fn = dtype == GEMV_DTYPE_F32    ? gemv::launch_f32
                  : dtype == GEMV_DTYPE_F16  ? gemv::launch_f16
                  : dtype == GEMV_DTYPE_BF16 ? gemv::launch_bf16
-                                            : gemv::launch_w8;
+                 : dtype == GEMV_DTYPE_W8   ? gemv::launch_w8
+                                            : gemv::launch_w4;
   float *ws = nullptr;
   if (p.kernel == GEMV_KERNEL_SPLIT_K) {
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), (size_t)p.workspace_bytes, s);
@@ -181,10 +190,16 @@ gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x
   return run(GEMV_DTYPE_W8, A, row_scale, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
 }
 
+gemv_status_t gemv_w4(const uint8_t *A, const float *group_scale, const uint16_t *x,
+                      const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
+                      gemv_stream_t stream) {
+  return run(GEMV_DTYPE_W4, A, group_scale, x, bias, nullptr, y, M, K, B, GEMV_ACT_NONE, false, stream);
+}
+
 gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
                       const void *bias, const void *residual, void *y, int64_t M, int64_t K, int B,
                       gemv_activation_t act, gemv_stream_t stream) {
-  if (dtype != GEMV_DTYPE_W8 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (dtype != GEMV_DTYPE_W8 && dtype != GEMV_DTYPE_W4 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
   return run((int)dtype, A, row_scale, x, bias, residual, y, M, K, B, (int)act, false, stream);
 }
 
@@ -192,7 +207,7 @@ gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_sc
                           const void *bias, void *y, int64_t I, int64_t K, int B,
                           gemv_stream_t stream) {
   if (I < 0) return GEMV_ERR_INVALID_VALUE;
-  if (dtype != GEMV_DTYPE_W8 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (dtype != GEMV_DTYPE_W8 && dtype != GEMV_DTYPE_W4 && row_scale != nullptr) return GEMV_ERR_INVALID_VALUE;
   int64_t m2;
   if (!mul_ok(I, 2, &m2)) return GEMV_ERR_INVALID_VALUE;
   return run((int)dtype, A, row_scale, x, bias, nullptr, y, m2, K, B, GEMV_ACT_NONE, true, stream);

@@ -48,6 +48,10 @@ struct Args {
   const void *residual = nullptr;
   int act = 0;          // 0: none, 1: SiLU
   int64_t half = 0;
+  // int4 (OpW4): one fp32 scale per 2^gshift consecutive elements of a row,
+  // gscale[m][k >> gshift], M x (K >> gshift)
+  const float *gscale = nullptr;
+  int gshift = 0;
 };
 
 // ------------------------------------------------------------------ memory access
@@ -105,6 +109,8 @@ struct OpF32 {
   using TX = float;
   static constexpr int VEC = 4;
   static constexpr int XCH = 1;
+  static constexpr int EPB = 1;        // elements per byte of A
+  static constexpr bool GROUPED = false;  // per-group scales (int4)
   __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
     e = fmaf(__uint_as_float(a.x), __uint_as_float(xv[0].x), e);
     o = fmaf(__uint_as_float(a.y), __uint_as_float(xv[0].y), o);
@@ -142,6 +148,8 @@ struct OpBF16 {
   using TX = __nv_bfloat16;
   static constexpr int VEC = 8;
   static constexpr int XCH = 1;
+  static constexpr int EPB = 1;        // elements per byte of A
+  static constexpr bool GROUPED = false;  // per-group scales (int4)
   __device__ static __forceinline__ void pair(float &e, float &o, uint32_t a, uint32_t x) {
     e = fmaf(bf16_lo(a), bf16_lo(x), e);
     o = fmaf(bf16_hi(a), bf16_hi(x), o);
@@ -202,6 +210,8 @@ struct OpF16 {
   using TX = __half;
   static constexpr int VEC = 8;
   static constexpr int XCH = 1;
+  static constexpr int EPB = 1;        // elements per byte of A
+  static constexpr bool GROUPED = false;  // per-group scales (int4)
   __device__ static __forceinline__ void pair(float &e, float &o, uint32_t a, uint32_t x) {
     float2 fa = f16x2_to_f2(a), fx = f16x2_to_f2(x);
     e = fmaf(fa.x, fx.x, e);
@@ -262,6 +272,8 @@ struct OpW8 {
   using TX = __nv_bfloat16;
   static constexpr int VEC = 16;
   static constexpr int XCH = 2;
+  static constexpr int EPB = 1;        // elements per byte of A
+  static constexpr bool GROUPED = false;  // per-group scales (int4)
   __device__ static __forceinline__ void word(float &e, float &o, uint32_t a, uint32_t x01,
                                               uint32_t x23) {
     const uint32_t f = a ^ 0x80808080u;
@@ -330,6 +342,98 @@ struct OpW8 {
     reinterpret_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
   }
 };
+
+// int4 weights, two per byte (even element in the low nibble), symmetric two's
+// complement; one fp32 scale per group of 2^gshift consecutive elements of a row,
+// applied once per 16-byte chunk (32 weights, inside one group: groups are at least
+// 32 long); bf16 x, bias and y.  Decoding is the int8 magic number at nibble width:
+// with u = q + 8 (nibbles XOR 8), the float with bits 0x4B0000uu is 2^23 + u, so
+// subtracting 2^23 + 8 leaves q exactly.
+struct OpW4 {
+  using TA = uint8_t;
+  using TX = __nv_bfloat16;
+  static constexpr int VEC = 32;
+  static constexpr int XCH = 4;
+  static constexpr int EPB = 2;
+  static constexpr bool GROUPED = true;
+  // word a (elements 8w .. 8w+7) against their 8 bf16 x values
+  __device__ static __forceinline__ void word(float2 &acc, uint32_t a, const uint4 &xw) {
+    const uint32_t f = a ^ 0x88888888u;
+    const uint32_t lo = f & 0x0F0F0F0Fu;          // elements 0, 2, 4, 6 in bytes 0..3
+    const uint32_t hi = (f >> 4) & 0x0F0F0F0Fu;   // elements 1, 3, 5, 7
+    const float2 mg = make_float2(-8388616.0f, -8388616.0f);
+    const uint32_t xw4[4] = {xw.x, xw.y, xw.z, xw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 q = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540 + j)),
+                                              __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540 + j))),
+                                  mg);
+      acc = __ffma2_rn(q, make_float2(bf16_lo(xw4[j]), bf16_hi(xw4[j])), acc);
+    }
+  }
+  __device__ static __forceinline__ void dot(float &e, float &o, const uint4 &a, const uint4 *xv) {
+    float2 acc = make_float2(e, o);
+    word(acc, a.x, xv[0]);
+    word(acc, a.y, xv[1]);
+    word(acc, a.z, xv[2]);
+    word(acc, a.w, xv[3]);
+    e = acc.x;
+    o = acc.y;
+  }
+  // element k of the row starting at byte `row` (unscaled)
+  __device__ static __forceinline__ float nibble(const void *A, int64_t row_byte, int64_t k) {
+    const uint32_t b = __ldg(reinterpret_cast<const unsigned char *>(A) + row_byte + (k >> 1));
+    const int v = (int)((k & 1) ? (b >> 4) : (b & 15u));
+    return (float)(v >= 8 ? v - 16 : v);
+  }
+  __device__ static __forceinline__ float x_elem(const void *x, int64_t i) {
+    return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16 *>(x) + i));
+  }
+  __device__ static __forceinline__ void store(void *y, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+// Bytes of one row of A.
+template <class Op>
+__device__ __forceinline__ int64_t row_bytes(int64_t K) {
+  return K * (int64_t)sizeof(typename Op::TA) / Op::EPB;
+}
+
+// The group scale of 16-byte chunk c of row `row` (1 for the ungrouped types).
+template <class Op>
+__device__ __forceinline__ float chunk_scale(const Args &a, int64_t row, int64_t c) {
+  if constexpr (Op::GROUPED) {
+    return __ldg(a.gscale + row * (a.K >> a.gshift) + ((c * Op::VEC) >> a.gshift));
+  } else {
+    return 1.f;
+  }
+}
+
+// One chunk's products added to (e, o); a grouped type sums the chunk first and
+// scales it once.
+template <class Op>
+__device__ __forceinline__ void dot_chunk(float &e, float &o, const uint4 &av, const uint4 *xv, float gs) {
+  if constexpr (Op::GROUPED) {
+    float le = 0.f, lo = 0.f;
+    Op::dot(le, lo, av, xv);
+    e = fmaf(gs, le, e);
+    o = fmaf(gs, lo, o);
+  } else {
+    Op::dot(e, o, av, xv);
+  }
+}
+
+// Element (row, k) of A as a float, with its group scale (element-load paths).
+template <class Op>
+__device__ __forceinline__ float a_value(const Args &a, int64_t row, int64_t k) {
+  if constexpr (Op::GROUPED) {
+    return __ldg(a.gscale + row * (a.K >> a.gshift) + (k >> a.gshift)) *
+           Op::nibble(a.A, row * (a.K >> 1), k);
+  } else {
+    return Op::a_elem(a.A, row * a.K + k);
+  }
+}
 
 // bias is stored in the output type: fp32 for OpF32, otherwise the x type.
 template <class Op>
@@ -449,15 +553,17 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
 
     if (VEC) {
       const int64_t nch = live ? K / Op::VEC : 0;
-      const char *arow = reinterpret_cast<const char *>(a.A) + row * K * (int64_t)sizeof(typename Op::TA);
+      const char *arow = reinterpret_cast<const char *>(a.A) + row * row_bytes<Op>(K);
       const char *xb0 = reinterpret_cast<const char *>(a.x);
       const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
       for (int64_t c0 = sub; c0 < nch; c0 += (int64_t)TPR * U) {
         uint4 av[U];
+        float gs[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t c = c0 + (int64_t)u * TPR;
           av[u] = (c < nch) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
+          gs[u] = (c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -469,7 +575,7 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
                 uint4 xv[Op::XCH];
 #pragma unroll
                 for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
-                Op::dot(e[b], o[b], av[u], xv);
+                dot_chunk<Op>(e[b], o[b], av[u], xv, gs[u]);
               }
             }
           }
@@ -478,7 +584,7 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
     } else {
       const int64_t kend = live ? K : 0;
       for (int64_t k = sub; k < kend; k += TPR) {
-        const float av = Op::a_elem(a.A, row * K + k);
+        const float av = a_value<Op>(a, row, k);
 #pragma unroll
         for (int b = 0; b < NB; ++b)
           if (b < B) e[b] = fmaf(av, Op::x_elem(a.x, (int64_t)b * K + k), e[b]);
@@ -521,16 +627,18 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
   const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
 
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-    const char *arow = reinterpret_cast<const char *>(a.A) + row * K * (int64_t)sizeof(typename Op::TA);
+    const char *arow = reinterpret_cast<const char *>(a.A) + row * row_bytes<Op>(K);
     float e[NB], o[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
     for (int64_t c0 = c_lo + tid; c0 < c_hi; c0 += (int64_t)kThreads * U) {
       uint4 av[U];
+      float gs[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + (int64_t)u * kThreads;
         av[u] = (c < c_hi) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
+        gs[u] = (c < c_hi) ? chunk_scale<Op>(a, row, c) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -542,7 +650,7 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
               uint4 xv[Op::XCH];
 #pragma unroll
               for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
-              Op::dot(e[b], o[b], av[u], xv);
+              dot_chunk<Op>(e[b], o[b], av[u], xv, gs[u]);
             }
           }
         }
@@ -731,7 +839,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   const uint64_t pol = evict_first_policy();
   const int64_t nch = K / Op::VEC;
   const int64_t rstride = (int64_t)gridDim.x * WARPS;
-  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const int64_t rowb = row_bytes<Op>(K);
   const char *A = reinterpret_cast<const char *>(a.A);
 
   // `row` and `base` (first chunk of the current load group) are the same in all
@@ -752,11 +860,13 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   int64_t base = 0;
   float gate_val = 0.f;
   uint4 buf[U];
+  float gbuf[U];  // group scales of the chunks in buf (int4)
   // prologue: first group of the first row
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int64_t c = base + lane + 32 * u;
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+    gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
   }
   // The epilogue operands of the CTA's first THREADS rows (pairs with SW) are
   // staged in shared memory while those loads are in flight, so that no row waits
@@ -785,8 +895,12 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     float e = 0.f, o = 0.f;
     for (;;) {
       uint4 cur[U];
+      float gcur[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) cur[u] = buf[u];
+      for (int u = 0; u < U; ++u) {
+        cur[u] = buf[u];
+        gcur[u] = gbuf[u];
+      }
       const int64_t cc = base + lane;
       // next group: same row, or the first group of this warp's next row (whose
       // epilogue operand is fetched with it)
@@ -797,6 +911,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
       for (int u = 0; u < U; ++u) {
         const int64_t c = base + lane + 32 * u;
         buf[u] = (row_live(nrow) && c < nch) ? ld_stream16(A + nrow * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
+        gbuf[u] = (row_live(nrow) && c < nch) ? chunk_scale<Op>(a, nrow, c) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -806,7 +921,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
 #pragma unroll
           for (int h = 0; h < Op::XCH; ++h)
             xv[h] = XS ? *reinterpret_cast<const uint4 *>(xb + c * XB + h * 16) : ld_x16(xb + c * XB + h * 16);
-          Op::dot(e, o, cur[u], xv);
+          dot_chunk<Op>(e, o, cur[u], xv, gcur[u]);
         }
       }
       if (nrow != row) break;

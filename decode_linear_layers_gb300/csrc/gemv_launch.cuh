@@ -40,6 +40,9 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
 
 template <class Op, int NB>
 cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  if constexpr (Op::GROUPED) {
+    return cudaErrorInvalidValue;  // not built for int4; the planner never picks it
+  } else {
   constexpr int T = kBatchedThreads;
   const dim3 grid((unsigned)p.grid), block(T);
   if constexpr (NB <= 4) {
@@ -64,6 +67,7 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
     return cudaSuccess;
+  }
   }
 }
 
@@ -132,10 +136,11 @@ cudaError_t launch(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t 
   }
 }
 
-// Defined in gemv_f32.cu, gemv_f16.cu, gemv_bf16.cu, gemv_w8.cu.
+// Defined in gemv_f32.cu, gemv_f16.cu, gemv_bf16.cu, gemv_w8.cu, gemv_w4.cu.
 cudaError_t launch_f32(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
 cudaError_t launch_f16(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
 cudaError_t launch_bf16(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
 cudaError_t launch_w8(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
+cudaError_t launch_w4(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s);
 
 }  // namespace gemv

@@ -42,11 +42,21 @@ int elem_bytes_a(int dtype) {
     case GEMV_DTYPE_F32: return 4;
     case GEMV_DTYPE_F16:
     case GEMV_DTYPE_BF16: return 2;
-    default: return 1;
+    default: return 1;  // int8; int4 packs two elements per byte
   }
 }
 
 int elem_bytes_x(int dtype) { return dtype == GEMV_DTYPE_F32 ? 4 : 2; }
+
+int chunk_elems(int dtype) {
+  switch (dtype) {
+    case GEMV_DTYPE_F32: return 4;
+    case GEMV_DTYPE_F16:
+    case GEMV_DTYPE_BF16: return 8;
+    case GEMV_DTYPE_W8: return 16;
+    default: return 32;  // int4: two per byte
+  }
+}
 
 static bool rowteam_lanes_ok(int l) { return l == 1 || l == 2 || l == 4 || l == 8 || l == 16; }
 
@@ -61,7 +71,7 @@ static int batched_staging(int nb, int64_t K, int sx) {
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out) {
   if (out == nullptr || num_sms < 1) return GEMV_ERR_INVALID_VALUE;
-  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W8) return GEMV_ERR_INVALID_VALUE;
+  if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W4) return GEMV_ERR_INVALID_VALUE;
   if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
   if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
   gemv_plan_t p = {};
@@ -72,12 +82,13 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
     *out = p;
     return GEMV_SUCCESS;
   }
-  const int sa = elem_bytes_a(dtype), sx = elem_bytes_x(dtype);
-  const int vec = 16 / sa;
+  const int sx = elem_bytes_x(dtype);
+  const int vec = chunk_elems(dtype);
   const bool vec_ok = aligned16 && (K % vec == 0);
   const int64_t nch = vec_ok ? K / vec : 0;
   p.nb = next_pow2(B);
-  const int bstage = batched_staging(p.nb, K, sx);
+  // the batched shared-memory kernels are not built for int4 (grouped scales)
+  const int bstage = dtype == GEMV_DTYPE_W4 ? -1 : batched_staging(p.nb, K, sx);
 
   int kernel = GEMV_KERNEL_AUTO;
   int param = 0;

@@ -23,6 +23,8 @@ constexpr int kUnrollBlockRow = 4;
 
 int elem_bytes_a(int dtype);
 int elem_bytes_x(int dtype);
+// Elements of A in one 16-byte chunk.
+int chunk_elems(int dtype);
 
 // Defined in gemv_api.cu.
 void record_cuda_error(int e);

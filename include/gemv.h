@@ -78,8 +78,13 @@ typedef enum gemv_dtype {
   GEMV_DTYPE_F32 = 0,  /* A, x, bias, y: fp32 */
   GEMV_DTYPE_F16 = 1,  /* A, x, bias, y: IEEE binary16 */
   GEMV_DTYPE_BF16 = 2, /* A, x, bias, y: bfloat16 */
-  GEMV_DTYPE_W8 = 3    /* A: int8 + fp32 row scale; x, bias, y: bfloat16 */
+  GEMV_DTYPE_W8 = 3,   /* A: int8 + fp32 row scale; x, bias, y: bfloat16 */
+  GEMV_DTYPE_W4 = 4    /* A: int4, two per byte, + fp32 scale per group of
+                          GEMV_W4_GROUP elements; x, bias, y: bfloat16 */
 } gemv_dtype_t;
+
+/* Elements of a row that share one int4 scale. */
+#define GEMV_W4_GROUP 128
 
 /* Maximum number of decode vectors per call. */
 #define GEMV_MAX_BATCH 16
@@ -100,6 +105,21 @@ gemv_status_t gemv_bf16(const uint16_t *A, const uint16_t *x, const uint16_t *bi
  * y[b][m] = row_scale[m] * sum_k A[m][k] x[b][k] + bias[m]; the int8 values are
  * widened to fp32 in registers (NPU MatMul post, sections 1.2 and 5.2). */
 gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x,
+                      const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
+                      gemv_stream_t stream);
+
+/* Weight-only int4 (NPU MatMul post, section 5.2: int4 halves the weight bytes of
+ * int8 again; scales, fp32 accumulation).  A holds M x K int4 values as M x K/2
+ * bytes, row-major; element k of row m is the low nibble of byte m*K/2 + k/2 for
+ * even k and the high nibble for odd k, symmetric two's complement in [-8, 7].
+ * group_scale is M x K/GEMV_W4_GROUP fp32: one scale per group of GEMV_W4_GROUP
+ * consecutive elements of a row.  x, bias, y are bf16.
+ *     y[b][m] = sum_k group_scale[m][k / GEMV_W4_GROUP] * A[m][k] * x[b][k] + bias[m]
+ * Each 16-byte chunk (32 weights, inside one group) is summed in fp32 and scaled
+ * once.  K must be a multiple of GEMV_W4_GROUP (GEMV_ERR_INVALID_VALUE otherwise);
+ * group_scale is required when M * K > 0.  B >= 2 runs the warp-per-row kernels
+ * (the batched shared-memory kernels are for the other types). */
+gemv_status_t gemv_w4(const uint8_t *A, const float *group_scale, const uint16_t *x,
                       const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
                       gemv_stream_t stream);
 
@@ -134,8 +154,9 @@ typedef enum gemv_activation {
 } gemv_activation_t;
 
 /* y[b][m] = act(s_m * sum_k A[m][k] x[b][k] + bias[m]) + residual[b][m]
- * Any storage type (`dtype`); row_scale only (and required) for GEMV_DTYPE_W8,
- * NULL otherwise.  residual is B x M in y's type, may be NULL, and may be y itself
+ * Any storage type (`dtype`); row_scale only (and required) for GEMV_DTYPE_W8
+ * (M scales) and GEMV_DTYPE_W4 (the M x K/GEMV_W4_GROUP group scales), NULL
+ * otherwise.  residual is B x M in y's type, may be NULL, and may be y itself
  * (in place: y += act(A x + bias)); it must not otherwise overlap y.  The kernel
  * choice, layouts and errors are those of the plain entry points. */
 gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
@@ -150,7 +171,8 @@ gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale,
  * One launch; the gate and up sums of an output meet in registers, so the 2I
  * intermediate values never reach memory.  Needs 16-byte aligned rows with at least
  * one 16-byte chunk per lane of a warp, and for B > 1 x[0..B) small enough to stage
- * in shared memory; otherwise GEMV_ERR_UNSUPPORTED and nothing is launched. */
+ * in shared memory and a storage type other than GEMV_DTYPE_W4; otherwise
+ * GEMV_ERR_UNSUPPORTED and nothing is launched. */
 gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
                           const void *bias, void *y, int64_t I, int64_t K, int B,
                           gemv_stream_t stream);

@@ -22,8 +22,9 @@ import decode_linear_layers_gb300 as g
 import oracle
 import workloads as W
 
-TOL = {"f32": (1e-5, 1e-6), "f16": (2e-3, 1e-3), "bf16": (2e-3, 1e-3), "w8": (2e-3, 1e-3)}
-U_OUT = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8, "w8": 2.0 ** -8}
+TOL = {"f32": (1e-5, 1e-6), "f16": (2e-3, 1e-3), "bf16": (2e-3, 1e-3), "w8": (2e-3, 1e-3),
+       "w4": (2e-3, 1e-3)}
+U_OUT = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8, "w8": 2.0 ** -8, "w4": 2.0 ** -8}
 
 
 def threads() -> int:
@@ -44,12 +45,15 @@ def to_device(inp: dict, dev="cuda") -> dict:
 
 
 def out_dtype(dtype: str):
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "w8": torch.bfloat16}[dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "w8": torch.bfloat16,
+            "w4": torch.bfloat16}[dtype]
 
 
 def call(dtype: str, d: dict, y: torch.Tensor, M: int, K: int, B: int, stream=None):
     if dtype == "w8":
         g.gemv_w8(d["A"], d["scale"], d["x"], d["bias"], y, M, K, B, stream)
+    elif dtype == "w4":
+        g.gemv_w4(d["A"], d["scale"], d["x"], d["bias"], y, M, K, B, stream)
     else:
         getattr(g, f"gemv_{dtype}")(d["A"], d["x"], d["bias"], y, M, K, B, stream)
 

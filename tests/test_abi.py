@@ -232,3 +232,29 @@ def test_plan_grid_never_exceeds_cap():
             for B in (1, 4, 16):
                 p = g.plan_for("bf16", M, Kd, B, num_sms=152)
                 assert 1 <= p["grid"] <= max(M, 152 * 32)
+
+
+def test_w4_host_checks():
+    w4 = g.lib().gemv_w4
+    assert w4(None, None, None, None, None, 0, 256, 2, None) == 0            # M == 0: no-op
+    assert w4(P, P + 64, P + 4096, None, P + 8192, 4, 100, 1, None) == 1     # K % 128 != 0
+    assert w4(P, None, P + 4096, None, P + 8192, 4, 256, 1, None) == 1       # scales required
+    assert w4(P, P + 64, P + 4096, None, P + 8192, 4, 256, 17, None) == 2    # B > 16
+    assert w4(P, P + 66, P + 4096, None, P + 8192, 4, 256, 1, None) == 1     # scales not 4-byte aligned
+    # y over the group scales (4 rows x 2 groups x 4 bytes at P + 8192)
+    assert w4(P, P + 8192, P + 4096, None, P + 8200, 4, 256, 1, None) == 1
+    # a row scale only for the int types
+    assert g.lib().gemv_ex(2, P, P + 64, P + 4096, None, None, P + 8192, 4, 256, 1, 0, None) == 1
+
+
+def test_plan_w4():
+    K = g.KERNELS
+    p = g.plan_for("w4", 8192, 8192, 1)
+    assert p["kernel"] == K["stream"] and p["x_staging"] == 1 and p["smem_bytes"] == 8192 * 2
+    for B in (2, 4, 9, 16):  # no batched shared-memory kernel for int4
+        assert g.plan_for("w4", 8192, 8192, B)["kernel"] == K["warp_per_row"]
+    # 32 weights per 16-byte chunk: K = 256 is 8 chunks -> 8 lanes per row
+    p = g.plan_for("w4", 1000, 256, 1)
+    assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 8
+    assert g.plan_for("w4", 100, 4096, 1, aligned16=False)["kernel"] == K["scalar"]
+    assert g.plan_for("w4", 8, 1 << 20, 1)["kernel"] == K["split_k"]

@@ -29,6 +29,7 @@ _BLOCK = 1 << 22
 _S_A, _S_X, _S_BIAS, _S_SCALE = 1, 2, 3, 4
 
 DTYPES = ("f32", "f16", "bf16", "w8")
+W4_GROUP = 128  # int4: elements of a row per scale
 
 # storage element sizes in bytes: (A, x, y, bias)
 ELEM_BYTES = {
@@ -36,6 +37,7 @@ ELEM_BYTES = {
     "f16": (2, 2, 2, 2),
     "bf16": (2, 2, 2, 2),
     "w8": (1, 2, 2, 2),
+    "w4": (0.5, 2, 2, 2),   # two int4 per byte
 }
 
 
@@ -112,15 +114,15 @@ def to_storage(a: np.ndarray, dt: str) -> torch.Tensor:
 class Workload:
     """One GEMV problem: shapes, storage dtype and input distributions."""
     name: str
-    dtype: str            # "f32" | "f16" | "bf16" | "w8"
+    dtype: str            # "f32" | "f16" | "bf16" | "w8" | "w4"
     M: int
     K: int
     B: int
     bias: bool
-    a_dist: tuple         # ("normal", sigma) | ("uniform", lo, hi) | ("int8", lo, hi)
+    a_dist: tuple         # ("normal", sigma) | ("uniform", lo, hi) | ("int8", lo, hi) | ("bytes",)
     x_dist: tuple
     bias_dist: tuple = ("normal", 1.0)
-    scale_dist: tuple = ("uniform", 1e-3, 1e-2)   # w8 only
+    scale_dist: tuple = ("uniform", 1e-3, 1e-2)   # w8 (per row), w4 (per group)
     seed: int = 0
 
     @property
@@ -144,6 +146,8 @@ def _draw(dist: tuple, n: int, seed: int, stream: int) -> np.ndarray:
         return uniform(n, dist[1], dist[2], seed, stream)
     if kind == "int8":
         return int8_uniform(n, dist[1], dist[2], seed, stream)
+    if kind == "bytes":  # uniform storage bytes: for int4, both nibbles uniform in [-8, 7]
+        return int8_uniform(n, -128, 127, seed, stream).view(np.uint8)
     raise ValueError(f"unknown distribution {dist!r}")
 
 
@@ -151,11 +155,18 @@ def make_inputs(w: Workload) -> dict:
     """CPU tensors in storage dtype, drawn in the fixed order A, x, bias, scale.
 
     Returns {"A": (M,K), "x": (B,K), "bias": (M,) or None, "scale": (M,) fp32 or None}.
-    For "w8", A is int8 and x / bias are bf16.
+    For "w8", A is int8 and x / bias are bf16.  For "w4", A is (M, K/2) uint8 (two
+    int4 per byte) and scale is (M, K/W4_GROUP) fp32.
     """
-    xdt = "bf16" if w.dtype == "w8" else w.dtype
-    a = _draw(w.a_dist, w.M * w.K, w.seed, _S_A)
-    if w.dtype == "w8":
+    xdt = "bf16" if w.dtype in ("w8", "w4") else w.dtype
+    if w.dtype == "w4":
+        a = _draw(w.a_dist, w.M * w.K // 2, w.seed, _S_A)
+        A = torch.from_numpy(a.astype(np.uint8, copy=False)).reshape(w.M, w.K // 2)
+    else:
+        a = _draw(w.a_dist, w.M * w.K, w.seed, _S_A)
+    if w.dtype == "w4":
+        pass  # A is already the packed bytes
+    elif w.dtype == "w8":
         A = torch.from_numpy(a.astype(np.int8, copy=False)).reshape(w.M, w.K)
     else:
         A = to_storage(a, w.dtype).reshape(w.M, w.K)
@@ -166,6 +177,9 @@ def make_inputs(w: Workload) -> dict:
     scale = None
     if w.dtype == "w8":
         scale = torch.from_numpy(_draw(w.scale_dist, w.M, w.seed, _S_SCALE))
+    elif w.dtype == "w4":
+        ng = w.K // W4_GROUP
+        scale = torch.from_numpy(_draw(w.scale_dist, w.M * ng, w.seed, _S_SCALE)).reshape(w.M, ng)
     return {"A": A, "x": x, "bias": bias, "scale": scale}
 
 
@@ -190,13 +204,16 @@ def qmin_bytes(dtype: str, M: int, K: int, B: int) -> int:
     "minimum bytes" model (m*k + k*n + m*n)*s with one element size per operand.
     """
     sa, sx, sy, _ = ELEM_BYTES[dtype]
-    return M * K * sa + B * K * sx + B * M * sy
+    a_bytes = M * K // 2 if dtype == "w4" else M * K * sa
+    return a_bytes + B * K * sx + B * M * sy
 
 
 def full_bytes(dtype: str, M: int, K: int, B: int, bias: bool) -> int:
-    """Q_min plus the per-row side inputs: bias (M*s_bias) and the w8 scale (4*M)."""
+    """Q_min plus the side inputs: bias (M*s_bias), the w8 row scale (4*M) and the
+    w4 group scales (4*M*K/W4_GROUP)."""
     _, _, _, sb = ELEM_BYTES[dtype]
     extra = (M * sb if bias else 0) + (4 * M if dtype == "w8" else 0)
+    extra += 4 * M * (K // W4_GROUP) if dtype == "w4" else 0
     return qmin_bytes(dtype, M, K, B) + extra
 
 
@@ -230,7 +247,15 @@ def _cfgs() -> list[Workload]:
 
 
 CONFIGS: list[Workload] = _cfgs()
-BY_NAME = {w.name: w for w in CONFIGS}
+
+# int4 weights with group-wise scales (the next storage type after int8): the
+# int8 shapes, and a Llama-3-8B FFN shape.
+W4_CONFIGS: list[Workload] = [
+    Workload("w4_8192x8192_b1_bias", "w4", 8192, 8192, 1, True, ("bytes",), ("normal", 1.0)),
+    Workload("w4_8192x8192_b4_bias", "w4", 8192, 8192, 4, True, ("bytes",), ("normal", 1.0)),
+    Workload("w4_14336x4096_b1", "w4", 14336, 4096, 1, False, ("bytes",), ("normal", 1.0)),
+]
+BY_NAME = {w.name: w for w in CONFIGS + W4_CONFIGS}
 
 # The fp32 sweep over K at M = 16384 with bias: the benchmark's headline workload
 # (one step = the three GEMVs back to back).
@@ -243,6 +268,8 @@ def small(dtype: str, M: int, K: int, B: int, bias: bool, seed: int = 0) -> Work
         a = ("normal", float(np.sqrt(1.0 / max(K, 1))))
     elif dtype == "w8":
         a = ("int8", -127, 127)
+    elif dtype == "w4":
+        a = ("bytes",)
     else:
         a = ("normal", 0.02)
     return Workload(f"{dtype}_{M}x{K}_b{B}{'_bias' if bias else ''}_s{seed}", dtype,
