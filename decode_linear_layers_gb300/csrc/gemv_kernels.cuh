@@ -828,13 +828,6 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t M = a.M, K = a.K;
   constexpr int XB = Op::XCH * 16;
-  if (XS) {
-    const int64_t n16 = K * (int64_t)sizeof(typename Op::TX) / 16;
-    const char *src = reinterpret_cast<const char *>(a.x);
-    for (int64_t i = threadIdx.x; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-  }
   const unsigned char *xb = XS ? xs : reinterpret_cast<const unsigned char *>(a.x);
   const uint64_t pol = evict_first_policy();
   const int64_t nch = K / Op::VEC;
@@ -868,10 +861,18 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
     gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
   }
+  // x is copied into shared memory (as stored) while those loads are in flight;
+  // one barrier below covers it and the epilogue operands.
+  if (XS) {
+    const int64_t n16 = nch * Op::XCH;
+    const char *src = reinterpret_cast<const char *>(a.x);
+    for (int64_t i = threadIdx.x; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   // The epilogue operands of the CTA's first THREADS rows (pairs with SW) are
-  // staged in shared memory while those loads are in flight, so that no row waits
-  // on a bias, scale or residual load after its reduction.  The j-th row of warp w
-  // is unit t = w + WARPS * j of the CTA: row (or pair) blockIdx.x + gridDim.x * t.
+  // staged in shared memory too, so that no row waits on a bias, scale or residual
+  // load after its reduction.  The j-th row of warp w is unit t = w + WARPS * j of
+  // the CTA: row (or pair) blockIdx.x + gridDim.x * t.
   __shared__ float ops[4][THREADS];
   const bool staged = a.bias != nullptr || a.scale != nullptr || a.residual != nullptr;
   if (staged) {
@@ -889,8 +890,9 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
         ops[2][t] = a.residual != nullptr ? residual_at<Op>(a.residual, r) : 0.f;
       }
     }
-    __syncthreads();
   }
+  if (XS) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (XS || staged) __syncthreads();
   while (row_live(row)) {
     float e = 0.f, o = 0.f;
     for (;;) {
