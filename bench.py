@@ -142,7 +142,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return
@@ -360,6 +360,9 @@ def run_ours(args, rank, world, local_rank):
                    "dtype": "f32", "l2": "flushed before every GEMV (write then read of a 2x L2 buffer)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "per_gemv_us": {w.name: round(t * 1e3, 3) for w, t in zip(head, per_gemv_ms)},
+        # the distribution behind each mean: one slow launch moves a mean of 200
+        "per_gemv_us_median": {w.name: round(statistics.median(t) * 1e3, 3) for w, t in zip(head, times)},
+        "per_gemv_us_max": {w.name: round(max(t) * 1e3, 3) for w, t in zip(head, times)},
         "per_gemv_kernel": {w.name: p["kernel_name"] for w, p in zip(head, plans)},
         "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed_region": round(t1 - t0, 3),

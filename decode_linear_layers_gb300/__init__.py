@@ -33,8 +33,8 @@ ACT_NONE, ACT_SILU = 0, 1
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3, "w4": 4}
 W4_GROUP = 128  # elements of a row that share one int4 scale
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
-           "split_k": 4, "batched": 5, "scalar": 6, "stream": 7}
-X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32"}
+           "split_k": 4, "batched": 5, "scalar": 6, "stream": 7, "xsplit": 8}
+X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32", 3: "regs"}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
 

@@ -228,7 +228,7 @@ int gemv_last_cuda_error(void) { return t_last_cuda_error; }
 uint64_t gemv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 gemv_status_t gemv_test_force_kernel(int kernel, int param) {
-  if (kernel < GEMV_KERNEL_AUTO || kernel > GEMV_KERNEL_STREAM || param < 0)
+  if (kernel < GEMV_KERNEL_AUTO || kernel > GEMV_KERNEL_XSPLIT || param < 0)
     return GEMV_ERR_INVALID_VALUE;
   g_force_kernel = kernel;
   g_force_param = kernel == GEMV_KERNEL_AUTO ? 0 : param;

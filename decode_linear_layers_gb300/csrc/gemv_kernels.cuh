@@ -476,11 +476,16 @@ __device__ __forceinline__ void store_act_res(const Args &a, int64_t i, float v,
   Op::store(a.y, i, v);
 }
 
+// (The residual is read after the arithmetic, through the read-only path: each
+// output is read and then written by the one thread that owns it and by no other,
+// so even in place the value read is the caller's.)
 template <class Op>
 __device__ __forceinline__ void epilogue_store(const Args &a, int b, int64_t m, float acc) {
+  float v = row_value<Op>(a, m, acc);
+  if (a.act == 1) v = silu(v);
   const int64_t i = (int64_t)b * a.M + m;
-  const float res = a.residual != nullptr ? residual_at<Op>(a.residual, i) : 0.f;
-  store_act_res<Op>(a, i, row_value<Op>(a, m, acc), res);
+  if (a.residual != nullptr) v += Op::x_elem(a.residual, i);
+  Op::store(a.y, i, v);
 }
 
 // A row's epilogue operands, loaded when the row's first A loads are issued so
@@ -546,7 +551,9 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
   for (int64_t base = (int64_t)blockIdx.x * TEAMS; base < M; base += (int64_t)gridDim.x * TEAMS) {
     const int64_t row = base + team;
     const bool live = row < M;
-    const RowPre pre = row_pre<Op, NB == 1>(a, row, live);
+    // operands loaded ahead of the A loads (not for fp32 rows: measured slower there)
+    constexpr bool kPre = sizeof(typename Op::TA) != 4;
+    const RowPre pre = kPre ? row_pre<Op, NB == 1>(a, row, live) : RowPre{1.f, 0.f, 0.f};
     float e[NB], o[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
@@ -558,12 +565,12 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
       const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
       for (int64_t c0 = sub; c0 < nch; c0 += (int64_t)TPR * U) {
         uint4 av[U];
-        float gs[U];
+        float gs[Op::GROUPED ? U : 1];  // group scales (int4 only)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t c = c0 + (int64_t)u * TPR;
           av[u] = (c < nch) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
-          gs[u] = (c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
+          if constexpr (Op::GROUPED) gs[u] = (c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -575,7 +582,7 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
                 uint4 xv[Op::XCH];
 #pragma unroll
                 for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
-                dot_chunk<Op>(e[b], o[b], av[u], xv, gs[u]);
+                dot_chunk<Op>(e[b], o[b], av[u], xv, Op::GROUPED ? gs[Op::GROUPED ? u : 0] : 1.f);
               }
             }
           }
@@ -598,8 +605,12 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
       for (int b = 0; b < NB; ++b) {
         if (b < B) {
           const int64_t i = (int64_t)b * M + row;
-          const float res = NB == 1 ? pre.res : (a.residual != nullptr ? residual_at<Op>(a.residual, i) : 0.f);
-          store_act_res<Op>(a, i, row_value_pre<Op>(a, pre, e[b]), res);
+          if (kPre) {
+            const float res = NB == 1 ? pre.res : (a.residual != nullptr ? residual_at<Op>(a.residual, i) : 0.f);
+            store_act_res<Op>(a, i, row_value_pre<Op>(a, pre, e[b]), res);
+          } else {
+            epilogue_store<Op>(a, b, row, e[b]);
+          }
         }
       }
     }
@@ -633,12 +644,12 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
     for (int b = 0; b < NB; ++b) e[b] = o[b] = 0.f;
     for (int64_t c0 = c_lo + tid; c0 < c_hi; c0 += (int64_t)kThreads * U) {
       uint4 av[U];
-      float gs[U];
+      float gs[Op::GROUPED ? U : 1];  // group scales (int4 only)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + (int64_t)u * kThreads;
         av[u] = (c < c_hi) ? ld_stream16(arow + c * 16, pol) : make_uint4(0, 0, 0, 0);
-        gs[u] = (c < c_hi) ? chunk_scale<Op>(a, row, c) : 0.f;
+        if constexpr (Op::GROUPED) gs[u] = (c < c_hi) ? chunk_scale<Op>(a, row, c) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -650,7 +661,7 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
               uint4 xv[Op::XCH];
 #pragma unroll
               for (int h = 0; h < Op::XCH; ++h) xv[h] = ld_x16(xb0 + b * xstride + c * XB + h * 16);
-              dot_chunk<Op>(e[b], o[b], av[u], xv, gs[u]);
+              dot_chunk<Op>(e[b], o[b], av[u], xv, Op::GROUPED ? gs[Op::GROUPED ? u : 0] : 1.f);
             }
           }
         }
@@ -853,13 +864,13 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   int64_t base = 0;
   float gate_val = 0.f;
   uint4 buf[U];
-  float gbuf[U];  // group scales of the chunks in buf (int4)
+  float gbuf[Op::GROUPED ? U : 1];  // group scales of the chunks in buf (int4 only)
   // prologue: first group of the first row
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int64_t c = base + lane + 32 * u;
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
-    gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
+    if constexpr (Op::GROUPED) gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
   }
   // x is copied into shared memory (as stored) while those loads are in flight;
   // one barrier below covers it and the epilogue operands.
@@ -873,9 +884,12 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   // staged in shared memory too, so that no row waits on a bias, scale or residual
   // load after its reduction.  The j-th row of warp w is unit t = w + WARPS * j of
   // the CTA: row (or pair) blockIdx.x + gridDim.x * t.
-  __shared__ float ops[4][THREADS];
-  const bool staged = a.bias != nullptr || a.scale != nullptr || a.residual != nullptr;
-  if (staged) {
+  // (fp32 rows run four CTAs per SM at 32 registers: they load the operands after
+  // the reduction instead, which measured faster than the staging's extra registers)
+  constexpr bool kStage = sizeof(typename Op::TA) != 4;
+  __shared__ float ops[4][kStage ? THREADS : 1];
+  const bool staged = kStage && (a.bias != nullptr || a.scale != nullptr || a.residual != nullptr);
+  if (kStage && staged) {
     const int t = threadIdx.x;
     const int64_t r = blockIdx.x + (int64_t)gridDim.x * t;
     if (SW ? r < half : r < M) {
@@ -897,11 +911,11 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     float e = 0.f, o = 0.f;
     for (;;) {
       uint4 cur[U];
-      float gcur[U];
+      float gcur[Op::GROUPED ? U : 1];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         cur[u] = buf[u];
-        gcur[u] = gbuf[u];
+        if constexpr (Op::GROUPED) gcur[u] = gbuf[u];
       }
       const int64_t cc = base + lane;
       // next group: same row, or the first group of this warp's next row (whose
@@ -913,7 +927,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
       for (int u = 0; u < U; ++u) {
         const int64_t c = base + lane + 32 * u;
         buf[u] = (row_live(nrow) && c < nch) ? ld_stream16(A + nrow * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
-        gbuf[u] = (row_live(nrow) && c < nch) ? chunk_scale<Op>(a, nrow, c) : 0.f;
+        if constexpr (Op::GROUPED) gbuf[u] = (row_live(nrow) && c < nch) ? chunk_scale<Op>(a, nrow, c) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -923,7 +937,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
 #pragma unroll
           for (int h = 0; h < Op::XCH; ++h)
             xv[h] = XS ? *reinterpret_cast<const uint4 *>(xb + c * XB + h * 16) : ld_x16(xb + c * XB + h * 16);
-          dot_chunk<Op>(e, o, cur[u], xv, gcur[u]);
+          dot_chunk<Op>(e, o, cur[u], xv, Op::GROUPED ? gcur[Op::GROUPED ? u : 0] : 1.f);
         }
       }
       if (nrow != row) break;
@@ -931,9 +945,9 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     const float s = group_sum<32>(e + o);
     if (lane == 0) {
       const bool up = SW && row >= half;
-      const int64_t t = ((up ? row - half : row) - blockIdx.x) / gridDim.x;  // unit index in the CTA
+      const int64_t t = kStage ? ((up ? row - half : row) - blockIdx.x) / gridDim.x : 0;  // unit index in the CTA
       RowPre p{1.f, 0.f, 0.f};
-      if (staged && t < THREADS) {
+      if (kStage && staged && t < THREADS) {
         p.bias = ops[up ? 2 : 0][t];
         p.s = ops[up ? 3 : 1][t];
         if (!SW) p.res = ops[2][t];
@@ -1095,6 +1109,169 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
     }
     g = ng;
   }
+}
+
+// ------------------------------------------------------------------ k_xsplit
+// B <= 4 (NB in {1, 2, 4}): the 512 threads of a CTA split K.  Thread L (= warp *
+// 32 + lane) owns chunks c = L + 512 j (j < J) of every row and keeps x for those
+// chunks, all NB vectors, in fp32 registers for the whole kernel: x is never read
+// from shared memory and never widened twice.  A CTA takes a contiguous block of
+// rows (balanced to within one); each thread copies its own chunks of the coming
+// rows into its own shared-memory slots with cp.async, P rows per commit group and
+// G groups in flight (P * G rows, P * G * J * 8 KB per SM, at no register cost),
+// and reads back only what it copied (no barrier for A).  Per row, each warp
+// reduces its NB partial sums with a reduce-scatter butterfly and leaves them in
+// red[]; every kXsT rows one barrier, then kXsT * NB threads add the 16 warp
+// partials in warp order and run the epilogue.  Fixed orders throughout: results
+// are reproducible.
+constexpr int kXsThreads = 512;
+constexpr int kXsWarps = kXsThreads / 32;
+constexpr int kXsT = 16;  // rows per barrier (a multiple of P)
+
+// NB values per lane summed over the 32 lanes of a warp.  The first log2(NB)
+// steps halve the values each lane carries (it keeps one half and receives the
+// partner's copy of it), the rest are plain xor steps.  Lane l ends with the total
+// of value l >> (5 - log2 NB).
+template <int NB>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
+#pragma unroll
+  for (int h = NB / 2, m = 16; h >= 1; h >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = upper ? v[i] : v[i + h];
+      const float keep = upper ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int m = 16 / NB; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+  return t;
+}
+
+template <class Op, int NB, int J, int P, int G>
+__global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
+  static_assert(NB == 1 || NB == 2 || NB == 4, "NB");
+  static_assert(kXsT % P == 0, "a barrier batch is whole groups");
+  constexpr int D = P * G;  // rows in the ring
+  extern __shared__ __align__(16) unsigned char ring[];  // [D][J][512] 16-byte slots
+  __shared__ float red[2][kXsT][kXsWarps][NB];
+  constexpr int LOGNB = NB == 4 ? 2 : NB == 2 ? 1 : 0;
+  constexpr int PV = Op::VEC / 2;  // fp32 pairs per chunk
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t M = a.M, K = a.K, nch = K / Op::VEC;
+  const int B = a.B;
+  const int64_t rowb = row_bytes<Op>(K);
+  const int64_t r0 = M * blockIdx.x / gridDim.x, r1 = M * (blockIdx.x + 1) / gridDim.x;
+  const int64_t n = r1 - r0;
+  const int64_t ngroups = (n + P - 1) / P;
+  const char *A = reinterpret_cast<const char *>(a.A) + r0 * rowb;
+
+  // this thread's chunks of rows g*P .. g*P+P-1 into their slots; one commit group
+  // per call (empty past the last row, so every iteration waits on the same count)
+  auto issue = [&](int64_t gi) {
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      const int64_t i = gi * P + q;
+      if (i < n) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int64_t c = tid + (int64_t)kXsThreads * j;
+          if (c < nch) cp_async16(ring + ((size_t)((i % D) * J + j) * kXsThreads + tid) * 16, A + i * rowb + c * 16);
+        }
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) issue(gi);
+
+  float2 xr[J][NB][PV];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t c = tid + (int64_t)kXsThreads * j;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int p = 0; p < PV; ++p) {
+        const int64_t k = c * Op::VEC + 2 * p;
+        xr[j][b][p] = (c < nch && b < B) ? make_float2(Op::x_elem(a.x, (int64_t)b * K + k),
+                                                       Op::x_elem(a.x, (int64_t)b * K + k + 1))
+                                         : make_float2(0.f, 0.f);
+      }
+  }
+
+  // epilogue operands of this thread's output in the current batch (threads
+  // tid < kXsT * NB: row tid / NB of the batch, vector tid % NB), loaded when the
+  // batch starts so that they have arrived when its sums are ready
+  RowPre pre{1.f, 0.f, 0.f};
+  constexpr int V = P * NB;  // values one group reduces (row q, vector b at q * NB + b)
+  constexpr int LOGV = V == 16 ? 4 : V == 8 ? 3 : V == 4 ? 2 : V == 2 ? 1 : 0;
+  static_assert((1 << LOGV) == V && V <= 32, "P * NB must be a power of two up to 32");
+  for (int64_t gi = 0; gi < ngroups; ++gi) {
+    const int64_t i0 = gi * P;
+    if (i0 % kXsT == 0 && tid < kXsT * NB) {
+      const int64_t row = r0 + i0 + tid / NB;
+      const int b = tid % NB;
+      const bool live = row < r1 && b < B;
+      pre = row_pre<Op, false>(a, row, live);
+      if (live && a.residual != nullptr) pre.res = residual_at<Op>(a.residual, (int64_t)b * M + row);
+    }
+    asm volatile("cp.async.wait_group %0;" ::"n"(G - 1) : "memory");  // group gi has landed
+    // the group's P rows (rows past n contribute zeros), then one reduction for all
+    float v[V];
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      const int s = (int)((i0 + q) % D);
+      float2 acc[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[b] = make_float2(0.f, 0.f);
+      if (i0 + q < n) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int64_t c = tid + (int64_t)kXsThreads * j;
+          if (c < nch) {
+            const uint4 av = *reinterpret_cast<const uint4 *>(ring + ((size_t)(s * J + j) * kXsThreads + tid) * 16);
+#pragma unroll
+            for (int w = 0; w < Op::VEC / 4; ++w) {
+              float2 q01, q23;
+              Op::quad2(av, w, q01, q23);
+#pragma unroll
+              for (int b = 0; b < NB; ++b) {
+                acc[b] = __ffma2_rn(q01, xr[j][b][2 * w], acc[b]);
+                acc[b] = __ffma2_rn(q23, xr[j][b][2 * w + 1], acc[b]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) v[q * NB + b] = acc[b].x + acc[b].y;
+    }
+    issue(gi + G);  // the group's slots are free again (this thread read them above)
+    const float part = warp_reduce_scatter<V>(v, lane);
+    const int hb = (int)((i0 / kXsT) & 1);
+    if ((lane & ((32 >> LOGV) - 1)) == 0) {
+      const int idx = lane >> (5 - LOGV);
+      red[hb][(int)(i0 % kXsT) + idx / NB][warp][idx % NB] = part;
+    }
+    const int64_t ilast = min(i0 + P, n) - 1;  // the group's last real row
+    const int t = (int)(ilast % kXsT);
+    if (t == kXsT - 1 || ilast == n - 1) {
+      __syncthreads();
+      if (tid < (t + 1) * NB) {
+        const int rr = tid / NB, b = tid % NB;
+        if (b < B) {
+          float sum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kXsWarps; ++w) sum += red[hb][rr][w][b];
+          store_act_res<Op>(a, (int64_t)b * M + r0 + (ilast - t) + rr, row_value_pre<Op>(a, pre, sum), pre.res);
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 }  // namespace gemv

@@ -90,6 +90,29 @@ cudaError_t launch_stream(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
   return cudaSuccess;
 }
 
+template <class Op, int NB, int J>
+cudaError_t launch_xsplit_j(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  if constexpr (Op::GROUPED || (NB != 1 && NB != 2 && NB != 4) || J * NB * Op::VEC > kXsplitMaxXRegs) {
+    return cudaErrorInvalidValue;  // not built; the planner never picks it
+  } else {
+    auto kern = k_xsplit<Op, NB, J, xsplit_rows_per_group(J), kXsplitGroups>;
+    cudaError_t e = allow_smem(kern, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)p.grid), dim3(kXsThreads), (size_t)p.smem_bytes, s>>>(a);
+    return cudaSuccess;
+  }
+}
+
+template <class Op, int NB>
+cudaError_t launch_xsplit(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+  switch (p.unroll) {
+    case 1: return launch_xsplit_j<Op, NB, 1>(p, a, s);
+    case 2: return launch_xsplit_j<Op, NB, 2>(p, a, s);
+    case 4: return launch_xsplit_j<Op, NB, 4>(p, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <class Op, int NB>
 cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
   switch (p.kernel) {
@@ -119,6 +142,8 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
     case GEMV_KERNEL_STREAM:
       if constexpr (NB == 1) return launch_stream<Op>(p, a, s);
       return cudaErrorInvalidValue;
+    case GEMV_KERNEL_XSPLIT:
+      return launch_xsplit<Op, NB>(p, a, s);
     default:
       return cudaErrorInvalidValue;
   }

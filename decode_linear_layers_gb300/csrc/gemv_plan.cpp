@@ -11,6 +11,8 @@
 // the thresholds come from timing every kernel on the GB300 configurations):
 //   rows not 16-byte aligned              -> SCALAR (element loads)
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
+//   fp32/fp16/bf16, B in 2..4, x slice fits 64 registers, at least 16 rows
+//     per SM and M < 65536               -> XSPLIT (K split over a CTA)
 //   B >= 2 and x[0..B) fits in smem       -> BATCHED
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
 //   B == 1 and at least 16 rows per SM    -> STREAM (persistent warps)
@@ -89,6 +91,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   p.nb = next_pow2(B);
   // the batched shared-memory kernels are not built for int4 (grouped scales)
   const int bstage = dtype == GEMV_DTYPE_W4 ? -1 : batched_staging(p.nb, K, sx);
+  // XSPLIT: chunks per thread J (a power of two up to 4) and x registers
+  const int xs_j = vec_ok && nch > 0 ? next_pow2(ceil_div(nch, kXsplitThreads)) : 0;
+  const bool xs_ok = vec_ok && dtype != GEMV_DTYPE_W4 && p.nb <= 4 && xs_j >= 1 && xs_j <= 4 &&
+                     xs_j * p.nb * vec <= kXsplitMaxXRegs;
 
   int kernel = GEMV_KERNEL_AUTO;
   int param = 0;
@@ -112,6 +118,9 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       case GEMV_KERNEL_STREAM:
         ok = vec_ok && B == 1;
         break;
+      case GEMV_KERNEL_XSPLIT:
+        ok = xs_ok;
+        break;
       case GEMV_KERNEL_SCALAR:
         ok = force_param == 0 || force_param == 4 || force_param == 32;
         break;
@@ -129,6 +138,11 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       kernel = GEMV_KERNEL_SCALAR;
     } else if (nch <= 16) {
       kernel = GEMV_KERNEL_ROWS_PER_WARP;
+    } else if (xs_ok && dtype != GEMV_DTYPE_W8 && B > 1 && M >= (int64_t)num_sms * 16 && M < 65536) {
+      // float types with 2..4 vectors: K split over a CTA, x in registers (the int8
+      // decode is cheaper in the row-per-warp kernels; with one vector the
+      // streaming kernel is as fast and needs no 128 KB shared-memory carve-out)
+      kernel = GEMV_KERNEL_XSPLIT;
     } else if (B > 1 && bstage >= 0 && nch >= 32) {
       kernel = GEMV_KERNEL_BATCHED;
     } else if (M >= 65536) {
@@ -205,6 +219,17 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       p.unroll = r == 4 ? 1 : 2;
       p.smem_bytes = (int)((int64_t)p.nb * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
       p.grid = num_sms;
+      break;
+    }
+    case GEMV_KERNEL_XSPLIT: {
+      // one 512-thread CTA per SM (at most one per row) over a contiguous block of
+      // rows; each thread J chunks of every row, x in registers
+      p.lanes_per_row = kXsplitThreads;
+      p.threads = kXsplitThreads;
+      p.unroll = xs_j;
+      p.x_staging = GEMV_X_REGS;
+      p.smem_bytes = xsplit_depth(xs_j) * xs_j * kXsplitThreads * 16;
+      p.grid = M < num_sms ? M : num_sms;
       break;
     }
     case GEMV_KERNEL_STREAM: {

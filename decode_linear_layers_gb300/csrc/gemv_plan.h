@@ -21,6 +21,15 @@ constexpr int kStreamThreads = 512;
 constexpr int kUnrollWarpRow = 4;
 constexpr int kUnrollBlockRow = 4;
 
+// XSPLIT: 512 threads split K; J chunks per thread; rows stream through a
+// cp.async ring of 16 / J rows (P rows per commit group, 4 groups in flight), so
+// the ring is 16 * 8 KB = 128 KB for every J; x slice <= 64 fp32 registers.
+constexpr int kXsplitThreads = 512;
+constexpr int kXsplitMaxXRegs = 64;
+constexpr int kXsplitGroups = 4;
+constexpr int xsplit_rows_per_group(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
+constexpr int xsplit_depth(int J) { return xsplit_rows_per_group(J) * kXsplitGroups; }
+
 int elem_bytes_a(int dtype);
 int elem_bytes_x(int dtype);
 // Elements of A in one 16-byte chunk.

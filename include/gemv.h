@@ -200,14 +200,18 @@ typedef enum gemv_kernel {
   GEMV_KERNEL_SPLIT_K = 4,       /* CTAs over K slices + fixed-order second pass */
   GEMV_KERNEL_BATCHED = 5,       /* B >= 2: x[0..B) in shared memory, R rows per warp */
   GEMV_KERNEL_SCALAR = 6,        /* element loads, for rows that are not 16-byte aligned */
-  GEMV_KERNEL_STREAM = 7         /* B == 1: persistent warps, one row at a time per warp,
+  GEMV_KERNEL_STREAM = 7,        /* B == 1: persistent warps, one row at a time per warp,
                                     loads double-buffered across rows, x in shared memory */
+  GEMV_KERNEL_XSPLIT = 8         /* B <= 4: the 512 threads of a CTA split K, x in fp32
+                                    registers, rows streamed by cp.async into per-thread
+                                    shared-memory slots */
 } gemv_kernel_t;
 
 /* Where a kernel reads x from (gemv_plan_t.x_staging). */
 #define GEMV_X_GLOBAL 0      /* through L1, from the caller's buffer */
 #define GEMV_X_SMEM 1        /* copied once per CTA into shared memory as stored */
 #define GEMV_X_SMEM_FP32 2   /* widened once per CTA into shared memory as fp32 */
+#define GEMV_X_REGS 3        /* each thread's slice widened once into fp32 registers */
 
 typedef struct gemv_plan {
   int kernel;              /* gemv_kernel_t */

@@ -164,16 +164,35 @@ def test_plan_stream_needs_one_vector():
     assert p["kernel"] == g.KERNELS["stream"] and p["x_staging"] == 0 and p["smem_bytes"] == 0
 
 
+def test_plan_xsplit():
+    K = g.KERNELS
+    # float types with 2..4 vectors whose x slice fits 64 registers per thread
+    for dt, Kd, B, J in (("f16", 4096, 4, 1), ("bf16", 8192, 4, 2), ("bf16", 14336, 2, 4), ("f32", 4096, 3, 2),
+                         ("f32", 8192, 2, 4)):
+        p = g.plan_for(dt, 14336, Kd, B)
+        assert p["kernel"] == K["xsplit"] and p["unroll"] == J, (dt, Kd, B, p)
+        assert p["smem_bytes"] == 128 * 1024 and p["grid"] == 152
+    # int8 keeps the row-per-warp kernels; so does every type with one vector
+    assert g.plan_for("w8", 8192, 8192, 4)["kernel"] == K["batched"]
+    assert g.plan_for("bf16", 14336, 4096, 1)["kernel"] == K["stream"]
+    assert g.plan_for("f32", 16384, 4096, 1)["kernel"] == K["stream"]
+    # x slice too large for registers (4 vectors x 4 chunks x 8 values) -> batched
+    assert g.plan_for("bf16", 4096, 16384, 4)["kernel"] == K["batched"]
+    # few rows per SM, or very many rows -> not the K-split kernel
+    assert g.plan_for("bf16", 1000, 4096, 4)["kernel"] != K["xsplit"]
+    assert g.plan_for("bf16", 128256, 4096, 2)["kernel"] != K["xsplit"]
+
+
 def test_plan_batched_staging():
     # fp32 x in shared memory for B <= 4 when it fits, as stored when only that fits
-    p = g.plan_for("bf16", 4096, 8192, 4)
+    p = g.plan_for("w8", 4096, 8192, 4)
     assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4
     p = g.plan_for("bf16", 4096, 16384, 4)
     assert p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2
     p = g.plan_for("bf16", 4096, 4096, 8)
     assert p["x_staging"] == 1 and p["rows_per_warp"] == 2
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
-    assert g.plan_for("bf16", 4096, 4096, 3)["smem_bytes"] == 4 * 4096 * 4
+    assert g.plan_for("w8", 4096, 4096, 3)["smem_bytes"] == 4 * 4096 * 4
     assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
 
 

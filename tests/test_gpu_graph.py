@@ -27,6 +27,7 @@ STEP = [
     ("w8", 1024, 8192, 4, True, "auto"),          # batched, B <= 4
     ("f32", 16384, 32, 1, True, "auto"),          # rows per warp
     ("bf16", 1000, 2048, 2, True, "split_k"),     # forced split-K with B = 2
+    ("bf16", 4096, 4096, 4, True, "xsplit"),      # K split over a CTA, cp.async ring
 ]
 
 

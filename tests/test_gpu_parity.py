@@ -53,7 +53,19 @@ SHAPES = [  # (M, K) with several tiles and ragged tails for each kernel family
 FORCED = [("rows_per_warp", 0), ("rows_per_warp", 1), ("rows_per_warp", 16),
           ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0), ("split_k", 3),
           ("split_k", 7), ("batched", 2), ("batched", 4), ("scalar", 4), ("scalar", 32),
-          ("stream", 0)]
+          ("stream", 0), ("xsplit", 0)]
+
+
+def xsplit_feasible(dtype, K, B):
+    """Mirror of the dispatcher's XSPLIT rule: B <= 4, 16-byte chunks, at most 4
+    chunks per thread of 512 and at most 64 fp32 x values per thread."""
+    vec = {"f32": 4, "f16": 8, "bf16": 8, "w8": 16}[dtype]
+    if K % vec or K == 0 or B > 4:
+        return False
+    nb = 1 << (B - 1).bit_length()
+    per = -(-(K // vec) // 512)
+    j = 1 << (per - 1).bit_length()
+    return j <= 4 and j * nb * vec <= 64
 
 
 def forced_feasible(dtype, kernel, param, K, B):
@@ -68,6 +80,8 @@ def forced_feasible(dtype, kernel, param, K, B):
         return K * sa // 16 >= 2
     if kernel == "stream":
         return B == 1
+    if kernel == "xsplit":
+        return xsplit_feasible(dtype, K, B)
     return True
 
 
@@ -142,7 +156,7 @@ def test_unaligned_rows(dtype):
 def test_guard_bytes_untouched(dtype):
     for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("batched", 4, 4), ("batched", 2, 9),
                              ("block_per_row", 0, 4), ("rows_per_warp", 2, 4), ("scalar", 32, 4),
-                             ("stream", 0, 1), ("warp_per_row", 0, 3)):
+                             ("stream", 0, 1), ("warp_per_row", 0, 3), ("xsplit", 0, 3), ("xsplit", 0, 1)):
         M, K = 333, 256
         w = W.small(dtype, M, K, B, False, seed=400)
         d = U.to_device(W.make_inputs(w))
@@ -235,7 +249,7 @@ def test_exact_closed_forms_on_gpu(dtype):
     xk = P.xkind(dtype)
     for kernel, param, B in (("auto", 0, 2), ("warp_per_row", 0, 2), ("block_per_row", 0, 2),
                              ("split_k", 5, 2), ("batched", 2, 2), ("batched", 2, 12), ("scalar", 32, 2),
-                             ("stream", 0, 1)):
+                             ("stream", 0, 1), ("xsplit", 0, 2), ("xsplit", 0, 4)):
         M, K = 96, 4096
         A = torch.ones(M, K, dtype=torch.int8 if dtype == "w8" else U.out_dtype(dtype))
         x = torch.ones(B, K, dtype=U.out_dtype(xk if dtype != "w8" else "bf16"))
