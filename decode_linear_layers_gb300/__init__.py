@@ -25,15 +25,16 @@ __all__ = [
     "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_w4", "gemv_bf16_splitk_noalloc", "gemv_ex",
     "gemv_swiglu", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
-    "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH",
+    "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH", "device_status", "test_stall",
 ]
 
-SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+SUCCESS, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
+MAX_BATCH, MAX_BATCH_TC = 16, 256
 ACT_NONE, ACT_SILU = 0, 1
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "w8": 3, "w4": 4}
 W4_GROUP = 128  # elements of a row that share one int4 scale
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
-           "split_k": 4, "batched": 5, "scalar": 6, "stream": 7, "xsplit": 8}
+           "split_k": 4, "batched": 5, "scalar": 6, "stream": 7, "xsplit": 8, "tc": 9}
 X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32", 3: "regs"}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
         L.gemv_test_force_kernel.restype = ci
         L.gemv_test_last_plan.argtypes = [ctypes.POINTER(Plan)]
         L.gemv_test_last_plan.restype = ci
+        L.gemv_get_device_status.argtypes = [vp, ctypes.POINTER(ci)]
+        L.gemv_get_device_status.restype = ci
+        L.gemv_test_stall.argtypes = [ci, i64]
+        L.gemv_test_stall.restype = ci
         _lib = L
     return _lib
 
@@ -121,6 +126,23 @@ def plan_for(dtype: str, M: int, K: int, B: int, aligned16: bool = True, num_sms
     if st != SUCCESS:
         raise GemvError(st)
     return p.as_dict()
+
+
+def device_status(stream=None) -> tuple:
+    """Synchronise `stream` and read (then clear) the device status word of the
+    kernels with bounded waits: (status, bits), status SUCCESS or
+    ERR_DEVICE_TIMEOUT; raises GemvError on a CUDA failure."""
+    bits = ctypes.c_int(0)
+    st = lib().gemv_get_device_status(_stream(stream), ctypes.byref(bits))
+    if st not in (SUCCESS, ERR_DEVICE_TIMEOUT):
+        _check(st)
+    return st, int(bits.value)
+
+
+def test_stall(stall: bool, timeout_ns: int = 0) -> None:
+    """TEST ONLY: make later tensor-core launches skip their first CTA's last MMA,
+    so that CTA's wait runs out after timeout_ns (<= 0: 2 s)."""
+    _check(lib().gemv_test_stall(int(bool(stall)), int(timeout_ns)))
 
 
 def force_kernel(kernel, param: int = 0) -> None:

@@ -6,6 +6,8 @@
 // pointers, sizes, a stream) and adds B, status codes, host-side validation
 // (the NPU MatMul post, section 3.1: parameter and shape checks before any
 // kernel) and the per-shape kernel choice of gemv_plan.cpp.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +30,17 @@ int g_force_param = 0;
 
 constexpr int kMaxDevices = 256;
 std::atomic<int> g_sm_count[kMaxDevices];
+
+// test-only: make a tensor-core launch skip one MMA so its bounded wait runs out
+int g_test_stall = 0;
+int64_t g_test_timeout_ns = 0;
+constexpr int64_t kDefaultTimeoutNs = 2000000000;  // 2 s
+
+// Device status word of the kernels with bounded waits (one per device: a
+// __device__ variable is instantiated in every context).
+__device__ int g_device_status;
+std::atomic<int *> g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
 
 gemv_status_t cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
@@ -65,6 +78,27 @@ gemv_status_t sm_count(int *out) {
   return GEMV_SUCCESS;
 }
 
+gemv_status_t status_word(int **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return GEMV_ERR_UNSUPPORTED;
+  int *p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    p = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      void *q = nullptr;
+      e = cudaGetSymbolAddress(&q, g_device_status);
+      if (e != cudaSuccess) return cuda_fail(e);
+      p = static_cast<int *>(q);
+      g_status_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return GEMV_SUCCESS;
+}
+
 typedef cudaError_t (*launch_fn)(const gemv_plan_t &, const gemv::Args &, float *, cudaStream_t);
 
 // M counts the rows of A.  swiglu: y has M / 2 entries per vector (M even).
@@ -76,7 +110,8 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   if (act != GEMV_ACT_NONE && act != GEMV_ACT_SILU) return GEMV_ERR_INVALID_VALUE;
   const bool w4 = dtype == GEMV_DTYPE_W4;
   if (w4 && K % GEMV_W4_GROUP != 0) return GEMV_ERR_INVALID_VALUE;
-  if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
+  const bool half16 = dtype == GEMV_DTYPE_F16 || dtype == GEMV_DTYPE_BF16;
+  if (B > GEMV_MAX_BATCH && !(half16 && B <= GEMV_MAX_BATCH_TC)) return GEMV_ERR_UNSUPPORTED;
   if (M == 0 || B == 0) return GEMV_SUCCESS;
   const int sa = gemv::elem_bytes_a(dtype), sx = gemv::elem_bytes_x(dtype);
   const int sy = sx;
@@ -133,6 +168,12 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   args.residual = residual;
   args.act = act;
   args.half = swiglu ? M / 2 : 0;
+  if (p.kernel == GEMV_KERNEL_TC) {
+    st = status_word(&args.status);
+    if (st != GEMV_SUCCESS) return st;
+    args.timeout_ns = g_test_stall && g_test_timeout_ns > 0 ? g_test_timeout_ns : kDefaultTimeoutNs;
+    args.test_stall = g_test_stall;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_in);
 
   launch_fn fn = dtype == GEMV_DTYPE_F32    ? gemv::launch_f32
@@ -141,7 +182,7 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
                  : dtype == GEMV_DTYPE_W8   ? gemv::launch_w8
                                             : gemv::launch_w4;
   float *ws = nullptr;
-  if (p.kernel == GEMV_KERNEL_SPLIT_K) {
+  if (p.kernel == GEMV_KERNEL_SPLIT_K || (p.kernel == GEMV_KERNEL_TC && p.workspace_bytes > 0)) {
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), (size_t)p.workspace_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -152,7 +193,8 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
     if (e == cudaSuccess) e = e2;
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  g_launches.fetch_add(p.kernel == GEMV_KERNEL_SPLIT_K ? 2 : 1, std::memory_order_relaxed);
+  const bool two = p.kernel == GEMV_KERNEL_SPLIT_K || (p.kernel == GEMV_KERNEL_TC && p.splits > 1);
+  g_launches.fetch_add(two ? 2 : 1, std::memory_order_relaxed);
   t_last_plan = p;
   t_have_plan = true;
   return GEMV_SUCCESS;
@@ -161,6 +203,33 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
 }  // namespace
 
 namespace gemv {
+// The tensor maps of the tcgen05 kernel.  cuTensorMapEncodeTiled is a driver
+// function: it is fetched once through the runtime, so the library needs no
+// link-time dependency on the driver library.
+bool tc_tensor_maps(int dtype, const void *A, const void *x, int64_t M, int64_t K, int B, int N, void *map_a,
+                    void *map_x) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (encode == nullptr || M <= 0 || K <= 0 || B <= 0) return false;
+  const CUtensorMapDataType t = dtype == GEMV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint32_t es[2] = {1, 1};
+  auto one = [&](void *map, const void *base, int64_t rows, cuuint32_t box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcPlanTileK, box_rows};
+    return encode(static_cast<CUtensorMap *>(map), t, 2, const_cast<void *>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  return one(map_a, A, M, (cuuint32_t)kTcPlanTileM) && one(map_x, x, B, (cuuint32_t)N);
+}
+
 // For other entry points of the library (gemv_noalloc.cu): keep the per-thread
 // CUDA error and the launch counter in one place.
 void record_cuda_error(int e) { t_last_cuda_error = e; }
@@ -219,6 +288,7 @@ const char *gemv_status_string(gemv_status_t s) {
     case GEMV_ERR_INVALID_VALUE: return "GEMV_ERR_INVALID_VALUE";
     case GEMV_ERR_UNSUPPORTED: return "GEMV_ERR_UNSUPPORTED";
     case GEMV_ERR_CUDA: return "GEMV_ERR_CUDA";
+    case GEMV_ERR_DEVICE_TIMEOUT: return "GEMV_ERR_DEVICE_TIMEOUT";
     default: return "GEMV_ERR_UNKNOWN";
   }
 }
@@ -228,10 +298,33 @@ int gemv_last_cuda_error(void) { return t_last_cuda_error; }
 uint64_t gemv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 gemv_status_t gemv_test_force_kernel(int kernel, int param) {
-  if (kernel < GEMV_KERNEL_AUTO || kernel > GEMV_KERNEL_XSPLIT || param < 0)
+  if (kernel < GEMV_KERNEL_AUTO || kernel > GEMV_KERNEL_TC || param < 0)
     return GEMV_ERR_INVALID_VALUE;
   g_force_kernel = kernel;
   g_force_param = kernel == GEMV_KERNEL_AUTO ? 0 : param;
+  return GEMV_SUCCESS;
+}
+
+gemv_status_t gemv_get_device_status(gemv_stream_t stream, int *bits) {
+  if (bits != nullptr) *bits = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int *p = nullptr;
+  gemv_status_t st = status_word(&p);
+  if (st != GEMV_SUCCESS) return st;
+  int v = 0;
+  e = cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v == 0) return GEMV_SUCCESS;
+  e = cudaMemset(p, 0, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (bits != nullptr) *bits = v;
+  return GEMV_ERR_DEVICE_TIMEOUT;
+}
+
+gemv_status_t gemv_test_stall(int stall, int64_t timeout_ns) {
+  g_test_stall = stall != 0;
+  g_test_timeout_ns = stall != 0 ? timeout_ns : 0;
   return GEMV_SUCCESS;
 }
 

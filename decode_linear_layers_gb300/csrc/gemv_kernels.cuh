@@ -52,6 +52,11 @@ struct Args {
   // gscale[m][k >> gshift], M x (K >> gshift)
   const float *gscale = nullptr;
   int gshift = 0;
+  // kernels with bounded waits (k_tc): device status word they OR a bit into on
+  // timeout, the wait limit, and a test switch that withholds one MMA
+  int *status = nullptr;
+  int64_t timeout_ns = 2000000000;
+  int test_stall = 0;
 };
 
 // ------------------------------------------------------------------ memory access

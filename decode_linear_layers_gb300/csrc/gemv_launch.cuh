@@ -4,8 +4,11 @@
 
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "gemv_kernels.cuh"
 #include "gemv_plan.h"
+#include "gemv_tc.cuh"
 
 namespace gemv {
 
@@ -149,8 +152,41 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
   }
 }
 
+// fp16/bf16 with more than 16 vectors (or forced): the tensor-core kernel, then the
+// split-K reduction when the K range is split.
+template <class Op>
+cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
+  if constexpr (!TcFormat<Op>::ok) {
+    return cudaErrorInvalidValue;  // the planner never picks it for these types
+  } else {
+    if (p.nb < 16 || p.nb > kTcMaxN || p.nb % 16 != 0 || p.splits < 1) return cudaErrorInvalidValue;
+    if (p.splits > 1 && ws == nullptr) return cudaErrorInvalidValue;
+    const int ka = tc_atoms(p.nb), stages = tc_stages(p.nb, ka);
+    if (stages < 2 || p.smem_bytes != stages * tc_stage_bytes(p.nb, ka) + 1024) return cudaErrorInvalidValue;
+    CUtensorMap map_a, map_x;
+    std::memset(&map_a, 0, sizeof map_a);
+    std::memset(&map_x, 0, sizeof map_x);
+    const int dt = TcFormat<Op>::bf16 ? GEMV_DTYPE_BF16 : GEMV_DTYPE_F16;
+    if (a.K > 0 && !tc_tensor_maps(dt, a.A, a.x, a.M, a.K, a.B, p.nb, &map_a, &map_x)) return cudaErrorInvalidValue;
+    auto kern = ka == 2 ? k_tc<Op, 2> : k_tc<Op, 1>;
+    cudaError_t e = allow_smem(kern, p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kTcThreads), (size_t)p.smem_bytes, s>>>(
+        map_a, map_x, a, p.splits > 1 ? ws : nullptr, (int64_t)p.unroll, p.nb, stages);
+    if (p.splits == 1) return cudaSuccess;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t total = a.M * a.B;
+    int64_t g = (total + kThreads - 1) / kThreads;
+    if (g > 65535) g = 65535;
+    k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
+    return cudaSuccess;
+  }
+}
+
 template <class Op>
 cudaError_t launch(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
+  if (p.kernel == GEMV_KERNEL_TC) return launch_tc<Op>(p, a, ws, s);
   switch (p.nb) {
     case 1: return launch_nb<Op, 1>(p, a, ws, s);
     case 2: return launch_nb<Op, 2>(p, a, ws, s);

@@ -9,6 +9,7 @@
 //
 // Rules used here (per call, from dtype, M, K, B, alignment and the SM count;
 // the thresholds come from timing every kernel on the GB300 configurations):
+//   fp16/bf16 with 17..256 vectors        -> TC (tcgen05 small-N GEMM)
 //   rows not 16-byte aligned              -> SCALAR (element loads)
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
 //   fp32/fp16/bf16, B in 2..4, x slice fits 64 registers, at least 16 rows
@@ -75,7 +76,8 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   if (out == nullptr || num_sms < 1) return GEMV_ERR_INVALID_VALUE;
   if (dtype < GEMV_DTYPE_F32 || dtype > GEMV_DTYPE_W4) return GEMV_ERR_INVALID_VALUE;
   if (M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
-  if (B > GEMV_MAX_BATCH) return GEMV_ERR_UNSUPPORTED;
+  const bool half16 = dtype == GEMV_DTYPE_F16 || dtype == GEMV_DTYPE_BF16;
+  if (B > GEMV_MAX_BATCH && !(half16 && B <= GEMV_MAX_BATCH_TC)) return GEMV_ERR_UNSUPPORTED;
   gemv_plan_t p = {};
   p.kernel = GEMV_KERNEL_AUTO;
   p.splits = 1;
@@ -88,7 +90,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   const int vec = chunk_elems(dtype);
   const bool vec_ok = aligned16 && (K % vec == 0);
   const int64_t nch = vec_ok ? K / vec : 0;
-  p.nb = next_pow2(B);
+  p.nb = B > GEMV_MAX_BATCH ? (B + 15) / 16 * 16 : next_pow2(B);
+  // more than 16 vectors: only the tensor-core kernel, which needs 16-byte rows
+  if (B > GEMV_MAX_BATCH && !vec_ok) return GEMV_ERR_UNSUPPORTED;
+  const bool tc_ok = half16 && vec_ok;
   // the batched shared-memory kernels are not built for int4 (grouped scales)
   const int bstage = dtype == GEMV_DTYPE_W4 ? -1 : batched_staging(p.nb, K, sx);
   // XSPLIT: chunks per thread J (a power of two up to 4) and x registers
@@ -119,7 +124,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         ok = vec_ok && B == 1;
         break;
       case GEMV_KERNEL_XSPLIT:
-        ok = xs_ok;
+        ok = xs_ok && B <= GEMV_MAX_BATCH;
+        break;
+      case GEMV_KERNEL_TC:
+        ok = tc_ok;
         break;
       case GEMV_KERNEL_SCALAR:
         ok = force_param == 0 || force_param == 4 || force_param == 32;
@@ -133,6 +141,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
     }
   }
 
+  if (B > GEMV_MAX_BATCH) kernel = GEMV_KERNEL_TC;  // the only kernel for 17..256 vectors
   if (kernel == GEMV_KERNEL_AUTO) {
     if (!vec_ok) {
       kernel = GEMV_KERNEL_SCALAR;
@@ -219,6 +228,31 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       p.unroll = r == 4 ? 1 : 2;
       p.smem_bytes = (int)((int64_t)p.nb * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
       p.grid = num_sms;
+      break;
+    }
+    case GEMV_KERNEL_TC: {
+      // N = B rounded up to 16 (p.nb); one 128-thread CTA per 128-row tile and K
+      // slice (p.splits slices of p.unroll k-tiles)
+      if (B <= GEMV_MAX_BATCH) p.nb = (B + 15) / 16 * 16;
+      const int64_t tiles = ceil_div(M, kTcPlanTileM);
+      const int64_t ktiles = K > 0 ? ceil_div(K, (int64_t)kTcPlanTileK * tc_plan_atoms(p.nb)) : 1;
+      // K slices so that all CTAs run in one wave (as many per SM as shared memory allows)
+      const int64_t smem = (int64_t)tc_plan_stages(p.nb) * tc_plan_stage_bytes(p.nb) + 1024;
+      int64_t per_sm = kSmemPerSm / (smem + 1024);
+      if (per_sm < 1) per_sm = 1;
+      int64_t s = (int64_t)num_sms * per_sm / tiles;
+      if (s > ktiles) s = ktiles;
+      if (s > 65535) s = 65535;
+      if (s < 1) s = 1;
+      const int64_t per = ceil_div(ktiles, s);
+      s = ceil_div(ktiles, per);  // no empty slice
+      p.threads = kTcPlanThreads;
+      p.grid = tiles;
+      p.splits = (int)s;
+      p.unroll = (int)per;
+      p.lanes_per_row = kTcPlanThreads;
+      p.smem_bytes = (int)smem;
+      p.workspace_bytes = s > 1 ? s * (int64_t)B * M * 4 : 0;
       break;
     }
     case GEMV_KERNEL_XSPLIT: {

@@ -30,6 +30,25 @@ constexpr int kXsplitGroups = 4;
 constexpr int xsplit_rows_per_group(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
 constexpr int xsplit_depth(int J) { return xsplit_rows_per_group(J) * kXsplitGroups; }
 
+// TC (tcgen05, fp16/bf16, B > 16): 128-row tiles, stages of one or two 64-column
+// swizzle atoms along K; as many stages (at most 8) as fit in 100 KB (two CTAs per
+// SM), plus 1024 bytes to align them.
+constexpr int kTcPlanThreads = 128;
+constexpr int kTcPlanTileM = 128;
+constexpr int kTcPlanTileK = 64;
+// 64-column atoms per stage: two for N <= 64, one above.
+constexpr int tc_plan_atoms(int n) { return n <= 64 ? 2 : 1; }
+constexpr int tc_plan_stage_bytes(int n) { return (kTcPlanTileM + n) * kTcPlanTileK * 2 * tc_plan_atoms(n); }
+constexpr int tc_plan_stages(int n) {
+  return 100 * 1024 / tc_plan_stage_bytes(n) < 8 ? 100 * 1024 / tc_plan_stage_bytes(n) : 8;
+}
+
+// Tensor maps of A (K x M) and x (K x B), 16-bit values, boxes 64 x 128 and 64 x N,
+// 128-byte swizzle, written to map_a and map_x (CUtensorMap, 128 bytes each).
+// Defined in gemv_api.cu; false if the driver's encoder is missing or refuses.
+bool tc_tensor_maps(int dtype, const void *A, const void *x, int64_t M, int64_t K, int B, int N, void *map_a,
+                    void *map_x);
+
 int elem_bytes_a(int dtype);
 int elem_bytes_x(int dtype);
 // Elements of A in one 16-byte chunk.

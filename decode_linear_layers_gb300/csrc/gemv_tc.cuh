@@ -1,0 +1,300 @@
+// k_tc: 16 < B <= 256 vectors, fp16/bf16 storage.  With more than 16 vectors the
+// GEMV becomes a small-N GEMM (B multiply-adds per weight byte pair), so it runs on
+// the 5th-generation tensor cores: Y^T (M x N) = A (M x K) . X^T (K x N), N = B
+// rounded up to a multiple of 16, fp32 accumulation in tensor memory.
+//
+// One CTA of 128 threads per 128-row tile of A (and per K slice when the tiles are
+// too few to occupy the SMs: split-K, the slices summed in index order by
+// k_splitk_reduce).  Thread 0 runs the pipeline: the tensor-memory accelerator (TMA)
+// copies each k-tile (128 x 64 of A, N x 64 of x, 128-byte swizzle, zeros outside
+// the matrix) into one of `stages` shared-memory stages, completing on the stage's
+// "full" mbarrier; thread 0 issues the stage's four MMAs (K = 16 each) and commits
+// them to the stage's "empty" mbarrier, which releases the stage for the next copy.
+// The 128-byte swizzle TMA writes is the tensor cores' canonical K-major layout:
+// 8-row x 128-byte atoms, 1024 bytes apart.  No barrier runs inside the loop.
+//
+// Every wait on an mbarrier is bounded (globaltimer); on timeout the CTA ORs a bit
+// into the device status word, waits (bounded) for its MMAs and copies in flight,
+// frees its tensor memory and returns.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (the encoder is fetched from the driver at run time)
+
+#include "gemv_kernels.cuh"
+
+namespace gemv {
+
+constexpr int kTcThreads = 128;  // one warpgroup: warp w reads TMEM lanes 32w..32w+31
+constexpr int kTcM = 128;        // rows per tile (the MMA's M)
+constexpr int kTcK = 64;         // K per stage: one 128-byte swizzle atom of 16-bit values
+constexpr int kTcMaxStages = 8;
+constexpr int kTcLag = 2;  // a stage is refilled two tiles after its MMAs were issued
+constexpr int kTcMaxN = 256;
+
+// device status bits (ORed into *Args::status)
+constexpr int kTcStatusMma = 16;   // a copy or an MMA commit did not arrive in time
+constexpr int kTcStatusDrain = 32; // the final wait for work in flight ran out
+
+__device__ __forceinline__ uint32_t tc_smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void tc_mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool tc_mbar_try_wait(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(tc_smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t tc_global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of the given parity; false after timeout_ns.
+__device__ __forceinline__ bool tc_mbar_wait(uint64_t *b, uint32_t parity, int64_t timeout_ns) {
+  if (tc_mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = tc_global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (tc_mbar_try_wait(b, parity)) return true;
+    if ((i & 63) == 0 && (int64_t)(tc_global_ns() - t0) > timeout_ns) return false;
+  }
+}
+
+// Shared-memory matrix descriptor of a K-major operand in 128-byte swizzle atoms
+// (8 rows x 128 bytes, atoms 1024 bytes apart along M/N: the stride byte offset;
+// the leading byte offset is not used by swizzled K-major layouts), descriptor
+// version 1, layout type 2 (128-byte swizzle).  Units of 16 bytes.  Steps of
+// K = 16 within an atom advance the start address by 32 bytes.
+__device__ __forceinline__ uint64_t tc_smem_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tc_mbar_arrive_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   tc_smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 2-D tile copy global -> shared by the tensor-memory accelerator, completing as
+// transaction bytes on `bar`.  c0 is the inner (K) coordinate: a multiple of 64
+// elements, so 128-byte aligned.
+__device__ __forceinline__ void tc_tma_2d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc_smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(tc_smem_u32(bar))
+      : "memory");
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both fp16 (0) or
+// both bf16 (1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t tc_idesc(bool bf16, int n) {
+  const uint32_t ab = bf16 ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The mbarrier gets one arrival when every MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   tc_smem_u32(b))
+               : "memory");
+}
+
+// The tensor-core path's storage types: fp16 (A/B format 0) and bf16 (format 1).
+template <class Op> struct TcFormat { static constexpr bool ok = false, bf16 = false; };
+template <> struct TcFormat<OpF16> { static constexpr bool ok = true, bf16 = false; };
+template <> struct TcFormat<OpBF16> { static constexpr bool ok = true, bf16 = true; };
+
+// A stage holds KA = 1 or 2 swizzle atoms along K (64 or 128 columns): 128 x 64 A
+// boxes, then N x 64 x boxes.  Stages: as many as fit in 100 KB (two CTAs per SM:
+// measured faster than one CTA with a deeper ring), at most kTcMaxStages.
+__host__ __device__ constexpr int tc_stage_bytes(int n, int ka) { return (kTcM + n) * kTcK * 2 * ka; }
+__host__ __device__ constexpr int tc_stages(int n, int ka) {
+  return 100 * 1024 / tc_stage_bytes(n, ka) < kTcMaxStages ? 100 * 1024 / tc_stage_bytes(n, ka) : kTcMaxStages;
+}
+// Wider stages for narrow N: each stage costs a fixed time to turn around, so it
+// should carry at least ~24 KB.
+__host__ __device__ constexpr int tc_atoms(int n) { return n <= 64 ? 2 : 1; }
+
+// grid (ceil(M / 128), splits); k-tiles [y * kt_per_split, ...) of K.  partial ==
+// nullptr: finish the outputs here (epilogue); otherwise write the slice's sums to
+// partial[(y * B + b) * M + m] for k_splitk_reduce.  map_a: A as (K, M) 16-bit
+// values, box 64 x 128; map_x: x as (K, B), box 64 x N; both 128-byte swizzle.
+template <class Op, int KA>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_x, const Args a,
+         float *partial, int64_t kt_per_split, int N, int stages) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full[kTcMaxStages], empty[kTcMaxStages];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int ok_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  const int64_t m0 = (int64_t)blockIdx.x * kTcM;
+  constexpr int KT = kTcK * KA;  // K per stage
+  const int64_t ktiles = (K + KT - 1) / KT;
+  const int64_t kt_lo = (int64_t)blockIdx.y * kt_per_split;
+  const int64_t kt_hi = kt_lo + kt_per_split < ktiles ? kt_lo + kt_per_split : ktiles;
+  const int64_t nt = kt_hi - kt_lo;  // at least 1 when K > 0 (the planner makes no empty slice)
+  const int S = stages;
+  // the swizzle atoms need 1024-byte alignment of every stage
+  unsigned char *smem = smem_raw + ((1024u - (tc_smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr uint32_t a_atom = kTcM * kTcK * 2;  // one 128 x 64 box of A
+  const uint32_t x_atom = (uint32_t)N * kTcK * 2, a_bytes = a_atom * KA, st_bytes = (a_atom + x_atom) * KA;
+  const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
+
+  if (nt <= 0) {  // K == 0: the empty sum
+    const int64_t m = m0 + tid;
+    for (int b = 0; b < B && m < M; ++b) {
+      if (partial != nullptr) partial[((int64_t)blockIdx.y * B + b) * M + m] = 0.f;
+      else epilogue_store<Op>(a, b, m, 0.f);
+    }
+    return;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem_u32(&tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc_mbar_init(&full[s], 1);
+      tc_mbar_init(&empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    ok_flag = 1;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_slot;
+
+  if (tid == 0) {
+    const uint32_t idesc = tc_idesc(TcFormat<Op>::bf16, N);
+    auto stage_a = [&](int s) { return smem + (size_t)s * st_bytes; };
+    auto load = [&](int64_t t, int s) {  // k-tile kt_lo + t into stage s
+      tc_mbar_arrive_expect_tx(&full[s], st_bytes);
+      const int32_t k0 = (int32_t)((kt_lo + t) * KT);
+#pragma unroll
+      for (int j = 0; j < KA; ++j) {
+        tc_tma_2d(stage_a(s) + j * a_atom, &map_a, k0 + j * kTcK, (int32_t)m0, &full[s]);
+        tc_tma_2d(stage_a(s) + a_bytes + j * x_atom, &map_x, k0 + j * kTcK, 0, &full[s]);
+      }
+    };
+    int64_t loaded = -1, consumed = -1, committed = -1;  // highest tile copied / waited for / committed
+    bool ok = true;
+    for (int64_t t = 0; t < nt && t < S; ++t) {
+      load(t, (int)t);
+      loaded = t;
+    }
+    for (int64_t i = 0; i < nt && ok; ++i) {
+      const int s = (int)(i % S);
+      if (!tc_mbar_wait(&full[s], (uint32_t)((i / S) & 1), a.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      consumed = i;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!(a.test_stall && blockIdx.x == 0 && blockIdx.y == 0 && i == nt - 1)) {  // test: the last tile never completes
+        const uint32_t sa = tc_smem_u32(stage_a(s)), sx = sa + a_bytes;
+#pragma unroll
+        for (int j = 0; j < KA; ++j)
+#pragma unroll
+          for (int kk = 0; kk < kTcK / 16; ++kk)
+            tc_mma(tmem, tc_smem_desc(sa + j * a_atom + kk * 32), tc_smem_desc(sx + j * x_atom + kk * 32), idesc,
+                   (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&empty[s]);
+        committed = i;
+      }
+      // refill the stage of tile i - kTcLag once its MMAs are done: those were
+      // committed kTcLag iterations ago, so the wait rarely has to wait
+      const int64_t j = i - (S > kTcLag ? kTcLag : S - 1);
+      if (j >= 0 && j + S < nt) {
+        const int ps = (int)(j % S);
+        if (!tc_mbar_wait(&empty[ps], (uint32_t)((j / S) & 1), a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        load(j + S, ps);
+        loaded = j + S;
+      }
+    }
+    if (ok) ok = tc_mbar_wait(&empty[(nt - 1) % S], (uint32_t)(((nt - 1) / S) & 1), a.timeout_ns);
+    if (!ok) {
+      // nothing may be in flight when the CTA frees its tensor memory and exits:
+      // the last committed MMAs (their commit covers all earlier ones) and every
+      // copy issued but not waited for
+      if (a.status != nullptr) atomicOr(a.status, kTcStatusMma);
+      bool drained = committed < 0 ||
+                     tc_mbar_wait(&empty[committed % S], (uint32_t)((committed / S) & 1), a.timeout_ns);
+      for (int64_t t = consumed + 1; t <= loaded && drained; ++t)
+        drained = tc_mbar_wait(&full[t % S], (uint32_t)((t / S) & 1), a.timeout_ns);
+      if (!drained && a.status != nullptr) atomicOr(a.status, kTcStatusDrain);
+    }
+    ok_flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!ok_flag) {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    return;
+  }
+
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const int64_t m = m0 + warp * 32 + lane;  // this thread's row: TMEM lane 32 * warp + lane
+  for (int c0 = 0; c0 < N; c0 += 16) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (m < M) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int b = c0 + j;
+        if (b < B) {
+          const float v = __uint_as_float(r[j]);
+          if (partial != nullptr) partial[((int64_t)blockIdx.y * B + b) * M + m] = v;
+          else epilogue_store<Op>(a, b, m, v);
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+}
+
+}  // namespace gemv

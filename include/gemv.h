@@ -46,7 +46,8 @@
  * Errors: the return value.  GEMV_ERR_INVALID_VALUE for negative sizes, NULL
  * pointers where data is needed, pointers not aligned to their element size,
  * sizes whose byte counts overflow int64, or y overlapping an input;
- * GEMV_ERR_UNSUPPORTED for B > 16; GEMV_ERR_CUDA when a CUDA call fails (the
+ * GEMV_ERR_UNSUPPORTED for B > 16 (B > 256 for fp16/bf16, whose 17..256 vectors run
+ * on the tensor cores); GEMV_ERR_CUDA when a CUDA call fails (the
  * cudaError_t is kept per thread, see gemv_last_cuda_error).  Nothing is enqueued
  * when an argument check fails.
  *
@@ -70,7 +71,8 @@ typedef enum gemv_status {
   GEMV_SUCCESS = 0,
   GEMV_ERR_INVALID_VALUE = 1,
   GEMV_ERR_UNSUPPORTED = 2,
-  GEMV_ERR_CUDA = 3
+  GEMV_ERR_CUDA = 3,
+  GEMV_ERR_DEVICE_TIMEOUT = 4 /* gemv_get_device_status: a kernel's bounded wait ran out */
 } gemv_status_t;
 
 /* Storage kinds, as used by gemv_plan_for. */
@@ -86,8 +88,11 @@ typedef enum gemv_dtype {
 /* Elements of a row that share one int4 scale. */
 #define GEMV_W4_GROUP 128
 
-/* Maximum number of decode vectors per call. */
+/* Maximum number of decode vectors per call of the CUDA-core GEMV kernels. */
 #define GEMV_MAX_BATCH 16
+/* fp16/bf16 only: up to this many vectors (B > GEMV_MAX_BATCH runs as a small-N
+ * GEMM on the tensor cores; the other storage types return GEMV_ERR_UNSUPPORTED). */
+#define GEMV_MAX_BATCH_TC 256
 
 /* fp32: A M x K, x B x K, y B x M.  The "16-sgemv" notes' SGEMV plus the lesson's bias. */
 gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float *y,
@@ -202,9 +207,12 @@ typedef enum gemv_kernel {
   GEMV_KERNEL_SCALAR = 6,        /* element loads, for rows that are not 16-byte aligned */
   GEMV_KERNEL_STREAM = 7,        /* B == 1: persistent warps, one row at a time per warp,
                                     loads double-buffered across rows, x in shared memory */
-  GEMV_KERNEL_XSPLIT = 8         /* B <= 4: the 512 threads of a CTA split K, x in fp32
+  GEMV_KERNEL_XSPLIT = 8,        /* B <= 4: the 512 threads of a CTA split K, x in fp32
                                     registers, rows streamed by cp.async into per-thread
                                     shared-memory slots */
+  GEMV_KERNEL_TC = 9             /* fp16/bf16, B > 16: tcgen05 MMA (M = 128 rows per CTA,
+                                    N = B rounded up to 16), fp32 accumulators in tensor
+                                    memory, split-K when the row tiles are few; waits bounded */
 } gemv_kernel_t;
 
 /* Where a kernel reads x from (gemv_plan_t.x_staging). */
@@ -246,6 +254,21 @@ gemv_status_t gemv_test_force_kernel(int kernel, int param);
 
 /* TEST ONLY — the plan of this thread's last successful launch. */
 gemv_status_t gemv_test_last_plan(gemv_plan_t *plan);
+
+/* Device-side status of the kernels with bounded waits (GEMV_KERNEL_TC).
+ * Synchronises `stream`, then returns GEMV_ERR_DEVICE_TIMEOUT if a wait of a kernel
+ * launched on the current device since the previous call ran out (the kernel then
+ * left its outputs unwritten, freed its tensor memory and returned with nothing in
+ * flight), else GEMV_SUCCESS; the status word is cleared.  `bits` (may be NULL)
+ * receives which wait ran out: 16 an MMA completion, 32 the final wait for work in
+ * flight.  GEMV_ERR_CUDA if the synchronisation or the read fails. */
+gemv_status_t gemv_get_device_status(gemv_stream_t stream, int *bits);
+
+/* TEST ONLY — not thread-safe.  With `stall` != 0 every later GEMV_KERNEL_TC launch
+ * skips the last MMA of its first CTA, so that CTA's wait for it runs out after
+ * `timeout_ns` (<= 0: the default of 2 s) and gemv_get_device_status reports
+ * GEMV_ERR_DEVICE_TIMEOUT.  stall = 0 restores normal launches. */
+gemv_status_t gemv_test_stall(int stall, int64_t timeout_ns);
 
 #ifdef __cplusplus
 }

@@ -78,7 +78,10 @@ def test_negative_sizes_and_big_batch():
         assert call(fn, P, P + 4096, None, P + 8192, -1, 4, 1, None) == 1
         assert call(fn, P, P + 4096, None, P + 8192, 4, -1, 1, None) == 1
         assert call(fn, P, P + 4096, None, P + 8192, 4, 4, -1, None) == 1
-        assert call(fn, P, P + 4096, None, P + 8192, 4, 4, 17, None) == 2
+    # more than 16 vectors: fp32 never; fp16/bf16 up to 256 (tensor cores)
+    assert call("gemv_f32", P, P + 4096, None, P + 8192, 4, 4, 17, None) == 2
+    for fn in ("gemv_f16", "gemv_bf16"):
+        assert call(fn, P, P + 4096, None, P + 8192, 4, 8, 257, None) == 2
     assert g.lib().gemv_w8(P, P + 64, P + 4096, None, P + 8192, 4, 4, 17, None) == 2
 
 
@@ -277,3 +280,34 @@ def test_plan_w4():
     assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 8
     assert g.plan_for("w4", 100, 4096, 1, aligned16=False)["kernel"] == K["scalar"]
     assert g.plan_for("w4", 8, 1 << 20, 1)["kernel"] == K["split_k"]
+
+
+def test_plan_tensor_cores():
+    K = g.KERNELS
+    # 17..256 vectors of fp16/bf16: the tcgen05 kernel, N = B rounded up to 16
+    p = g.plan_for("bf16", 4096, 4096, 32)
+    assert p["kernel"] == K["tc"] and p["nb"] == 32 and p["threads"] == 128 and p["grid"] == 32
+    # N <= 64: stages of two 64-column atoms (128 + N rows x 256 bytes), as many as
+    # fit in 100 KB (at most 8), + 1024 bytes to align them
+    assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024
+    # split-K so that all CTAs run in one wave (two CTAs per SM here): at most 9
+    # slices of 32 k-tiles of 128, i.e. 8 slices of 4 (no empty slice)
+    assert p["splits"] == 8 and p["unroll"] == 4 and p["workspace_bytes"] == 8 * 32 * 4096 * 4
+    assert p["grid"] * p["splits"] <= 2 * 152
+    p = g.plan_for("f16", 4096, 4096, 17)
+    assert p["kernel"] == K["tc"] and p["nb"] == 32
+    p = g.plan_for("bf16", 128256, 4096, 256)
+    assert p["kernel"] == K["tc"] and p["nb"] == 256 and p["splits"] == 1 and p["workspace_bytes"] == 0
+    assert p["smem_bytes"] == 2 * (128 + 256) * 128 + 1024
+    # no empty slice: splits * k-tiles per slice covers K exactly once
+    for M, Kd in ((300, 1000), (1, 64), (5000, 4104), (128, 16384)):
+        p = g.plan_for("bf16", M, Kd, 40)
+        kt = -(-Kd // 128)  # N = 48: 128-column k-tiles
+        assert (p["splits"] - 1) * p["unroll"] < kt <= p["splits"] * p["unroll"], (M, Kd, p)
+    for dt in ("f32", "w8"):
+        with pytest.raises(g.GemvError):
+            g.plan_for(dt, 100, 64, 17)
+    with pytest.raises(g.GemvError):
+        g.plan_for("bf16", 100, 64, 257)
+    with pytest.raises(g.GemvError):       # more than 16 vectors needs 16-byte rows
+        g.plan_for("bf16", 100, 60, 17)

@@ -1,0 +1,173 @@
+"""The tensor-core kernel (GEMV_KERNEL_TC): fp16/bf16 with 17..256 vectors.
+
+* every batch size class (N = B rounded up to 16 from 32 to 256, ragged B), both
+  storage types, shapes with ragged M (partial 128-row tiles) and ragged K (partial
+  64-column stages), with and without split-K, with and without bias;
+* decode-size matrices on sampled rows (the oracle on a subset of A's rows);
+* bit-identical repeats, K = 0, one row, the fused epilogue, guard bytes around y,
+  CUDA-graph capture (the split-K scratch comes from the stream-ordered pool);
+* the kernel forced for B <= 16 (N = 16);
+* bounded waits: a launch that skips one MMA reports GEMV_ERR_DEVICE_TIMEOUT through
+  gemv_get_device_status, without a fault or a hang, and the next launch is normal.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import decode_linear_layers_gb300 as g
+import oracle
+import workloads as W
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+HALF = ("f16", "bf16")
+
+
+@pytest.fixture(autouse=True)
+def _auto_dispatch():
+    g.force_kernel("auto")
+    g.test_stall(False)
+    yield
+    g.force_kernel("auto")
+    g.test_stall(False)
+
+
+def _bits(t):
+    return t.view(torch.int16)
+
+
+@pytest.mark.parametrize("dtype", HALF)
+@pytest.mark.parametrize("B", [17, 24, 32, 48, 64, 100, 128, 200, 256])
+def test_tc_parity(dtype, B):
+    seed = B
+    for (M, K) in ((128, 64), (300, 1000), (1, 4096), (1000, 520)):
+        bias = (M + B) % 2 == 0
+        w = W.small(dtype, M, K, B, bias, seed=seed)
+        seed += 1
+        inp = W.make_inputs(w)
+        y_ref, absdot = U.oracle_for(dtype, inp)
+        d = U.to_device(inp)
+        y1 = U.run_gpu(dtype, d, M, K, B)
+        p = g.last_plan()
+        assert p["kernel_name"] == "tc" and p["nb"] == -(-B // 16) * 16, p
+        y2 = U.run_gpu(dtype, d, M, K, B)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(y1), _bits(y2)), "results differ between two identical calls"
+        U.assert_close(dtype, y1, y_ref, absdot, with_rounding=True,
+                       what=f"{dtype} tc M={M} K={K} B={B} splits={p['splits']} bias={bias}")
+    assert g.device_status() == (g.SUCCESS, 0)
+
+
+@pytest.mark.parametrize("dtype,M,K,B", [("bf16", 14336, 4096, 32), ("bf16", 4096, 14336, 128),
+                                         ("f16", 28672, 4096, 64), ("bf16", 6144, 4096, 256)])
+def test_tc_decode_sizes_sampled_rows(dtype, M, K, B):
+    w = W.small(dtype, M, K, B, True, seed=5)
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    y = U.run_gpu(dtype, d, M, K, B)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(0).choice(M, size=192, replace=False))
+    sub = {"A": inp["A"][rows], "x": inp["x"], "bias": inp["bias"][rows], "scale": None}
+    y_ref, absdot = U.oracle_for(dtype, sub)
+    U.assert_close(dtype, y[:, rows], y_ref, absdot, what=f"{dtype} tc {M}x{K} B={B} sampled rows")
+
+
+@pytest.mark.parametrize("dtype", HALF)
+def test_tc_k_zero_and_one_row(dtype):
+    M, B = 200, 40
+    bias = torch.randn(M, generator=torch.Generator().manual_seed(1)).to(U.out_dtype(dtype)).cuda()
+    y = torch.full((B, M), 3.0, dtype=U.out_dtype(dtype), device="cuda")
+    empty = torch.empty(0, dtype=U.out_dtype(dtype), device="cuda")
+    getattr(g, f"gemv_{dtype}")(empty, empty, bias, y, M, 0, B)
+    torch.cuda.synchronize()
+    assert torch.equal(y, bias.expand(B, M))
+
+
+@pytest.mark.parametrize("dtype", HALF)
+@pytest.mark.parametrize("B", [1, 5, 16])
+def test_tc_forced_small_batches(dtype, B):
+    M, K = 700, 2048
+    w = W.small(dtype, M, K, B, True, seed=40 + B)
+    inp = W.make_inputs(w)
+    y_ref, absdot = U.oracle_for(dtype, inp)
+    g.force_kernel("tc")
+    y = U.run_gpu(dtype, U.to_device(inp), M, K, B)
+    assert g.last_plan()["kernel_name"] == "tc" and g.last_plan()["nb"] == 16
+    U.assert_close(dtype, y, y_ref, absdot, with_rounding=True, what=f"{dtype} tc forced B={B}")
+
+
+@pytest.mark.parametrize("dtype", HALF)
+def test_tc_epilogue(dtype):
+    M, K, B = 1000, 4096, 64
+    w = W.small(dtype, M, K, B, True, seed=77)
+    inp = W.make_inputs(w)
+    xdt = U.out_dtype(dtype)
+    r = (torch.randn(B, M, generator=torch.Generator().manual_seed(3)) * 2).to(xdt)
+    y_ref, _, absdot = oracle.gemv_ex(dtype, W.storage_bits(inp["A"]), W.storage_bits(inp["x"]),
+                                      W.storage_bits(inp["bias"]), None, residual=W.storage_bits(r), act=1,
+                                      nthreads=U.threads())
+    d = U.to_device(inp)
+    y = r.cuda()
+    g.gemv_ex(dtype, d["A"], None, d["x"], d["bias"], y, y, M, K, B, 1)
+    assert g.last_plan()["kernel_name"] == "tc"
+    U.assert_close_ex(dtype, y, y_ref, absdot, 1, what=f"{dtype} tc silu + residual in place")
+
+
+def test_tc_guard_bytes():
+    M, K, B = 333, 256, 40
+    w = W.small("bf16", M, K, B, False, seed=400)
+    d = U.to_device(W.make_inputs(w))
+    n = B * M
+    buf = torch.full((n + 2048,), 7, dtype=torch.bfloat16, device="cuda")
+    y = buf[1024:1024 + n]
+    U.call("bf16", d, y, M, K, B)
+    torch.cuda.synchronize()
+    assert bool((buf[:1024] == 7).all()) and bool((buf[1024 + n:] == 7).all())
+
+
+def test_tc_in_cuda_graph():
+    M, K, B = 4096, 4096, 32  # split-K: scratch from the stream-ordered pool
+    w = W.small("bf16", M, K, B, False, seed=991)
+    d = U.to_device(W.make_inputs(w))
+    y = torch.empty(B, M, dtype=torch.bfloat16, device="cuda")
+    U.call("bf16", d, y, M, K, B)
+    assert g.last_plan()["splits"] > 1
+    torch.cuda.synchronize()
+    eager = y.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        U.call("bf16", d, y, M, K, B)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    y.zero_()
+    with torch.cuda.graph(graph):
+        U.call("bf16", d, y, M, K, B)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(eager))
+
+
+def test_tc_bounded_wait_reports_timeout_and_recovers():
+    M, K, B = 1024, 2048, 32
+    w = W.small("bf16", M, K, B, True, seed=990)
+    inp = W.make_inputs(w)
+    y_ref, absdot = U.oracle_for("bf16", inp)
+    d = U.to_device(inp)
+    assert g.device_status() == (g.SUCCESS, 0)
+    # CTA (0, 0) skips its last MMA: the wait for that stage's commit runs out after
+    # 50 ms; the CTA drains its other MMAs and copies, frees its tensor memory and
+    # returns, and the status word says so.  The other CTAs finish normally.
+    g.test_stall(True, 50_000_000)
+    y = torch.zeros(B, M, dtype=torch.bfloat16, device="cuda")
+    U.call("bf16", d, y, M, K, B)
+    st, bits = g.device_status()
+    assert st == g.ERR_DEVICE_TIMEOUT and bits & 16, (st, bits)
+    assert g.device_status() == (g.SUCCESS, 0), "the status word is cleared by the read"
+    g.test_stall(False)
+    y2 = U.run_gpu("bf16", d, M, K, B)
+    assert g.device_status() == (g.SUCCESS, 0)
+    U.assert_close("bf16", y2, y_ref, absdot, with_rounding=True, what="tc after a timeout")
