@@ -161,8 +161,8 @@ cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
   } else {
     if (p.nb < 16 || p.nb > kTcMaxN || p.nb % 16 != 0 || p.splits < 1) return cudaErrorInvalidValue;
     if (p.splits > 1 && ws == nullptr) return cudaErrorInvalidValue;
-    const int ka = tc_atoms(p.nb), stages = tc_stages(p.nb, ka);
-    if (stages < 2 || p.smem_bytes != stages * tc_stage_bytes(p.nb, ka) + 1024) return cudaErrorInvalidValue;
+    const int ka = tc_atoms(p.nb), sb = tc_stage_bytes(p.nb, ka), stages = (p.smem_bytes - 1024) / sb;
+    if (stages < 2 || stages > kTcMaxStages || p.smem_bytes != stages * sb + 1024) return cudaErrorInvalidValue;
     CUtensorMap map_a, map_x;
     std::memset(&map_a, 0, sizeof map_a);
     std::memset(&map_x, 0, sizeof map_x);

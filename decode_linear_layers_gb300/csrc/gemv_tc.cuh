@@ -5,13 +5,14 @@
 //
 // One CTA of 128 threads per 128-row tile of A (and per K slice when the tiles are
 // too few to occupy the SMs: split-K, the slices summed in index order by
-// k_splitk_reduce).  Thread 0 runs the pipeline: the tensor-memory accelerator (TMA)
-// copies each k-tile (128 x 64 of A, N x 64 of x, 128-byte swizzle, zeros outside
-// the matrix) into one of `stages` shared-memory stages, completing on the stage's
-// "full" mbarrier; thread 0 issues the stage's four MMAs (K = 16 each) and commits
-// them to the stage's "empty" mbarrier, which releases the stage for the next copy.
-// The 128-byte swizzle TMA writes is the tensor cores' canonical K-major layout:
-// 8-row x 128-byte atoms, 1024 bytes apart.  No barrier runs inside the loop.
+// k_splitk_reduce).  Two threads run the pipeline.  A producer (lane 0 of warp 0)
+// has the tensor-memory accelerator (TMA) copy each k-tile (128 x 64 or 128 x 128
+// of A and N x 64/128 of x, 128-byte swizzle, zeros outside the matrix) into a free
+// stage, completing on the stage's "full" mbarrier; an MMA issuer (lane 0 of warp 1)
+// waits for it, issues the stage's MMAs (K = 16 each) and commits them to the
+// stage's "empty" mbarrier, which frees the stage for the producer.  The 128-byte
+// swizzle TMA writes is the tensor cores' canonical K-major layout: 8-row x 128-byte
+// atoms, 1024 bytes apart.  No CTA barrier runs inside the loop.
 //
 // Every wait on an mbarrier is bounded (globaltimer); on timeout the CTA ORs a bit
 // into the device status word, waits (bounded) for its MMAs and copies in flight,
@@ -28,7 +29,6 @@ constexpr int kTcThreads = 128;  // one warpgroup: warp w reads TMEM lanes 32w..
 constexpr int kTcM = 128;        // rows per tile (the MMA's M)
 constexpr int kTcK = 64;         // K per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kTcMaxStages = 8;
-constexpr int kTcLag = 2;  // a stage is refilled two tiles after its MMAs were issued
 constexpr int kTcMaxN = 256;
 
 // device status bits (ORed into *Args::status)
@@ -67,6 +67,24 @@ __device__ __forceinline__ bool tc_mbar_wait(uint64_t *b, uint32_t parity, int64
   for (uint32_t i = 1;; ++i) {
     if (tc_mbar_try_wait(b, parity)) return true;
     if ((i & 63) == 0 && (int64_t)(tc_global_ns() - t0) > timeout_ns) return false;
+  }
+}
+
+// The same wait for one of two cooperating threads: it gives up early once the
+// other has set *abort, and sets *abort itself on timeout.
+__device__ __forceinline__ bool tc_mbar_wait_or_abort(uint64_t *b, uint32_t parity, int64_t timeout_ns,
+                                                      volatile int *abort) {
+  if (tc_mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = tc_global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (tc_mbar_try_wait(b, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if ((int64_t)(tc_global_ns() - t0) > timeout_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
   }
 }
 
@@ -132,12 +150,9 @@ template <> struct TcFormat<OpF16> { static constexpr bool ok = true, bf16 = fal
 template <> struct TcFormat<OpBF16> { static constexpr bool ok = true, bf16 = true; };
 
 // A stage holds KA = 1 or 2 swizzle atoms along K (64 or 128 columns): 128 x 64 A
-// boxes, then N x 64 x boxes.  Stages: as many as fit in 100 KB (two CTAs per SM:
-// measured faster than one CTA with a deeper ring), at most kTcMaxStages.
+// boxes, then N x 64 x boxes.  The number of stages comes with the plan (its
+// shared-memory size).
 __host__ __device__ constexpr int tc_stage_bytes(int n, int ka) { return (kTcM + n) * kTcK * 2 * ka; }
-__host__ __device__ constexpr int tc_stages(int n, int ka) {
-  return 100 * 1024 / tc_stage_bytes(n, ka) < kTcMaxStages ? 100 * 1024 / tc_stage_bytes(n, ka) : kTcMaxStages;
-}
 // Wider stages for narrow N: each stage costs a fixed time to turn around, so it
 // should carry at least ~24 KB.
 __host__ __device__ constexpr int tc_atoms(int n) { return n <= 64 ? 2 : 1; }
@@ -153,7 +168,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full[kTcMaxStages], empty[kTcMaxStages];
   __shared__ uint32_t tmem_slot;
-  __shared__ int ok_flag;
+  __shared__ int abort_flag;                                  // set by either role on timeout
+  __shared__ long long sh_loaded, sh_consumed, sh_committed;  // for the drain after an abort
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t M = a.M, K = a.K;
   const int B = a.B;
@@ -190,17 +206,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_mbar_init(&empty[s], 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    ok_flag = 1;
+    abort_flag = 0;
+    sh_loaded = sh_consumed = sh_committed = -1;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
 
-  if (tid == 0) {
-    const uint32_t idesc = tc_idesc(TcFormat<Op>::bf16, N);
-    auto stage_a = [&](int s) { return smem + (size_t)s * st_bytes; };
-    auto load = [&](int64_t t, int s) {  // k-tile kt_lo + t into stage s
+  // Two roles, one thread each: lane 0 of warp 0 copies k-tiles into free stages,
+  // lane 0 of warp 1 issues the MMAs of landed stages; the other threads wait at the
+  // barrier below for the accumulators.
+  auto stage_a = [&](int s) { return smem + (size_t)s * st_bytes; };
+  volatile int *abort = &abort_flag;
+  if (warp == 0 && lane == 0) {
+    int64_t loaded = -1;
+    for (int64_t t = 0; t < nt; ++t) {
+      const int s = (int)(t % S);
+      // the stage is free once the MMAs of tile t - S have completed
+      if (t >= S && !tc_mbar_wait_or_abort(&empty[s], (uint32_t)(((t - S) / S) & 1), a.timeout_ns, abort)) break;
       tc_mbar_arrive_expect_tx(&full[s], st_bytes);
       const int32_t k0 = (int32_t)((kt_lo + t) * KT);
 #pragma unroll
@@ -208,16 +232,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_tma_2d(stage_a(s) + j * a_atom, &map_a, k0 + j * kTcK, (int32_t)m0, &full[s]);
         tc_tma_2d(stage_a(s) + a_bytes + j * x_atom, &map_x, k0 + j * kTcK, 0, &full[s]);
       }
-    };
-    int64_t loaded = -1, consumed = -1, committed = -1;  // highest tile copied / waited for / committed
-    bool ok = true;
-    for (int64_t t = 0; t < nt && t < S; ++t) {
-      load(t, (int)t);
       loaded = t;
     }
-    for (int64_t i = 0; i < nt && ok; ++i) {
+    sh_loaded = loaded;
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = tc_idesc(TcFormat<Op>::bf16, N);
+    int64_t consumed = -1, committed = -1;
+    bool ok = true;
+    for (int64_t i = 0; i < nt; ++i) {
       const int s = (int)(i % S);
-      if (!tc_mbar_wait(&full[s], (uint32_t)((i / S) & 1), a.timeout_ns)) {
+      if (!tc_mbar_wait_or_abort(&full[s], (uint32_t)((i / S) & 1), a.timeout_ns, abort)) {
         ok = false;
         break;
       }
@@ -234,35 +258,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_commit(&empty[s]);
         committed = i;
       }
-      // refill the stage of tile i - kTcLag once its MMAs are done: those were
-      // committed kTcLag iterations ago, so the wait rarely has to wait
-      const int64_t j = i - (S > kTcLag ? kTcLag : S - 1);
-      if (j >= 0 && j + S < nt) {
-        const int ps = (int)(j % S);
-        if (!tc_mbar_wait(&empty[ps], (uint32_t)((j / S) & 1), a.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        load(j + S, ps);
-        loaded = j + S;
-      }
     }
-    if (ok) ok = tc_mbar_wait(&empty[(nt - 1) % S], (uint32_t)(((nt - 1) / S) & 1), a.timeout_ns);
-    if (!ok) {
-      // nothing may be in flight when the CTA frees its tensor memory and exits:
-      // the last committed MMAs (their commit covers all earlier ones) and every
-      // copy issued but not waited for
+    // the last commit covers every MMA of the CTA
+    if (ok) tc_mbar_wait_or_abort(&empty[(nt - 1) % S], (uint32_t)(((nt - 1) / S) & 1), a.timeout_ns, abort);
+    sh_consumed = consumed;
+    sh_committed = committed;
+  }
+  __syncthreads();
+  if (abort_flag) {
+    // nothing may be in flight when the CTA frees its tensor memory and exits: the
+    // last committed MMAs (their commit covers all earlier ones) and every copy
+    // issued but not waited for
+    if (tid == 0) {
       if (a.status != nullptr) atomicOr(a.status, kTcStatusMma);
+      const int64_t committed = sh_committed, consumed = sh_consumed, loaded = sh_loaded;
       bool drained = committed < 0 ||
                      tc_mbar_wait(&empty[committed % S], (uint32_t)((committed / S) & 1), a.timeout_ns);
       for (int64_t t = consumed + 1; t <= loaded && drained; ++t)
         drained = tc_mbar_wait(&full[t % S], (uint32_t)((t / S) & 1), a.timeout_ns);
       if (!drained && a.status != nullptr) atomicOr(a.status, kTcStatusDrain);
     }
-    ok_flag = ok ? 1 : 0;
-  }
-  __syncthreads();
-  if (!ok_flag) {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");

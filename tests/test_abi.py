@@ -287,18 +287,21 @@ def test_plan_tensor_cores():
     # 17..256 vectors of fp16/bf16: the tcgen05 kernel, N = B rounded up to 16
     p = g.plan_for("bf16", 4096, 4096, 32)
     assert p["kernel"] == K["tc"] and p["nb"] == 32 and p["threads"] == 128 and p["grid"] == 32
-    # N <= 64: stages of two 64-column atoms (128 + N rows x 256 bytes), as many as
-    # fit in 100 KB (at most 8), + 1024 bytes to align them
-    assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024
-    # split-K so that all CTAs run in one wave (two CTAs per SM here): at most 9
-    # slices of 32 k-tiles of 128, i.e. 8 slices of 4 (no empty slice)
-    assert p["splits"] == 8 and p["unroll"] == 4 and p["workspace_bytes"] == 8 * 32 * 4096 * 4
-    assert p["grid"] * p["splits"] <= 2 * 152
+    # N <= 64: stages of two 64-column atoms (128 + N rows x 256 bytes); 32 row tiles
+    # leave SMs free, so the deep ring: as many stages as fit in 200 KB (at most 8),
+    # + 1024 bytes to align them, one CTA per SM
+    assert p["smem_bytes"] == 5 * (128 + 32) * 256 + 1024
+    # split-K so that all CTAs run in one wave: 4 slices of 8 k-tiles of 128
+    assert p["splits"] == 4 and p["unroll"] == 8 and p["workspace_bytes"] == 4 * 32 * 4096 * 4
+    assert p["grid"] * p["splits"] <= 152
     p = g.plan_for("f16", 4096, 4096, 17)
     assert p["kernel"] == K["tc"] and p["nb"] == 32
+    # at least as many row tiles as SMs: two CTAs per SM, a 100 KB ring
     p = g.plan_for("bf16", 128256, 4096, 256)
     assert p["kernel"] == K["tc"] and p["nb"] == 256 and p["splits"] == 1 and p["workspace_bytes"] == 0
     assert p["smem_bytes"] == 2 * (128 + 256) * 128 + 1024
+    p = g.plan_for("bf16", 28672, 4096, 32)
+    assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024 and p["grid"] == 224 and p["splits"] == 1
     # no empty slice: splits * k-tiles per slice covers K exactly once
     for M, Kd in ((300, 1000), (1, 64), (5000, 4104), (128, 16384)):
         p = g.plan_for("bf16", M, Kd, 40)
