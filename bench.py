@@ -44,6 +44,7 @@ import workloads as W  # noqa: E402
 METRIC = "GEMV achieved HBM GB/s (cold L2) & % of GB300 peak; µs per y=A·x"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 # the kernel code and its launch configuration: the DRAM traffic of a committed
 # ncu capture is reported only while these are unchanged
 KERNEL_SOURCES = ["gemv_kernels.cuh", "gemv_launch.cuh", "gemv_plan.cpp"]
@@ -119,6 +120,17 @@ def measured_peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak_tflops():
+    """Dense bf16 tensor throughput (burst) measured on this GPU model, else the
+    fallback figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def host_cores() -> int:
@@ -384,7 +396,7 @@ def sweep(args, torch, g, dev, flush, peak):
     """Every configuration at full size (and the int4 workloads): µs, GB/s and
     fraction of peak."""
     out = []
-    names = [w.name for w in W.CONFIGS + W.W4_CONFIGS]
+    names = [w.name for w in W.CONFIGS + W.W4_CONFIGS + W.TC_CONFIGS]
     if args.only:
         names = [n for n in names if n in args.only.split(",")]
     for n in names:
@@ -403,6 +415,9 @@ def sweep(args, torch, g, dev, flush, peak):
                     "qmin_bytes": w.qmin_bytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                     "gflops": round(w.flops / (med * 1e-3) / 1e9, 1),
                     "roofline_us": round(w.qmin_bytes / (peak * 1e9) * 1e6, 3)})
+        if plan["kernel_name"] == "tc":  # a contraction on the tensor cores: its own roofline too
+            tp, _ = measured_tensor_peak_tflops()
+            out[-1]["frac_of_tensor_peak"] = round(w.flops / (med * 1e-3) / 1e12 / tp, 4)
         del d, y
         torch.cuda.empty_cache()
     return out

@@ -36,6 +36,8 @@ W4_GROUP = 128  # elements of a row that share one int4 scale
 KERNELS = {"auto": 0, "rows_per_warp": 1, "warp_per_row": 2, "block_per_row": 3,
            "split_k": 4, "batched": 5, "scalar": 6, "stream": 7, "xsplit": 8, "tc": 9}
 X_STAGING = {0: "global", 1: "smem", 2: "smem_fp32", 3: "regs"}
+# BATCHED kernel variants (plan "variant"; force_kernel("batched", variant + 1))
+BATCHED_ROWPAIR, BATCHED_RING, BATCHED_RING_MIXED = 0, 1, 2
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
 
@@ -44,7 +46,7 @@ class Plan(ctypes.Structure):
                 ("rows_per_warp", ctypes.c_int), ("splits", ctypes.c_int), ("unroll", ctypes.c_int),
                 ("x_staging", ctypes.c_int), ("nb", ctypes.c_int),
                 ("threads", ctypes.c_int), ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("variant", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}

@@ -144,9 +144,11 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   gemv_plan_t p;
   if (swiglu) {
     // one vector: the streaming kernel walks gate/up row pairs; more: the batched
-    // kernels carry each pair as their R = 2 rows
+    // kernels carry each pair as two of their rows (the variant the dispatcher picks,
+    // or the one a test forced)
     const int want = B == 1 ? GEMV_KERNEL_STREAM : GEMV_KERNEL_BATCHED;
-    st = gemv::plan(dtype, M, K, B, al16, sms, want, B == 1 ? 0 : 2, &p);
+    const int param = B > 1 && g_force_kernel == GEMV_KERNEL_BATCHED ? g_force_param : 0;
+    st = gemv::plan(dtype, M, K, B, al16, sms, want, param, &p);
     if (st != GEMV_SUCCESS) return st;
     if (p.kernel != want) return GEMV_ERR_UNSUPPORTED;
   } else {

@@ -16,9 +16,12 @@
 //   k_blockrow  all 256 threads of a CTA on one row (lesson 3's block-per-row
 //               kernel), optionally over one K slice of it (split-K pass 1).
 //   k_splitk_reduce  split-K pass 2: sums the slices in slice order.
-//   k_batch_lo  2 <= B <= 4: x in shared memory (fp32 where it fits), R rows per
-//               warp, every widened A element meets all B vectors, packed FMAs.
-//   k_batched2  5 <= B <= 16: x in shared memory as stored, R rows per warp.
+//   k_batched2  2 <= B <= 16 (row pairs): x in shared memory as stored, 2 rows per
+//               warp, the next loads in registers, mixed-precision FMAs.
+//   k_batch_ring  2 <= B <= 16: A through a per-thread cp.async ring, x in shared
+//               memory (fp32 where it fits), R rows per warp, packed FMAs.
+//   k_xsplit    B <= 4: the CTA splits K, x in fp32 registers.
+//   k_tc        fp16/bf16, 17..256 vectors: tcgen05 tensor cores (gemv_tc.cuh).
 //
 // All reductions are fixed trees (xor butterflies, shared memory in warp order,
 // slices in index order): no atomics, bitwise-reproducible results.
@@ -182,6 +185,10 @@ struct OpBF16 {
     pair1(acc, a.z, xv[0].z);
     pair1(acc, a.w, xv[0].w);
   }
+  // acc += a * x, bf16 operands, fp32 accumulator (the product is exact in fp32)
+  __device__ static __forceinline__ void fma_mixed(float &acc, unsigned short a, unsigned short x) {
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
+  }
   __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
     const uint32_t u0 = w ? a.z : a.x, u1 = w ? a.w : a.y;
     q01 = make_float2(bf16_lo(u0), bf16_hi(u0));
@@ -243,6 +250,10 @@ struct OpF16 {
     pair1(acc, a.y, xv[0].y);
     pair1(acc, a.z, xv[0].z);
     pair1(acc, a.w, xv[0].w);
+  }
+  // acc += a * x, fp16 operands, fp32 accumulator (the product is exact in fp32)
+  __device__ static __forceinline__ void fma_mixed(float &acc, unsigned short a, unsigned short x) {
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(x));
   }
   __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
     q01 = f16x2_to_f2(w ? a.z : a.x);
@@ -968,154 +979,6 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   }
 }
 
-// ------------------------------------------------------------------ k_batch_lo
-// 2 <= B <= 4 (NB in {1, 2, 4}).  x[0..B) staged once per CTA in shared memory,
-// fp32 when XF32, laid out as [b][quad w][chunk c][4] so that the lanes of a warp
-// (consecutive chunks) read consecutive words: no bank conflicts.  Vectors
-// B..NB-1 are zero, so the inner loops run over all NB vectors without a branch.  Each warp
-// carries R rows and takes U chunks of each per step; every A element is widened
-// once and meets all B vectors; every x value feeds R rows.  (even, odd)
-// accumulator pairs take packed FMAs.  The next step's loads (possibly of the next
-// row group) are in flight while the current step is used, and the first ones are
-// issued before x is staged.
-template <class Op, int NB, int R, int U, int THREADS, bool XF32, bool SW = false>
-__global__ void __launch_bounds__(THREADS, 1) k_batch_lo(const Args a) {
-  static_assert(!SW || R == 2, "SwiGLU pairs the gate and up row of one output");
-  extern __shared__ __align__(16) unsigned char xs[];
-  constexpr int WARPS = THREADS / 32;
-  constexpr int QW = Op::VEC / 4;
-  constexpr int SX = (int)sizeof(typename Op::TX);
-  constexpr int XE = XF32 ? 4 : SX;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t M = a.M, K = a.K;
-  const int B = a.B;
-  const uint64_t pol = evict_first_policy();
-  const int64_t nch = K / Op::VEC;
-  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
-  const char *A = reinterpret_cast<const char *>(a.A);
-  // row r of group g: g * R + r, or with SW the gate row g and the up row g + half
-  const int64_t groups = SW ? a.half : (M + R - 1) / R;
-  auto row_of = [&](int64_t gg, int r) -> int64_t { return SW ? gg + r * a.half : gg * R + r; };
-  const int64_t gstride = (int64_t)gridDim.x * WARPS;
-
-  int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
-  int64_t base = 0;  // first chunk of the step, the same in every lane of the warp
-  uint4 nxt[U][R];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int64_t row = row_of(g, r), c = base + lane + 32 * u;
-      nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
-                                                     : make_uint4(0, 0, 0, 0);
-    }
-  {  // stage x: 4-element groups, [b][w][c][4] (no runtime division)
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(a.x);
-    for (int b = 0; b < B; ++b)
-      for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
-        const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
-        unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
-        const unsigned char *sp = src + ((int64_t)b * K + k0) * SX;
-        if (SX == 4) {
-          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(sp);
-        } else if (XF32) {
-          float q[4];
-          Op::xquad(sp, q);
-          *reinterpret_cast<float4 *>(dst) = make_float4(q[0], q[1], q[2], q[3]);
-        } else {
-          *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(sp);
-        }
-      }
-    for (int b = B; b < NB; ++b)
-      for (int64_t k0 = 4 * (int64_t)tid; k0 < K; k0 += 4 * THREADS) {
-        const int64_t c = k0 / Op::VEC, w = (k0 % Op::VEC) / 4;
-        unsigned char *dst = xs + ((((int64_t)b * QW + w) * nch + c) * 4) * XE;
-        if (XE == 4) *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-        else *reinterpret_cast<uint2 *>(dst) = make_uint2(0, 0);
-      }
-    __syncthreads();
-  }
-
-  while (g < groups) {
-    float2 acc[R][NB];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
-    int64_t ng;
-    for (;;) {
-      uint4 cur[U][R];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int r = 0; r < R; ++r) cur[u][r] = nxt[u][r];
-      const int64_t cb = base + lane;
-      ng = g;
-      base += 32 * U;
-      if (base >= nch) { ng = g + gstride; base = 0; }
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int64_t row = row_of(ng, r), c = base + lane + 32 * u;
-          nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
-                                                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t cc = cb + 32 * u;
-        if (cc < nch) {
-#pragma unroll
-          for (int w = 0; w < QW; ++w) {
-            float2 q01[R], q23[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) Op::quad2(cur[u][r], w, q01[r], q23[r]);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const unsigned char *xp = xs + ((((int64_t)b * QW + w) * nch + cc) * 4) * XE;
-              float2 x01, x23;
-              if (XE == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(xp);
-                x01 = make_float2(v.x, v.y);
-                x23 = make_float2(v.z, v.w);
-              } else {
-                float q[4];
-                Op::xquad(xp, q);
-                x01 = make_float2(q[0], q[1]);
-                x23 = make_float2(q[2], q[3]);
-              }
-#pragma unroll
-              for (int r = 0; r < R; ++r) {
-                acc[r][b] = __ffma2_rn(q01[r], x01, acc[r][b]);
-                acc[r][b] = __ffma2_rn(q23[r], x23, acc[r][b]);
-              }
-            }
-          }
-        }
-      }
-      if (ng != g) break;
-    }
-    if constexpr (SW) {
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const float s0 = group_sum<32>(acc[0][b].x + acc[0][b].y);
-        const float s1 = group_sum<32>(acc[1][b].x + acc[1][b].y);
-        if (lane == 0 && b < B) epilogue_swiglu<Op>(a, b, g, s0, s1);
-      }
-    } else {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float s = group_sum<32>(acc[r][b].x + acc[r][b].y);
-          if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
-        }
-      }
-    }
-    g = ng;
-  }
-}
-
 // ------------------------------------------------------------------ k_xsplit
 // B <= 4 (NB in {1, 2, 4}): the 512 threads of a CTA split K.  Thread L (= warp *
 // 32 + lane) owns chunks c = L + 512 j (j < J) of every row and keeps x for those
@@ -1153,6 +1016,347 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
 #pragma unroll
   for (int m = 16 / NB; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
   return t;
+}
+
+// ------------------------------------------------------------------ k_batch_ring
+// 2 <= B <= 16 (NB in {2, 4, 8, 16}).  One 512-thread CTA per SM, persistent; each
+// warp carries R rows at a time (row groups dealt round-robin over CTAs and warps,
+// so every SM gets an equal share).
+// - A streams through a per-thread cp.async ring in shared memory: at step j of a
+//   row group, lane l uses chunk 32j + l of each of the R rows.  Every step is one
+//   commit group, issued G steps ahead (across row-group boundaries), and a lane
+//   reads back only the slots it filled itself, so A needs no barrier and no
+//   registers while in flight.
+// - x[0..NB) is staged once per CTA, fp32 when it fits (XE = 4) else as stored, in
+//   planes of 16-byte words indexed by chunk, so that the lanes of a warp
+//   (consecutive chunks) read consecutive words: no bank conflicts.  Vectors
+//   B..NB-1 are zero.
+// - NB <= 4: (even, odd) accumulator pairs per (row, vector); a plane holds one
+//   vector's quad w of every chunk.  NB >= 8 (PAIRS): one accumulator pair per
+//   (row, vector pair), i.e. vectors 2p and 2p + 1, which halves the accumulator
+//   registers; a plane holds vector pair p interleaved element by element
+//   (x[2p][k], x[2p+1][k]) and each A element is broadcast to both halves.  Either
+//   way each A element is widened once and meets all NB vectors through packed
+//   FMAs, and every sum is taken in element order.
+// - A row group's R * NB sums are reduced by one reduce-scatter butterfly, after
+//   which lane l holds sum l (row l / NB, vector l % NB, replicated over 32 / (R*NB)
+//   lanes) and runs its epilogue, with the operands it loaded when the group began.
+// SW (R = 2): the two rows are SwiGLU's gate row g and up row g + half.
+
+// Four 16-bit x values in two words, widened to fp32 (exact for both types).
+__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __half) {
+  const float2 f0 = f16x2_to_f2(w0), f1 = f16x2_to_f2(w1);
+  f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
+}
+__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __nv_bfloat16) {
+  f[0] = bf16_lo(w0); f[1] = bf16_hi(w0); f[2] = bf16_lo(w1); f[3] = bf16_hi(w1);
+}
+__device__ __forceinline__ float2 widen2(uint32_t w, __half) { return f16x2_to_f2(w); }
+__device__ __forceinline__ float2 widen2(uint32_t w, __nv_bfloat16) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+// The two 16-bit halves of a word (low half = lower element).
+__device__ __forceinline__ void split_halves(uint32_t w, unsigned short &lo, unsigned short &hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds8(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// inner-loop forms of k_batch_ring
+constexpr int kRingEvenOdd = 0;  // (even, odd) accumulator pairs per (row, vector)
+constexpr int kRingPairs = 1;    // one accumulator pair per (row, vector pair)
+constexpr int kRingMixed = 2;    // one fp32 accumulator per (row, vector), 16-bit operands
+
+template <class Op, int NB, int R, int G, int XE, bool SW, int MODE = (NB >= 8 ? kRingPairs : kRingEvenOdd),
+          int THREADS = 512>
+__global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
+  constexpr int WARPS = THREADS / 32;
+  constexpr bool PAIRS = MODE == kRingPairs;
+  static_assert(MODE != kRingMixed || (XE == 2 && Op::VEC == 8), "mixed FMAs take 16-bit A and x");
+  constexpr int NP = NB / 2;                      // vector pairs
+  constexpr int QW = Op::VEC / 4;                 // 4-element quads per chunk
+  constexpr int SX = (int)sizeof(typename Op::TX);
+  constexpr int V = R * NB;                       // sums per row group
+  constexpr int LOGV = V == 32 ? 5 : V == 16 ? 4 : V == 8 ? 3 : V == 4 ? 2 : 1;
+  static_assert((1 << LOGV) == V, "R * NB must be a power of two up to 32");
+  static_assert(XE == 4 || (XE == 2 && SX == 2), "x staged as fp32 or as stored 16-bit");
+  static_assert(!SW || R == 2, "SwiGLU pairs the gate and up row of one output");
+  // bytes of one staged word per chunk and plane: 16 for PAIRS and fp32 quads, 8 for
+  // 16-bit quads
+  constexpr int WB = PAIRS ? 16 : 4 * XE;
+  // planes: PAIRS fp32: [p][k pair h < VEC/2]; PAIRS 16-bit: [p][quad w];
+  // otherwise [b][quad w]
+  constexpr int PPV = PAIRS ? (XE == 4 ? Op::VEC / 2 : QW) : QW;  // planes per vector (pair)
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  const int64_t nch = K / Op::VEC;
+  if (nch == 0) return;  // K = 0 never reaches this kernel
+  const int64_t nsteps = (nch + 31) / 32;
+  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const char *A = reinterpret_cast<const char *>(a.A);
+  const int64_t groups = SW ? a.half : (M + R - 1) / R;
+  auto row_of = [&](int64_t gg, int r) -> int64_t { return SW ? gg + r * a.half : gg * R + r; };
+  const int64_t gstride = (int64_t)gridDim.x * WARPS;
+
+  // shared memory: x planes, then the ring [warp][stage][row][lane] of 16-byte slots
+  const int64_t pstride = nch * WB;  // bytes per plane
+  const int64_t xbytes = (int64_t)(PAIRS ? NP : NB) * PPV * pstride;
+  const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t ring_s = xs_s + (uint32_t)xbytes + (uint32_t)((warp * G * R * 32 + lane) * 16);
+
+  // producer position: row group pg, step pj (chunks 32 pj + lane)
+  int64_t pg = blockIdx.x + (int64_t)gridDim.x * warp, pj = 0;
+  auto issue = [&](int stage) {
+    if (pg < groups) {
+      const int64_t c = 32 * pj + lane;
+      if (c < nch) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int64_t row = row_of(pg, r);
+          if (row < M) {
+            const uint32_t dst = ring_s + (uint32_t)((stage * R + r) * 32 * 16);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(A + row * rowb + c * 16)
+                         : "memory");
+          }
+        }
+      }
+      if (++pj == nsteps) { pj = 0; pg += gstride; }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // x staging.  Copied as stored (planes of one vector's quads): cp.async straight
+  // into place, one commit group issued before A's first steps.  Interleaved or
+  // widened: eight items (quads of one vector or of a vector pair) per thread in
+  // flight through registers at a time.
+  const unsigned char *xsrc = reinterpret_cast<const unsigned char *>(a.x);
+  const int64_t nq = K / 4;  // quads per vector
+  constexpr bool XCOPY = !PAIRS && XE == SX;
+  if constexpr (XCOPY) {
+    for (int64_t i = tid; i < (int64_t)B * nq; i += THREADS) {
+      const int64_t b = i / nq, q = i - b * nq;
+      const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
+      const uint32_t dst = xs_s + (uint32_t)(((b * PPV + w) * nch + c) * WB);
+      const unsigned char *sp = xsrc + (b * K + 4 * q) * SX;
+      if constexpr (WB == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(sp) : "memory");
+      else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(sp) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int64_t i = (int64_t)B * PPV * pstride / 16 + tid; i < xbytes / 16; i += THREADS)
+      reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);  // vectors B..NB-1
+  }
+#pragma unroll
+  for (int s = 0; s < G; ++s) issue(s);
+
+  if constexpr (XCOPY) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(G) : "memory");  // x's group (the oldest)
+  } else {
+    // quad q of vector b (zero past B), as 4 fp32 values or 2 words of 16-bit values
+    auto load_quad = [&](int64_t b, int64_t q) -> uint4 {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (b < B) {
+        const unsigned char *sp = xsrc + (b * K + 4 * q) * SX;
+        if (SX == 4) {
+          v = *reinterpret_cast<const uint4 *>(sp);
+        } else {
+          const uint2 h = *reinterpret_cast<const uint2 *>(sp);
+          v.x = h.x;
+          v.y = h.y;
+        }
+      }
+      return v;
+    };
+    auto to_f32 = [&](const uint4 &v, float (&f)[4]) {
+      if constexpr (SX == 4) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+      } else {
+        widen4(v.x, v.y, f, typename Op::TX());
+      }
+    };
+    constexpr int NV = PAIRS ? NP : NB;  // items per quad index: vector pairs or vectors
+    const int64_t items = (int64_t)NV * nq;
+    for (int64_t i0 = tid; i0 < items; i0 += 8 * THREADS) {
+      uint4 v0[8], v1[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + (int64_t)u * THREADS;
+        v0[u] = make_uint4(0, 0, 0, 0);
+        v1[u] = make_uint4(0, 0, 0, 0);
+        if (i < items) {
+          const int64_t iv = i / nq, q = i - iv * nq;
+          v0[u] = load_quad(PAIRS ? 2 * iv : iv, q);
+          if (PAIRS) v1[u] = load_quad(2 * iv + 1, q);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + (int64_t)u * THREADS;
+        if (i >= items) continue;
+        const int64_t iv = i / nq, q = i - iv * nq;
+        const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
+        if constexpr (PAIRS && XE == 4) {
+          float f0[4], f1[4];
+          to_f32(v0[u], f0);
+          to_f32(v1[u], f1);
+          unsigned char *d0 = smem + ((iv * PPV + 2 * w) * nch + c) * WB;
+          *reinterpret_cast<float4 *>(d0) = make_float4(f0[0], f1[0], f0[1], f1[1]);
+          *reinterpret_cast<float4 *>(d0 + pstride) = make_float4(f0[2], f1[2], f0[3], f1[3]);
+        } else if constexpr (PAIRS) {
+          unsigned char *d = smem + ((iv * PPV + w) * nch + c) * WB;
+          *reinterpret_cast<uint4 *>(d) =
+              make_uint4(__byte_perm(v0[u].x, v1[u].x, 0x5410), __byte_perm(v0[u].x, v1[u].x, 0x7632),
+                         __byte_perm(v0[u].y, v1[u].y, 0x5410), __byte_perm(v0[u].y, v1[u].y, 0x7632));
+        } else {  // widened to fp32, one vector's quads
+          float f0[4];
+          to_f32(v0[u], f0);
+          unsigned char *d = smem + ((iv * PPV + w) * nch + c) * WB;
+          *reinterpret_cast<float4 *>(d) = make_float4(f0[0], f0[1], f0[2], f0[3]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  const int idx = lane >> (5 - LOGV);  // the sum this lane ends with
+  const bool owner = (lane & ((32 >> LOGV) - 1)) == 0;
+  int stage = 0;
+  for (int64_t g = blockIdx.x + (int64_t)gridDim.x * warp; g < groups; g += gstride) {
+    // this lane's epilogue operands (row idx / NB, vector idx % NB), in flight
+    // while the group streams
+    const int er = idx / NB, eb = idx % NB;
+    const int64_t erow = row_of(g, er);
+    const bool live = owner && eb < B && erow < M && !SW;
+    RowPre pre = row_pre<Op, false>(a, erow, live);
+    if (live && a.residual != nullptr) pre.res = residual_at<Op>(a.residual, (int64_t)eb * M + erow);
+
+    constexpr int NA = PAIRS ? NP : NB;  // accumulator pairs per row
+    float2 acc[R][NA];
+    float accm[R][NB];  // kRingMixed
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int i = 0; i < NA; ++i) acc[r][i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) accm[r][b] = 0.f;
+    }
+    for (int64_t j = 0; j < nsteps; ++j) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(G - 1) : "memory");  // this step has landed
+      uint4 av[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) av[r] = lds16(ring_s + (uint32_t)((stage * R + r) * 32 * 16));
+      issue(stage);  // this lane's slots of the stage are free again
+      stage = stage + 1 == G ? 0 : stage + 1;
+      const int64_t c = 32 * j + lane;
+      if (c >= nch) continue;
+      const uint32_t xc = xs_s + (uint32_t)(c * WB);
+#pragma unroll
+      for (int w = 0; w < QW; ++w) {
+        if constexpr (MODE == kRingMixed) {
+          // the 16-bit halves of A (once per row) and of x (once per vector), then
+          // one mixed-precision FMA per product
+          unsigned short ah[R][4];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            split_halves(w ? av[r].z : av[r].x, ah[r][0], ah[r][1]);
+            split_halves(w ? av[r].w : av[r].y, ah[r][2], ah[r][3]);
+          }
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint2 h = lds8(xc + (uint32_t)((b * PPV + w) * pstride));
+            unsigned short xh[4];
+            split_halves(h.x, xh[0], xh[1]);
+            split_halves(h.y, xh[2], xh[3]);
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) Op::fma_mixed(accm[r][b], ah[r][e], xh[e]);
+          }
+          continue;
+        }
+        float2 q01[R], q23[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) Op::quad2(av[r], w, q01[r], q23[r]);
+        if constexpr (PAIRS) {
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            float2 X[4];
+            if constexpr (XE == 4) {
+              const uint4 u0 = lds16(xc + (uint32_t)((p * PPV + 2 * w) * pstride));
+              const uint4 u1 = lds16(xc + (uint32_t)((p * PPV + 2 * w + 1) * pstride));
+              X[0] = make_float2(__uint_as_float(u0.x), __uint_as_float(u0.y));
+              X[1] = make_float2(__uint_as_float(u0.z), __uint_as_float(u0.w));
+              X[2] = make_float2(__uint_as_float(u1.x), __uint_as_float(u1.y));
+              X[3] = make_float2(__uint_as_float(u1.z), __uint_as_float(u1.w));
+            } else {
+              const uint4 u = lds16(xc + (uint32_t)((p * PPV + w) * pstride));
+              X[0] = widen2(u.x, typename Op::TX());
+              X[1] = widen2(u.y, typename Op::TX());
+              X[2] = widen2(u.z, typename Op::TX());
+              X[3] = widen2(u.w, typename Op::TX());
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              acc[r][p] = __ffma2_rn(make_float2(q01[r].x, q01[r].x), X[0], acc[r][p]);
+              acc[r][p] = __ffma2_rn(make_float2(q01[r].y, q01[r].y), X[1], acc[r][p]);
+              acc[r][p] = __ffma2_rn(make_float2(q23[r].x, q23[r].x), X[2], acc[r][p]);
+              acc[r][p] = __ffma2_rn(make_float2(q23[r].y, q23[r].y), X[3], acc[r][p]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint32_t xa = xc + (uint32_t)((b * PPV + w) * pstride);
+            float2 x01, x23;
+            if constexpr (XE == 4) {
+              const uint4 u = lds16(xa);
+              x01 = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+              x23 = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+            } else {
+              const uint2 h = lds8(xa);
+              float f[4];
+              widen4(h.x, h.y, f, typename Op::TX());
+              x01 = make_float2(f[0], f[1]);
+              x23 = make_float2(f[2], f[3]);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              acc[r][b] = __ffma2_rn(q01[r], x01, acc[r][b]);
+              acc[r][b] = __ffma2_rn(q23[r], x23, acc[r][b]);
+            }
+          }
+        }
+      }
+    }
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        v[r * NB + b] = MODE == kRingMixed ? accm[r][b]
+                        : PAIRS ? ((b & 1) ? acc[r][b / 2].y : acc[r][b / 2].x)
+                                : acc[r][b].x + acc[r][b].y;
+    const float part = warp_reduce_scatter<V>(v, lane);
+    if constexpr (SW) {
+      // gate sum b sits at lane b * 32 / V, its up sum 16 lanes above
+      const float up = __shfl_down_sync(0xffffffffu, part, 16);
+      if (owner && idx < NB && idx < B) epilogue_swiglu<Op>(a, idx, g, part, up);
+    } else {
+      if (live) store_act_res<Op>(a, (int64_t)eb * M + erow, row_value_pre<Op>(a, pre, part), pre.res);
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 template <class Op, int NB, int J, int P, int G>

@@ -43,34 +43,43 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
 
 template <class Op, int NB>
 cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
-  if constexpr (Op::GROUPED) {
-    return cudaErrorInvalidValue;  // not built for int4; the planner never picks it
+  if constexpr (Op::GROUPED || NB < 2) {
+    return cudaErrorInvalidValue;  // not built for int4 or one vector; the planner never picks it
   } else {
-  constexpr int T = kBatchedThreads;
-  const dim3 grid((unsigned)p.grid), block(T);
-  if constexpr (NB <= 4) {
-    // B <= 4: x in shared memory (fp32 where it fits), R = 2 or 4 rows per warp
+    const dim3 grid((unsigned)p.grid), block(kBatchedThreads);
     auto run = [&](auto kern) -> cudaError_t {
       cudaError_t e = allow_smem(kern, p.smem_bytes);
       if (e != cudaSuccess) return e;
       kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
       return cudaSuccess;
     };
-    // R = 2 rows per warp with U = 2 chunks per step, or R = 4 with U = 1;
-    // SwiGLU (a.half > 0) pairs each gate row with its up row (R = 2)
-    const bool f32x = p.x_staging == GEMV_X_SMEM_FP32;
-    if (a.half > 0)
-      return f32x ? run(k_batch_lo<Op, NB, 2, 2, T, true, true>) : run(k_batch_lo<Op, NB, 2, 2, T, false, true>);
-    if (p.rows_per_warp == 2)
-      return f32x ? run(k_batch_lo<Op, NB, 2, 2, T, true>) : run(k_batch_lo<Op, NB, 2, 2, T, false>);
-    return f32x ? run(k_batch_lo<Op, NB, 4, 1, T, true>) : run(k_batch_lo<Op, NB, 4, 1, T, false>);
-  } else {
-    auto kern = a.half > 0 ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
-    cudaError_t e = allow_smem(kern, p.smem_bytes);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
-    return cudaSuccess;
-  }
+    constexpr int T = kBatchedThreads;
+    static_assert(T == 512, "the ring kernel is built for 512 threads");
+    const bool sw = a.half > 0;  // SwiGLU: gate and up row of one output per row pair
+    constexpr int SX = (int)sizeof(typename Op::TX);
+    constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
+    switch (p.variant) {
+      case GEMV_BATCHED_ROWPAIR:
+        return sw ? run(k_batched2<Op, NB, 2, 2, T, true>) : run(k_batched2<Op, NB, 2, 2, T>);
+      case GEMV_BATCHED_RING: {
+        constexpr int R = ring_rows(NB), G = 8 / R;
+        constexpr int MODE = NB >= 8 ? kRingPairs : kRingEvenOdd;
+        const bool x32 = p.x_staging == GEMV_X_SMEM_FP32 || SX == 4;
+        if (!sw && p.rows_per_warp != R) return cudaErrorInvalidValue;
+        if (sw)
+          return x32 ? run(k_batch_ring<Op, NB, 2, 4, 4, true, MODE>) : run(k_batch_ring<Op, NB, 2, 4, SX, true, MODE>);
+        return x32 ? run(k_batch_ring<Op, NB, R, G, 4, false, MODE>) : run(k_batch_ring<Op, NB, R, G, SX, false, MODE>);
+      }
+      case GEMV_BATCHED_RING_MIXED:
+        if constexpr (A16 && SX == 2 && Op::VEC == 8) {
+          if (p.rows_per_warp != 2 || p.x_staging != GEMV_X_SMEM) return cudaErrorInvalidValue;
+          return sw ? run(k_batch_ring<Op, NB, 2, 4, 2, true, kRingMixed>)
+                    : run(k_batch_ring<Op, NB, 2, 4, 2, false, kRingMixed>);
+        }
+        return cudaErrorInvalidValue;
+      default:
+        return cudaErrorInvalidValue;
+    }
   }
 }
 

@@ -12,9 +12,11 @@
 //   fp16/bf16 with 17..256 vectors        -> TC (tcgen05 small-N GEMM)
 //   rows not 16-byte aligned              -> SCALAR (element loads)
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
-//   fp32/fp16/bf16, B in 2..4, x slice fits 64 registers, at least 16 rows
-//     per SM and M < 65536               -> XSPLIT (K split over a CTA)
-//   B >= 2 and x[0..B) fits in smem       -> BATCHED
+//   fp32, B == 2, x slice fits 64 registers, at least 16 rows per SM and
+//     M < 65536                           -> XSPLIT (K split over a CTA)
+//   B >= 2 and x[0..B) fits in smem       -> BATCHED: fp16/bf16 with 9..16
+//     vectors and at most one row pair per warp -> ROWPAIR, otherwise the
+//     cp.async ring (mixed-precision FMAs for fp16/bf16 with 9..16 vectors)
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
 //   B == 1 and at least 16 rows per SM    -> STREAM (persistent warps)
 //   at least 16 rows per SM, or <= 4 KB   -> WARP_PER_ROW
@@ -63,11 +65,14 @@ int chunk_elems(int dtype) {
 
 static bool rowteam_lanes_ok(int l) { return l == 1 || l == 2 || l == 4 || l == 8 || l == 16; }
 
-// x staging of the batched kernels (NB vectors, the padded ones zero): B <= 4
-// prefers fp32 in shared memory.
-static int batched_staging(int nb, int64_t K, int sx) {
-  if (nb <= 4 && (int64_t)nb * K * 4 <= kBatchedSmemMax) return GEMV_X_SMEM_FP32;
-  if ((int64_t)nb * K * sx <= kBatchedSmemMax) return GEMV_X_SMEM;
+// The row-pair kernel stages x[0..NB) as stored.
+static bool rowpair_fits(int nb, int64_t K, int sx) { return (int64_t)nb * K * sx <= kBatchedSmemMax; }
+
+// x staging of the BATCHED ring kernel: fp32 where x and the ring fit, else as
+// stored; -1 if x does not fit.
+static int ring_staging(int nb, int64_t K, int sx) {
+  if (sx != 4 && (int64_t)nb * K * 4 + kRingBytes <= kRingSmemMax) return GEMV_X_SMEM_FP32;
+  if ((int64_t)nb * K * sx + kRingBytes <= kRingSmemMax) return GEMV_X_SMEM;
   return -1;
 }
 
@@ -95,7 +100,11 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   if (B > GEMV_MAX_BATCH && !vec_ok) return GEMV_ERR_UNSUPPORTED;
   const bool tc_ok = half16 && vec_ok;
   // the batched shared-memory kernels are not built for int4 (grouped scales)
-  const int bstage = dtype == GEMV_DTYPE_W4 ? -1 : batched_staging(p.nb, K, sx);
+  // the batched kernels are not built for int4 (grouped scales)
+  const int rstage = dtype == GEMV_DTYPE_W4 ? -1 : ring_staging(p.nb, K, sx);
+  const bool rowpair_ok = dtype != GEMV_DTYPE_W4 && rowpair_fits(p.nb, K, sx);
+  const bool mixed_ok = half16 && (int64_t)p.nb * K * 2 + kRingBytes <= kRingSmemMax;
+  const bool batched_ok = rstage >= 0 || rowpair_ok;
   // XSPLIT: chunks per thread J (a power of two up to 4) and x registers
   const int xs_j = vec_ok && nch > 0 ? next_pow2(ceil_div(nch, kXsplitThreads)) : 0;
   const bool xs_ok = vec_ok && dtype != GEMV_DTYPE_W4 && p.nb <= 4 && xs_j >= 1 && xs_j <= 4 &&
@@ -117,8 +126,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         ok = vec_ok && nch >= 2 && force_param >= 0;
         break;
       case GEMV_KERNEL_BATCHED:
-        ok = vec_ok && bstage >= 0 &&
-             (force_param == 0 || force_param == 2 || (force_param == 4 && p.nb <= 4));
+        ok = vec_ok && B >= 2 &&
+             ((force_param == 0 && batched_ok) || (force_param == 1 + GEMV_BATCHED_RING && rstage >= 0) ||
+              (force_param == 1 + GEMV_BATCHED_ROWPAIR && rowpair_ok) ||
+              (force_param == 1 + GEMV_BATCHED_RING_MIXED && mixed_ok));
         break;
       case GEMV_KERNEL_STREAM:
         ok = vec_ok && B == 1;
@@ -147,12 +158,12 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       kernel = GEMV_KERNEL_SCALAR;
     } else if (nch <= 16) {
       kernel = GEMV_KERNEL_ROWS_PER_WARP;
-    } else if (xs_ok && dtype != GEMV_DTYPE_W8 && B > 1 && M >= (int64_t)num_sms * 16 && M < 65536) {
-      // float types with 2..4 vectors: K split over a CTA, x in registers (the int8
-      // decode is cheaper in the row-per-warp kernels; with one vector the
-      // streaming kernel is as fast and needs no 128 KB shared-memory carve-out)
+    } else if (xs_ok && dtype == GEMV_DTYPE_F32 && B == 2 && M >= (int64_t)num_sms * 16 && M < 65536) {
+      // fp32 with 2 vectors: K split over a CTA, x in registers (measured: fp32
+      // 8192x4096 26.6 us against 28.7 in the ring kernel; for 16-bit types and
+      // more vectors the ring kernel is faster, with one vector the streaming one)
       kernel = GEMV_KERNEL_XSPLIT;
-    } else if (B > 1 && bstage >= 0 && nch >= 32) {
+    } else if (B > 1 && batched_ok && nch >= 32) {
       kernel = GEMV_KERNEL_BATCHED;
     } else if (M >= 65536) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;
@@ -220,14 +231,37 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // x is staged once per CTA, so the grid is persistent: one 512-thread CTA
       // per SM; each warp carries R rows.
       // x[0..NB) is staged (vectors B..NB-1 zero): the inner loops have no branch
-      int r = param != 0 ? param : 2;
-      if (p.nb > 4) r = 2;
-      p.rows_per_warp = r;
       p.threads = kBatchedThreads;
-      p.x_staging = p.nb <= 4 ? bstage : GEMV_X_SMEM;
-      p.unroll = r == 4 ? 1 : 2;
-      p.smem_bytes = (int)((int64_t)p.nb * K * (p.x_staging == GEMV_X_SMEM_FP32 ? 4 : sx));
       p.grid = num_sms;
+      // variant: forced (param = variant + 1), else the row-pair kernel for 4..16
+      // vectors with at most one row pair per warp (nothing to amortise a ring's
+      // fill on: f16 4096x4096 B = 4 14.3 us against 16.4, bf16 4096x14336 B = 4
+      // 30.7 against 36.9), else the ring, with mixed-precision FMAs for fp16/bf16
+      // with 2 or 9..16 vectors (bf16 14336x4096 B = 16 63.5 us against 65.5 with
+      // packed FMAs and 72.9 in the row-pair kernel; B = 2 24.0 against 26.6) and
+      // packed FMAs otherwise (B = 8 34.8 us against 38.9 mixed and 44.0 row-pair)
+      int v;
+      if (param != 0) {
+        v = param - 1;
+      } else if (rstage < 0 || (rowpair_ok && p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2)) {
+        v = GEMV_BATCHED_ROWPAIR;
+      } else {
+        v = (half16 && (p.nb == 16 || p.nb == 2) && mixed_ok) ? GEMV_BATCHED_RING_MIXED : GEMV_BATCHED_RING;
+      }
+      p.variant = v;
+      if (v == GEMV_BATCHED_ROWPAIR) {
+        p.rows_per_warp = 2;
+        p.x_staging = GEMV_X_SMEM;
+        p.unroll = 2;
+        p.smem_bytes = (int)((int64_t)p.nb * K * sx);
+      } else {
+        // ring: R rows per warp, a G = 8 / R step ring; the mixed form reads x as stored
+        const int xs = v == GEMV_BATCHED_RING_MIXED ? GEMV_X_SMEM : rstage;
+        p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb);
+        p.x_staging = xs;
+        p.unroll = 8 / p.rows_per_warp;
+        p.smem_bytes = (int)((int64_t)p.nb * K * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes);
+      }
       break;
     }
     case GEMV_KERNEL_TC: {

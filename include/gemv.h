@@ -233,7 +233,16 @@ typedef struct gemv_plan {
   int64_t grid;            /* CTAs of the first (or only) kernel */
   int smem_bytes;          /* dynamic shared memory per CTA */
   int64_t workspace_bytes; /* split-K partial sums (stream-ordered pool) */
+  int variant;             /* BATCHED: GEMV_BATCHED_* */
 } gemv_plan_t;
+
+/* BATCHED kernel variants (gemv_plan_t.variant; also the force parameter + 1). */
+#define GEMV_BATCHED_ROWPAIR 0    /* x as stored, 2 rows per warp, the next loads in
+                                     registers, mixed-precision FMAs */
+#define GEMV_BATCHED_RING 1       /* A through a per-thread cp.async ring in shared
+                                     memory, x widened to fp32 where it fits, packed
+                                     fp32x2 FMAs (vector pairs for 8 and 16 vectors) */
+#define GEMV_BATCHED_RING_MIXED 2 /* the ring with mixed-precision FMAs on 16-bit A and x */
 
 /* Host-only: the plan the entry points would use on a device with `num_sms` SMs.
  * `aligned16` says whether A and x start on 16-byte boundaries.  Launches nothing,
@@ -246,8 +255,8 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
 /* TEST ONLY — not thread-safe.  Make every later call use `kernel` with `param`
  * (lanes_per_row, rows_per_warp or splits; 0 = the dispatcher's choice) when the
  * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  STREAM needs
- * B == 1; BATCHED needs x[0..B) to fit in shared memory and takes rows_per_warp
- * 2 or 4 for B <= 4 and 2 for B > 4.  A forced kernel
+ * B == 1; BATCHED needs x[0..B) to fit in shared memory and takes the variant + 1
+ * (GEMV_BATCHED_*; the mixed-precision ring only for fp16/bf16).  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);

@@ -145,17 +145,18 @@ def test_plan_config_shapes():
     p = g.plan_for("f16", 4096, 4096, 1)
     assert p["kernel"] == K["stream"] and p["unroll"] == 4 and p["x_staging"] == 1
     assert p["smem_bytes"] == 4096 * 2 and p["grid"] == 2 * 152
-    p = g.plan_for("f16", 4096, 4096, 16)
+    p = g.plan_for("f16", 4096, 4096, 16)   # one row pair per warp: the row-pair kernel
     assert p["kernel"] == K["batched"] and p["nb"] == 16 and p["x_staging"] == 1
+    assert p["variant"] == g.BATCHED_ROWPAIR
     assert p["smem_bytes"] == 16 * 4096 * 2 and p["rows_per_warp"] == 2 and p["grid"] == 152
     for M, Kd in ((14336, 4096), (4096, 14336)):
         assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["stream"]
     p = g.plan_for("bf16", 128256, 4096, 1)
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
     assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["stream"]
-    p = g.plan_for("w8", 8192, 8192, 4)
-    assert p["kernel"] == K["batched"] and p["x_staging"] == 2 and p["rows_per_warp"] == 2
-    assert p["smem_bytes"] == 4 * 8192 * 4 and p["unroll"] == 2
+    p = g.plan_for("w8", 8192, 8192, 4)     # the ring: fp32 x (128 KB) + the 64 KB ring
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["x_staging"] == 2
+    assert p["rows_per_warp"] == 4 and p["unroll"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + 64 * 1024
 
 
 def test_plan_stream_needs_one_vector():
@@ -169,34 +170,57 @@ def test_plan_stream_needs_one_vector():
 
 def test_plan_xsplit():
     K = g.KERNELS
-    # float types with 2..4 vectors whose x slice fits 64 registers per thread
-    for dt, Kd, B, J in (("f16", 4096, 4, 1), ("bf16", 8192, 4, 2), ("bf16", 14336, 2, 4), ("f32", 4096, 3, 2),
-                         ("f32", 8192, 2, 4)):
-        p = g.plan_for(dt, 14336, Kd, B)
-        assert p["kernel"] == K["xsplit"] and p["unroll"] == J, (dt, Kd, B, p)
+    # fp32 with 2 vectors whose x slice fits 64 registers per thread
+    for Kd, J in ((4096, 2), (8192, 4), (2048, 1)):
+        p = g.plan_for("f32", 14336, Kd, 2)
+        assert p["kernel"] == K["xsplit"] and p["unroll"] == J, (Kd, p)
         assert p["smem_bytes"] == 128 * 1024 and p["grid"] == 152
-    # int8 keeps the row-per-warp kernels; so does every type with one vector
-    assert g.plan_for("w8", 8192, 8192, 4)["kernel"] == K["batched"]
+    # 16-bit and int8 types, and fp32 with 3..4 vectors, take the ring kernel; one
+    # vector the streaming kernel
+    for dt, Kd, B in (("f16", 4096, 4), ("bf16", 8192, 4), ("bf16", 14336, 2), ("f32", 4096, 3), ("w8", 8192, 4)):
+        p = g.plan_for(dt, 14336, Kd, B)
+        assert p["kernel"] == K["batched"], (dt, Kd, B, p)
+        assert p["variant"] == (g.BATCHED_RING_MIXED if (dt, B) == ("bf16", 2) else g.BATCHED_RING), (dt, B, p)
     assert g.plan_for("bf16", 14336, 4096, 1)["kernel"] == K["stream"]
     assert g.plan_for("f32", 16384, 4096, 1)["kernel"] == K["stream"]
-    # x slice too large for registers (4 vectors x 4 chunks x 8 values) -> batched
-    assert g.plan_for("bf16", 4096, 16384, 4)["kernel"] == K["batched"]
     # few rows per SM, or very many rows -> not the K-split kernel
-    assert g.plan_for("bf16", 1000, 4096, 4)["kernel"] != K["xsplit"]
-    assert g.plan_for("bf16", 128256, 4096, 2)["kernel"] != K["xsplit"]
+    assert g.plan_for("f32", 1000, 4096, 2)["kernel"] != K["xsplit"]
+    assert g.plan_for("f32", 128256, 4096, 2)["kernel"] != K["xsplit"]
 
 
 def test_plan_batched_staging():
-    # fp32 x in shared memory for B <= 4 when it fits, as stored when only that fits
-    p = g.plan_for("w8", 4096, 8192, 4)
-    assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4
-    p = g.plan_for("bf16", 4096, 16384, 4)
-    assert p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2
-    p = g.plan_for("bf16", 4096, 4096, 8)
-    assert p["x_staging"] == 1 and p["rows_per_warp"] == 2
+    K = g.KERNELS
+    ring = 64 * 1024
+    # the ring: fp32 x when x and the 64 KB ring fit in 227 KB, else x as stored
+    p = g.plan_for("w8", 8192, 8192, 4)
+    assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + ring
+    p = g.plan_for("bf16", 8192, 16384, 4)
+    assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2 + ring
+    assert p["rows_per_warp"] == 4 and p["unroll"] == 2
+    # at most one row pair per warp (M <= 2 x 16 warps x 152 SMs) and 4..16 vectors:
+    # the row-pair kernel, x as stored
+    p = g.plan_for("bf16", 4096, 14336, 4)
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1 and p["smem_bytes"] == 4 * 14336 * 2
+    assert g.plan_for("f16", 4096, 4096, 2)["variant"] == g.BATCHED_RING_MIXED
+    assert g.plan_for("w8", 4096, 4096, 2)["variant"] == g.BATCHED_RING
+    p = g.plan_for("bf16", 8192, 4096, 8)   # vector pairs, 4 rows per warp, 2-step ring
+    assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["unroll"] == 2
+    # 9..16 vectors of fp16/bf16: the mixed-precision ring with many rows, the row-pair
+    # kernel with at most one row pair per warp
+    p = g.plan_for("bf16", 14336, 4096, 16)
+    assert p["variant"] == g.BATCHED_RING_MIXED and p["x_staging"] == 1 and p["smem_bytes"] == 16 * 4096 * 2 + ring
+    p = g.plan_for("f16", 4864, 4096, 9)
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 4096 * 2
+    p = g.plan_for("f16", 4866, 4096, 9)
+    assert p["variant"] == g.BATCHED_RING_MIXED and p["rows_per_warp"] == 2 and p["unroll"] == 4
+    # x too large for the ring but within 200 KB: the row-pair kernel
+    p = g.plan_for("bf16", 20000, 6144, 16)
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 6144 * 2
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
-    assert g.plan_for("w8", 4096, 4096, 3)["smem_bytes"] == 4 * 4096 * 4
+    assert g.plan_for("w8", 8192, 4096, 3)["smem_bytes"] == 4 * 4096 * 4 + ring
     assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
+    # int4 has no batched kernel
+    assert g.plan_for("w4", 8192, 8192, 4)["kernel"] != K["batched"]
 
 
 def test_plan_small_k_lanes():

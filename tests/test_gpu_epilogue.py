@@ -91,6 +91,31 @@ def test_swiglu(dtype):
                               what=f"swiglu {dtype} I={I} K={K} B={B} [{g.last_plan()['kernel_name']}]")
 
 
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_swiglu_batched_variants(dtype):
+    # every batched kernel variant (forced: variant + 1) carries SwiGLU's gate/up row pairs
+    I, K = 1000, 2048
+    for B in (2, 7, 16):
+        w = W.small(dtype, 2 * I, K, B, True, seed=3100 + B)
+        inp = W.make_inputs(w)
+        y_ref, gate, up, adg, adu = oracle.swiglu(dtype, W.storage_bits(inp["A"]), W.storage_bits(inp["x"]),
+                                                  W.storage_bits(inp["bias"]),
+                                                  None if inp["scale"] is None else inp["scale"].numpy(),
+                                                  nthreads=U.threads())
+        d = U.to_device(inp)
+        for param in (1, 2, 3):
+            if param == 3 and dtype not in ("f16", "bf16"):
+                continue
+            g.force_kernel("batched", param)
+            y = torch.empty((B, I), dtype=U.out_dtype(dtype), device="cuda")
+            g.gemv_swiglu(dtype, d["A"], d["scale"], d["x"], d["bias"], y, I, K, B)
+            plan = g.last_plan()
+            g.force_kernel("auto")
+            assert plan["kernel_name"] == "batched" and plan["variant"] == param - 1, plan
+            U.assert_close_swiglu(dtype, y, y_ref, gate, up, adg, adu,
+                                  what=f"swiglu {dtype} B={B} variant={param - 1}")
+
+
 def test_swiglu_decode_size():
     # the gate/up projection of a Llama-3-8B-shaped layer: I = 14336, K = 4096
     I, K = 14336, 4096

@@ -52,7 +52,7 @@ SHAPES = [  # (M, K) with several tiles and ragged tails for each kernel family
 ]
 FORCED = [("rows_per_warp", 0), ("rows_per_warp", 1), ("rows_per_warp", 16),
           ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0), ("split_k", 3),
-          ("split_k", 7), ("batched", 2), ("batched", 4), ("scalar", 4), ("scalar", 32),
+          ("split_k", 7), ("batched", 1), ("batched", 2), ("batched", 3), ("scalar", 4), ("scalar", 32),
           ("stream", 0), ("xsplit", 0)]
 
 
@@ -74,8 +74,13 @@ def forced_feasible(dtype, kernel, param, K, B):
     sx = 4 if dtype == "f32" else 2
     nb = 1 << (B - 1).bit_length()
     if kernel == "batched":
-        fits = (nb <= 4 and nb * K * 4 <= 200 * 1024) or nb * K * sx <= 200 * 1024
-        return fits and (param in (0, 2) or (param == 4 and nb <= 4))
+        # param = variant + 1: 1 the row-pair kernel (x as stored in 200 KB), 2 the
+        # cp.async ring (x and a 64 KB ring in 227 KB), 3 the mixed-precision ring
+        ring = (sx != 4 and nb * K * 4 + 65536 <= 227 * 1024) or nb * K * sx + 65536 <= 227 * 1024
+        rowpair = nb * K * sx <= 200 * 1024
+        mixed = dtype in ("f16", "bf16") and nb * K * 2 + 65536 <= 227 * 1024
+        ok = {0: ring or rowpair, 1: rowpair, 2: ring, 3: mixed}.get(param, False)
+        return B >= 2 and ok
     if kernel == "split_k":
         return K * sa // 16 >= 2
     if kernel == "stream":
@@ -107,6 +112,8 @@ def test_forced_kernel(dtype, kernel, param):
             g.force_kernel("auto")
             if forced_feasible(dtype, kernel, param, K, B):
                 assert plan["kernel"] == g.KERNELS[kernel], (plan, kernel)
+                if kernel == "batched" and param > 0:
+                    assert plan["variant"] == param - 1, (plan, param)
             U.assert_close(dtype, y, y_ref, absdot, with_rounding=True,
                            what=f"{dtype} {kernel}/{param} M={M} K={K} B={B} bias={bias}")
 
@@ -154,7 +161,8 @@ def test_unaligned_rows(dtype):
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
 def test_guard_bytes_untouched(dtype):
-    for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("batched", 4, 4), ("batched", 2, 9),
+    for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("batched", 1, 4), ("batched", 2, 9),
+                             ("batched", 1, 9), ("batched", 3, 16), ("batched", 3, 2),
                              ("block_per_row", 0, 4), ("rows_per_warp", 2, 4), ("scalar", 32, 4),
                              ("stream", 0, 1), ("warp_per_row", 0, 3), ("xsplit", 0, 3), ("xsplit", 0, 1)):
         M, K = 333, 256
@@ -248,7 +256,8 @@ def test_exact_closed_forms_on_gpu(dtype):
     # A = 1, x = 1 gives y = K exactly (times the w8 scale) in every kernel family
     xk = P.xkind(dtype)
     for kernel, param, B in (("auto", 0, 2), ("warp_per_row", 0, 2), ("block_per_row", 0, 2),
-                             ("split_k", 5, 2), ("batched", 2, 2), ("batched", 2, 12), ("scalar", 32, 2),
+                             ("split_k", 5, 2), ("batched", 2, 2), ("batched", 2, 12), ("batched", 1, 2),
+                             ("batched", 1, 12), ("batched", 3, 12), ("scalar", 32, 2),
                              ("stream", 0, 1), ("xsplit", 0, 2), ("xsplit", 0, 4)):
         M, K = 96, 4096
         A = torch.ones(M, K, dtype=torch.int8 if dtype == "w8" else U.out_dtype(dtype))

@@ -255,7 +255,19 @@ W4_CONFIGS: list[Workload] = [
     Workload("w4_8192x8192_b4_bias", "w4", 8192, 8192, 4, True, ("bytes",), ("normal", 1.0)),
     Workload("w4_14336x4096_b1", "w4", 14336, 4096, 1, False, ("bytes",), ("normal", 1.0)),
 ]
-BY_NAME = {w.name: w for w in CONFIGS + W4_CONFIGS}
+# More than 16 vectors (fp16/bf16 only): the tensor-core crossover, on the fp16
+# 4096x4096 and bf16 decode shapes of the configurations.
+TC_CONFIGS: list[Workload] = [
+    Workload("f16_4096x4096_b32", "f16", 4096, 4096, 32, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("f16_4096x4096_b64", "f16", 4096, 4096, 64, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("f16_4096x4096_b256", "f16", 4096, 4096, 256, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("bf16_14336x4096_b32", "bf16", 14336, 4096, 32, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("bf16_14336x4096_b128", "bf16", 14336, 4096, 128, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("bf16_4096x14336_b64", "bf16", 4096, 14336, 64, False, ("normal", 0.02), ("normal", 1.0)),
+    Workload("bf16_128256x4096_b64", "bf16", 128256, 4096, 64, False, ("normal", 0.02), ("normal", 1.0)),
+]
+
+BY_NAME = {w.name: w for w in CONFIGS + W4_CONFIGS + TC_CONFIGS}
 
 # The fp32 sweep over K at M = 16384 with bias: the benchmark's headline workload
 # (one step = the three GEMVs back to back).
