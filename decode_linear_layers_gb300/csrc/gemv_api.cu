@@ -150,7 +150,8 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
     const int param = B > 1 && g_force_kernel == GEMV_KERNEL_BATCHED ? g_force_param : 0;
     st = gemv::plan(dtype, M, K, B, al16, sms, want, param, &p);
     if (st != GEMV_SUCCESS) return st;
-    if (p.kernel != want) return GEMV_ERR_UNSUPPORTED;
+    // (a K-split plan sums slices in a second pass, which knows no row pairs)
+    if (p.kernel != want || p.splits > 1) return GEMV_ERR_UNSUPPORTED;
   } else {
     st = gemv::plan(dtype, M, K, B, al16, sms, g_force_kernel, g_force_param, &p);
     if (st != GEMV_SUCCESS) return st;
@@ -184,7 +185,7 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
                  : dtype == GEMV_DTYPE_W8   ? gemv::launch_w8
                                             : gemv::launch_w4;
   float *ws = nullptr;
-  if (p.kernel == GEMV_KERNEL_SPLIT_K || (p.kernel == GEMV_KERNEL_TC && p.workspace_bytes > 0)) {
+  if (p.workspace_bytes > 0) {  // split-K partial sums: SPLIT_K, TC or BATCHED over K slices
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), (size_t)p.workspace_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
@@ -195,7 +196,8 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
     if (e == cudaSuccess) e = e2;
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  const bool two = p.kernel == GEMV_KERNEL_SPLIT_K || (p.kernel == GEMV_KERNEL_TC && p.splits > 1);
+  const bool two = p.kernel == GEMV_KERNEL_SPLIT_K || (p.kernel == GEMV_KERNEL_TC && p.splits > 1) ||
+                   (p.kernel == GEMV_KERNEL_BATCHED && p.splits > 1);
   g_launches.fetch_add(two ? 2 : 1, std::memory_order_relaxed);
   t_last_plan = p;
   t_have_plan = true;

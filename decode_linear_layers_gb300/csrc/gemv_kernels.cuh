@@ -1077,7 +1077,8 @@ constexpr int kRingMixed = 2;    // one fp32 accumulator per (row, vector), 16-b
 
 template <class Op, int NB, int R, int G, int XE, bool SW, int MODE = (NB >= 8 ? kRingPairs : kRingEvenOdd),
           int THREADS = 512>
-__global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
+__global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *partial,
+                                                           int64_t chunks_per_split) {
   constexpr int WARPS = THREADS / 32;
   constexpr bool PAIRS = MODE == kRingPairs;
   static_assert(MODE != kRingMixed || (XE == 2 && Op::VEC == 8), "mixed FMAs take 16-bit A and x");
@@ -1099,11 +1100,16 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t M = a.M, K = a.K;
   const int B = a.B;
-  const int64_t nch = K / Op::VEC;
-  if (nch == 0) return;  // K = 0 never reaches this kernel
+  // K slice blockIdx.y: chunks c0 .. c0 + nch - 1 of every row (all of K when the
+  // grid has one slice); its sums go to partial[slice][b][m] for k_splitk_reduce
+  const int64_t c0 = (int64_t)blockIdx.y * chunks_per_split;
+  const int64_t nch_all = K / Op::VEC;
+  const int64_t nch = nch_all - c0 < chunks_per_split ? nch_all - c0 : chunks_per_split;
+  if (nch <= 0) return;  // K = 0 never reaches this kernel; the plan has no empty slice
   const int64_t nsteps = (nch + 31) / 32;
   const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
-  const char *A = reinterpret_cast<const char *>(a.A);
+  const char *A = reinterpret_cast<const char *>(a.A) + c0 * 16;
+  const int64_t k0 = c0 * Op::VEC;  // first element of the slice
   const int64_t groups = SW ? a.half : (M + R - 1) / R;
   auto row_of = [&](int64_t gg, int r) -> int64_t { return SW ? gg + r * a.half : gg * R + r; };
   const int64_t gstride = (int64_t)gridDim.x * WARPS;
@@ -1138,8 +1144,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
   // into place, one commit group issued before A's first steps.  Interleaved or
   // widened: eight items (quads of one vector or of a vector pair) per thread in
   // flight through registers at a time.
-  const unsigned char *xsrc = reinterpret_cast<const unsigned char *>(a.x);
-  const int64_t nq = K / 4;  // quads per vector
+  const unsigned char *xsrc = reinterpret_cast<const unsigned char *>(a.x) + k0 * SX;
+  const int64_t nq = nch * Op::VEC / 4;  // quads per vector in the slice
   constexpr bool XCOPY = !PAIRS && XE == SX;
   if constexpr (XCOPY) {
     for (int64_t i = tid; i < (int64_t)B * nq; i += THREADS) {
@@ -1238,8 +1244,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
     const int er = idx / NB, eb = idx % NB;
     const int64_t erow = row_of(g, er);
     const bool live = owner && eb < B && erow < M && !SW;
-    RowPre pre = row_pre<Op, false>(a, erow, live);
-    if (live && a.residual != nullptr) pre.res = residual_at<Op>(a.residual, (int64_t)eb * M + erow);
+    RowPre pre = row_pre<Op, false>(a, erow, live && partial == nullptr);
+    if (live && partial == nullptr && a.residual != nullptr)
+      pre.res = residual_at<Op>(a.residual, (int64_t)eb * M + erow);
 
     constexpr int NA = PAIRS ? NP : NB;  // accumulator pairs per row
     float2 acc[R][NA];
@@ -1352,6 +1359,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a) {
       // gate sum b sits at lane b * 32 / V, its up sum 16 lanes above
       const float up = __shfl_down_sync(0xffffffffu, part, 16);
       if (owner && idx < NB && idx < B) epilogue_swiglu<Op>(a, idx, g, part, up);
+    } else if (partial != nullptr) {
+      if (live) partial[((int64_t)blockIdx.y * B + eb) * M + erow] = part;
     } else {
       if (live) store_act_res<Op>(a, (int64_t)eb * M + erow, row_value_pre<Op>(a, pre, part), pre.res);
     }

@@ -42,39 +42,57 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
 }
 
 template <class Op, int NB>
-cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
+cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
   if constexpr (Op::GROUPED || NB < 2) {
     return cudaErrorInvalidValue;  // not built for int4 or one vector; the planner never picks it
   } else {
-    const dim3 grid((unsigned)p.grid), block(kBatchedThreads);
-    auto run = [&](auto kern) -> cudaError_t {
-      cudaError_t e = allow_smem(kern, p.smem_bytes);
-      if (e != cudaSuccess) return e;
-      kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
-      return cudaSuccess;
-    };
     constexpr int T = kBatchedThreads;
     static_assert(T == 512, "the ring kernel is built for 512 threads");
+    const dim3 block(T);
     const bool sw = a.half > 0;  // SwiGLU: gate and up row of one output per row pair
+    if (p.splits < 1 || (p.splits > 1 && (ws == nullptr || sw || p.variant == GEMV_BATCHED_ROWPAIR)))
+      return cudaErrorInvalidValue;
+    // the ring over K slice blockIdx.y (p.splits slices of chunks_per_split chunks),
+    // then with several slices the fixed-order sum of the slices and the epilogue
+    const int64_t nch = a.K / Op::VEC;
+    const int64_t cps = (nch + p.splits - 1) / p.splits;
+    auto ring = [&](auto kern) -> cudaError_t {
+      cudaError_t e = allow_smem(kern, p.smem_bytes);
+      if (e != cudaSuccess) return e;
+      kern<<<dim3((unsigned)p.grid, (unsigned)p.splits), block, (size_t)p.smem_bytes, s>>>(
+          a, p.splits > 1 ? ws : nullptr, cps);
+      e = cudaGetLastError();
+      if (e != cudaSuccess || p.splits == 1) return e;
+      const int64_t total = a.M * a.B;
+      int64_t g = (total + kThreads - 1) / kThreads;
+      if (g > 65535) g = 65535;
+      k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
+      return cudaSuccess;
+    };
     constexpr int SX = (int)sizeof(typename Op::TX);
     constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
     switch (p.variant) {
-      case GEMV_BATCHED_ROWPAIR:
-        return sw ? run(k_batched2<Op, NB, 2, 2, T, true>) : run(k_batched2<Op, NB, 2, 2, T>);
+      case GEMV_BATCHED_ROWPAIR: {
+        auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
+        cudaError_t e = allow_smem(kern, p.smem_bytes);
+        if (e != cudaSuccess) return e;
+        kern<<<dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s>>>(a);
+        return cudaSuccess;
+      }
       case GEMV_BATCHED_RING: {
         constexpr int R = ring_rows(NB), G = 8 / R;
         constexpr int MODE = NB >= 8 ? kRingPairs : kRingEvenOdd;
         const bool x32 = p.x_staging == GEMV_X_SMEM_FP32 || SX == 4;
         if (!sw && p.rows_per_warp != R) return cudaErrorInvalidValue;
         if (sw)
-          return x32 ? run(k_batch_ring<Op, NB, 2, 4, 4, true, MODE>) : run(k_batch_ring<Op, NB, 2, 4, SX, true, MODE>);
-        return x32 ? run(k_batch_ring<Op, NB, R, G, 4, false, MODE>) : run(k_batch_ring<Op, NB, R, G, SX, false, MODE>);
+          return x32 ? ring(k_batch_ring<Op, NB, 2, 4, 4, true, MODE>) : ring(k_batch_ring<Op, NB, 2, 4, SX, true, MODE>);
+        return x32 ? ring(k_batch_ring<Op, NB, R, G, 4, false, MODE>) : ring(k_batch_ring<Op, NB, R, G, SX, false, MODE>);
       }
       case GEMV_BATCHED_RING_MIXED:
         if constexpr (A16 && SX == 2 && Op::VEC == 8) {
           if (p.rows_per_warp != 2 || p.x_staging != GEMV_X_SMEM) return cudaErrorInvalidValue;
-          return sw ? run(k_batch_ring<Op, NB, 2, 4, 2, true, kRingMixed>)
-                    : run(k_batch_ring<Op, NB, 2, 4, 2, false, kRingMixed>);
+          return sw ? ring(k_batch_ring<Op, NB, 2, 4, 2, true, kRingMixed>)
+                    : ring(k_batch_ring<Op, NB, 2, 4, 2, false, kRingMixed>);
         }
         return cudaErrorInvalidValue;
       default:
@@ -150,7 +168,7 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
       return cudaSuccess;
     }
     case GEMV_KERNEL_BATCHED:
-      return launch_batched<Op, NB>(p, a, s);
+      return launch_batched<Op, NB>(p, a, ws, s);
     case GEMV_KERNEL_STREAM:
       if constexpr (NB == 1) return launch_stream<Op>(p, a, s);
       return cudaErrorInvalidValue;

@@ -14,9 +14,10 @@
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
 //   fp32, B == 2, x slice fits 64 registers, at least 16 rows per SM and
 //     M < 65536                           -> XSPLIT (K split over a CTA)
-//   B >= 2 and x[0..B) fits in smem       -> BATCHED: fp16/bf16 with 9..16
-//     vectors and at most one row pair per warp -> ROWPAIR, otherwise the
-//     cp.async ring (mixed-precision FMAs for fp16/bf16 with 9..16 vectors)
+//   B >= 2 (not int4)                     -> BATCHED: 4..16 vectors and at most
+//     one row pair per warp -> ROWPAIR, otherwise the cp.async ring (mixed-
+//     precision FMAs for fp16/bf16 with 2 or 9..16 vectors), over K slices with a
+//     second pass when x[0..B) does not fit in shared memory whole
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
 //   B == 1 and at least 16 rows per SM    -> STREAM (persistent warps)
 //   at least 16 rows per SM, or <= 4 KB   -> WARP_PER_ROW
@@ -76,6 +77,16 @@ static int ring_staging(int nb, int64_t K, int sx) {
   return -1;
 }
 
+// K slices of the ring kernel: 1 when x[0..NB) fits with the ring, else the fewest
+// slices (at most 64) whose share of x fits as stored; 0 if none does.
+static int ring_slices(int nb, int64_t nch, int vec, int sx) {
+  for (int s = 1; s <= 64; ++s) {
+    const int64_t cps = (nch + s - 1) / s;
+    if (ring_staging(nb, cps * vec, sx) >= 0) return s;
+  }
+  return 0;
+}
+
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out) {
   if (out == nullptr || num_sms < 1) return GEMV_ERR_INVALID_VALUE;
@@ -101,9 +112,13 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   const bool tc_ok = half16 && vec_ok;
   // the batched shared-memory kernels are not built for int4 (grouped scales)
   // the batched kernels are not built for int4 (grouped scales)
-  const int rstage = dtype == GEMV_DTYPE_W4 ? -1 : ring_staging(p.nb, K, sx);
+  // the ring kernel over rslices K slices (x staged per slice), the row-pair kernel
+  // over all of K
+  const int rslices = dtype == GEMV_DTYPE_W4 || nch == 0 ? 0 : ring_slices(p.nb, nch, vec, sx);
+  const int64_t rcps = rslices > 0 ? ceil_div(nch, rslices) : 0;  // chunks per slice
+  const int rstage = rslices > 0 ? ring_staging(p.nb, rcps * vec, sx) : -1;
   const bool rowpair_ok = dtype != GEMV_DTYPE_W4 && rowpair_fits(p.nb, K, sx);
-  const bool mixed_ok = half16 && (int64_t)p.nb * K * 2 + kRingBytes <= kRingSmemMax;
+  const bool mixed_ok = half16 && rstage >= 0;  // x as stored fits wherever fp32 x does
   const bool batched_ok = rstage >= 0 || rowpair_ok;
   // XSPLIT: chunks per thread J (a power of two up to 4) and x registers
   const int xs_j = vec_ok && nch > 0 ? next_pow2(ceil_div(nch, kXsplitThreads)) : 0;
@@ -243,7 +258,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       int v;
       if (param != 0) {
         v = param - 1;
-      } else if (rstage < 0 || (rowpair_ok && p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2)) {
+      } else if (rstage < 0 || (rowpair_ok && (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2)))) {
         v = GEMV_BATCHED_ROWPAIR;
       } else {
         v = (half16 && (p.nb == 16 || p.nb == 2) && mixed_ok) ? GEMV_BATCHED_RING_MIXED : GEMV_BATCHED_RING;
@@ -255,12 +270,17 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         p.unroll = 2;
         p.smem_bytes = (int)((int64_t)p.nb * K * sx);
       } else {
-        // ring: R rows per warp, a G = 8 / R step ring; the mixed form reads x as stored
+        // ring: R rows per warp, a G = 8 / R step ring; the mixed form reads x as
+        // stored.  Over rslices K slices (x too large to stage whole): grid.x CTAs per
+        // slice, one CTA per SM in all, partial sums [slice][b][m], then a second pass.
         const int xs = v == GEMV_BATCHED_RING_MIXED ? GEMV_X_SMEM : rstage;
         p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb);
         p.x_staging = xs;
         p.unroll = 8 / p.rows_per_warp;
-        p.smem_bytes = (int)((int64_t)p.nb * K * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes);
+        p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes);
+        p.splits = rslices;
+        p.grid = num_sms / rslices > 0 ? num_sms / rslices : 1;
+        p.workspace_bytes = rslices > 1 ? (int64_t)rslices * B * M * 4 : 0;
       }
       break;
     }

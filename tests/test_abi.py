@@ -216,6 +216,20 @@ def test_plan_batched_staging():
     # x too large for the ring but within 200 KB: the row-pair kernel
     p = g.plan_for("bf16", 20000, 6144, 16)
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 6144 * 2
+    # x too large to stage whole (and for the row-pair kernel): the ring over K
+    # slices, one CTA per SM in all, partial sums [slice][b][m] and a second pass
+    p = g.plan_for("w8", 8192, 8192, 16)
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["splits"] == 2
+    assert p["x_staging"] == 1 and p["smem_bytes"] == 16 * 4096 * 2 + ring and p["grid"] == 76
+    assert p["workspace_bytes"] == 2 * 16 * 8192 * 4
+    p = g.plan_for("bf16", 4096, 14336, 16)   # 1792 chunks in 3 slices of 598
+    assert p["variant"] == g.BATCHED_RING_MIXED and p["splits"] == 3 and p["grid"] == 50
+    assert p["smem_bytes"] == 16 * 598 * 8 * 2 + ring and p["workspace_bytes"] == 3 * 16 * 4096 * 4
+    p = g.plan_for("bf16", 4096, 14336, 8)    # 8 x 14336 bf16 (229 KB): two slices
+    assert p["variant"] == g.BATCHED_RING and p["splits"] == 2 and p["x_staging"] == 1
+    assert p["smem_bytes"] == 8 * 7168 * 2 + ring
+    p = g.plan_for("bf16", 4096, 14336, 4)    # the row-pair kernel's x fits (115 KB)
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["splits"] == 1
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
     assert g.plan_for("w8", 8192, 4096, 3)["smem_bytes"] == 4 * 4096 * 4 + ring
     assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
@@ -254,8 +268,11 @@ def test_plan_few_rows_long_k():
 
 
 def test_plan_batch_too_big_for_smem():
-    # 16 vectors of 16384 bf16 = 512 KB of x: not staged, warp per row instead
+    # 16 vectors of 16384 bf16 = 512 KB of x: staged in 4 K slices of 128 KB
     p = g.plan_for("bf16", 8192, 16384, 16)
+    assert p["kernel"] == g.KERNELS["batched"] and p["nb"] == 16 and p["splits"] == 4 and p["grid"] == 38
+    # beyond 64 slices (x of more than ~10 MB): warp per row, x through L1
+    p = g.plan_for("bf16", 8192, 1 << 20, 16)
     assert p["kernel"] == g.KERNELS["warp_per_row"] and p["nb"] == 16
 
 

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import decode_linear_layers_gb300 as g
+import oracle
 import workloads as W
 from tests import gpu_util as U
 from tests import oracle_pins as P
@@ -75,10 +76,13 @@ def forced_feasible(dtype, kernel, param, K, B):
     nb = 1 << (B - 1).bit_length()
     if kernel == "batched":
         # param = variant + 1: 1 the row-pair kernel (x as stored in 200 KB), 2 the
-        # cp.async ring (x and a 64 KB ring in 227 KB), 3 the mixed-precision ring
-        ring = (sx != 4 and nb * K * 4 + 65536 <= 227 * 1024) or nb * K * sx + 65536 <= 227 * 1024
+        # cp.async ring (x, or its share of one of at most 64 K slices, as stored
+        # next to a 64 KB ring in 227 KB), 3 the mixed-precision ring
+        vec = {"f32": 4, "f16": 8, "bf16": 8, "w8": 16}[dtype]
+        nch = K // vec
+        ring = any(nb * (-(-nch // s)) * vec * sx + 65536 <= 227 * 1024 for s in range(1, 65))
         rowpair = nb * K * sx <= 200 * 1024
-        mixed = dtype in ("f16", "bf16") and nb * K * 2 + 65536 <= 227 * 1024
+        mixed = dtype in ("f16", "bf16") and ring
         ok = {0: ring or rowpair, 1: rowpair, 2: ring, 3: mixed}.get(param, False)
         return B >= 2 and ok
     if kernel == "split_k":
@@ -116,6 +120,43 @@ def test_forced_kernel(dtype, kernel, param):
                     assert plan["variant"] == param - 1, (plan, param)
             U.assert_close(dtype, y, y_ref, absdot, with_rounding=True,
                            what=f"{dtype} {kernel}/{param} M={M} K={K} B={B} bias={bias}")
+
+
+@pytest.mark.parametrize("dtype,M,K,B", [("bf16", 4096, 14336, 16), ("w8", 8192, 8192, 16),
+                                         ("f16", 3000, 14336, 9), ("bf16", 2500, 30000, 5),
+                                         ("f32", 1000, 20000, 12)])
+def test_batched_k_slices(dtype, M, K, B):
+    # x[0..B) too large to stage whole: the ring over K slices, partial sums and a
+    # fixed-order second pass (sampled rows against the oracle, with bias; repeats
+    # bitwise equal; the fused epilogue through the second pass)
+    if dtype == "w8":
+        K -= K % 16
+    w = W.small(dtype, M, K, B, True, seed=M + K)
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    y1 = U.run_gpu(dtype, d, M, K, B)
+    plan = g.last_plan()
+    assert plan["kernel_name"] == "batched" and plan["splits"] > 1, plan
+    y2 = U.run_gpu(dtype, d, M, K, B)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "results differ between two identical calls"
+    rows = np.sort(np.random.default_rng(1).choice(M, size=min(M, 160), replace=False))
+    sub = {"A": inp["A"][rows], "x": inp["x"], "bias": inp["bias"][rows],
+           "scale": None if inp["scale"] is None else inp["scale"][rows]}
+    y_ref, absdot = U.oracle_for(dtype, sub)
+    U.assert_close(dtype, y1[:, rows], y_ref, absdot, with_rounding=True,
+                   what=f"{dtype} {M}x{K} B={B} splits={plan['splits']} variant={plan['variant']}")
+    # SiLU and an in-place residual, applied by the second pass
+    xdt = U.out_dtype(dtype)
+    r = (torch.randn(B, M, generator=torch.Generator().manual_seed(7)) * 2).to(xdt)
+    sub_r = r[:, rows].contiguous()
+    y_ref2, _, absdot2 = oracle.gemv_ex(dtype, W.storage_bits(sub["A"]), W.storage_bits(sub["x"]),
+                                        W.storage_bits(sub["bias"]), None if sub["scale"] is None else sub["scale"].numpy(),
+                                        residual=W.storage_bits(sub_r), act=1, nthreads=U.threads())
+    y = r.cuda()
+    g.gemv_ex(dtype, d["A"], d["scale"], d["x"], d["bias"], y, y, M, K, B, 1)
+    assert g.last_plan()["splits"] > 1
+    U.assert_close_ex(dtype, y[:, rows], y_ref2, absdot2, 1, what=f"{dtype} {M}x{K} B={B} k-slices silu+res")
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
