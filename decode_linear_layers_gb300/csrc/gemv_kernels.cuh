@@ -396,6 +396,20 @@ struct OpW4 {
     e = acc.x;
     o = acc.y;
   }
+  // elements 4w .. 4w+3 of a chunk as two fp32 pairs (unscaled): word w / 2, bytes
+  // 2 (w % 2) and 2 (w % 2) + 1, low nibble first
+  __device__ static __forceinline__ void quad2(const uint4 &a, int w, float2 &q01, float2 &q23) {
+    const int j = w >> 1;
+    const uint32_t word = j == 0 ? a.x : j == 1 ? a.y : j == 2 ? a.z : a.w;
+    const uint32_t f = word ^ 0x88888888u;
+    const uint32_t lo = f & 0x0F0F0F0Fu, hi = (f >> 4) & 0x0F0F0F0Fu;
+    const uint32_t b0 = (uint32_t)(w & 1) * 2;
+    const float2 mg = make_float2(-8388616.0f, -8388616.0f);
+    q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540 + b0)),
+                                 __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540 + b0))), mg);
+    q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541 + b0)),
+                                 __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7541 + b0))), mg);
+  }
   // element k of the row starting at byte `row` (unscaled)
   __device__ static __forceinline__ float nibble(const void *A, int64_t row_byte, int64_t k) {
     const uint32_t b = __ldg(reinterpret_cast<const unsigned char *>(A) + row_byte + (k >> 1));
@@ -1107,7 +1121,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   const int64_t nch = nch_all - c0 < chunks_per_split ? nch_all - c0 : chunks_per_split;
   if (nch <= 0) return;  // K = 0 never reaches this kernel; the plan has no empty slice
   const int64_t nsteps = (nch + 31) / 32;
-  const int64_t rowb = K * (int64_t)sizeof(typename Op::TA);
+  const int64_t rowb = row_bytes<Op>(K);
   const char *A = reinterpret_cast<const char *>(a.A) + c0 * 16;
   const int64_t k0 = c0 * Op::VEC;  // first element of the slice
   const int64_t groups = SW ? a.half : (M + R - 1) / R;
@@ -1119,6 +1133,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   const int64_t xbytes = (int64_t)(PAIRS ? NP : NB) * PPV * pstride;
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t ring_s = xs_s + (uint32_t)xbytes + (uint32_t)((warp * G * R * 32 + lane) * 16);
+  // int4: each slot's group scale, in a second ring [warp][stage][row][lane] of floats
+  constexpr bool GRP = Op::GROUPED;
+  const uint32_t sc_s = xs_s + (uint32_t)xbytes + (uint32_t)(WARPS * G * R * 32 * 16) +
+                        (uint32_t)((warp * G * R * 32 + lane) * 4);
+  const int64_t gpr = K >> a.gshift;  // groups per row (int4)
 
   // producer position: row group pg, step pj (chunks 32 pj + lane)
   int64_t pg = blockIdx.x + (int64_t)gridDim.x * warp, pj = 0;
@@ -1133,6 +1152,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
             const uint32_t dst = ring_s + (uint32_t)((stage * R + r) * 32 * 16);
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(A + row * rowb + c * 16)
                          : "memory");
+            if constexpr (GRP) {
+              const float *gs = a.gscale + row * gpr + (((c0 + c) * Op::VEC) >> a.gshift);
+              asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sc_s + (uint32_t)((stage * R + r) * 32 * 4)),
+                           "l"(gs) : "memory");
+            }
           }
         }
       }
@@ -1263,6 +1287,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
       uint4 av[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) av[r] = lds16(ring_s + (uint32_t)((stage * R + r) * 32 * 16));
+      float gsc[GRP ? R : 1];
+      if constexpr (GRP) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(gsc[r]) : "r"(sc_s + (uint32_t)((stage * R + r) * 32 * 4)));
+      }
       issue(stage);  // this lane's slots of the stage are free again
       stage = stage + 1 == G ? 0 : stage + 1;
       const int64_t c = 32 * j + lane;
@@ -1294,7 +1324,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
         }
         float2 q01[R], q23[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) Op::quad2(av[r], w, q01[r], q23[r]);
+        for (int r = 0; r < R; ++r) {
+          Op::quad2(av[r], w, q01[r], q23[r]);
+          if constexpr (GRP) {  // int4: the chunk's group scale, applied to the weights
+            q01[r] = __fmul2_rn(q01[r], make_float2(gsc[r], gsc[r]));
+            q23[r] = __fmul2_rn(q23[r], make_float2(gsc[r], gsc[r]));
+          }
+        }
         if constexpr (PAIRS) {
 #pragma unroll
           for (int p = 0; p < NP; ++p) {

@@ -43,8 +43,8 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
 
 template <class Op, int NB>
 cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
-  if constexpr (Op::GROUPED || NB < 2) {
-    return cudaErrorInvalidValue;  // not built for int4 or one vector; the planner never picks it
+  if constexpr (NB < 2) {
+    return cudaErrorInvalidValue;  // not built for one vector; the planner never picks it
   } else {
     constexpr int T = kBatchedThreads;
     static_assert(T == 512, "the ring kernel is built for 512 threads");
@@ -72,15 +72,17 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
     constexpr int SX = (int)sizeof(typename Op::TX);
     constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
     switch (p.variant) {
-      case GEMV_BATCHED_ROWPAIR: {
-        auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
-        cudaError_t e = allow_smem(kern, p.smem_bytes);
-        if (e != cudaSuccess) return e;
-        kern<<<dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s>>>(a);
-        return cudaSuccess;
-      }
+      case GEMV_BATCHED_ROWPAIR:
+        if constexpr (!Op::GROUPED) {  // not built for int4's group scales
+          auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
+          cudaError_t e = allow_smem(kern, p.smem_bytes);
+          if (e != cudaSuccess) return e;
+          kern<<<dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s>>>(a);
+          return cudaSuccess;
+        }
+        return cudaErrorInvalidValue;
       case GEMV_BATCHED_RING: {
-        constexpr int R = ring_rows(NB), G = 8 / R;
+        constexpr int R = ring_rows(NB, Op::GROUPED), G = 8 / R;
         constexpr int MODE = NB >= 8 ? kRingPairs : kRingEvenOdd;
         const bool x32 = p.x_staging == GEMV_X_SMEM_FP32 || SX == 4;
         if (!sw && p.rows_per_warp != R) return cudaErrorInvalidValue;

@@ -14,7 +14,7 @@
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
 //   fp32, B == 2, x slice fits 64 registers, at least 16 rows per SM and
 //     M < 65536                           -> XSPLIT (K split over a CTA)
-//   B >= 2 (not int4)                     -> BATCHED: 4..16 vectors and at most
+//   B >= 2                                -> BATCHED: 4..16 vectors and at most
 //     one row pair per warp -> ROWPAIR, otherwise the cp.async ring (mixed-
 //     precision FMAs for fp16/bf16 with 2 or 9..16 vectors), over K slices with a
 //     second pass when x[0..B) does not fit in shared memory whole
@@ -71,18 +71,19 @@ static bool rowpair_fits(int nb, int64_t K, int sx) { return (int64_t)nb * K * s
 
 // x staging of the BATCHED ring kernel: fp32 where x and the ring fit, else as
 // stored; -1 if x does not fit.
-static int ring_staging(int nb, int64_t K, int sx) {
-  if (sx != 4 && (int64_t)nb * K * 4 + kRingBytes <= kRingSmemMax) return GEMV_X_SMEM_FP32;
-  if ((int64_t)nb * K * sx + kRingBytes <= kRingSmemMax) return GEMV_X_SMEM;
+static int ring_staging(int nb, int64_t K, int sx, int64_t extra) {
+  const int64_t room = kRingSmemMax - kRingBytes - extra;
+  if (sx != 4 && (int64_t)nb * K * 4 <= room) return GEMV_X_SMEM_FP32;
+  if ((int64_t)nb * K * sx <= room) return GEMV_X_SMEM;
   return -1;
 }
 
 // K slices of the ring kernel: 1 when x[0..NB) fits with the ring, else the fewest
 // slices (at most 64) whose share of x fits as stored; 0 if none does.
-static int ring_slices(int nb, int64_t nch, int vec, int sx) {
+static int ring_slices(int nb, int64_t nch, int vec, int sx, int64_t extra) {
   for (int s = 1; s <= 64; ++s) {
     const int64_t cps = (nch + s - 1) / s;
-    if (ring_staging(nb, cps * vec, sx) >= 0) return s;
+    if (ring_staging(nb, cps * vec, sx, extra) >= 0) return s;
   }
   return 0;
 }
@@ -114,9 +115,12 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   // the batched kernels are not built for int4 (grouped scales)
   // the ring kernel over rslices K slices (x staged per slice), the row-pair kernel
   // over all of K
-  const int rslices = dtype == GEMV_DTYPE_W4 || nch == 0 ? 0 : ring_slices(p.nb, nch, vec, sx);
+  // (int4: the ring also carries each slot's group scale; the row-pair kernel is not
+  // built for grouped scales)
+  const int64_t rextra = dtype == GEMV_DTYPE_W4 ? kRingScaleBytes : 0;
+  const int rslices = nch == 0 ? 0 : ring_slices(p.nb, nch, vec, sx, rextra);
   const int64_t rcps = rslices > 0 ? ceil_div(nch, rslices) : 0;  // chunks per slice
-  const int rstage = rslices > 0 ? ring_staging(p.nb, rcps * vec, sx) : -1;
+  const int rstage = rslices > 0 ? ring_staging(p.nb, rcps * vec, sx, rextra) : -1;
   const bool rowpair_ok = dtype != GEMV_DTYPE_W4 && rowpair_fits(p.nb, K, sx);
   const bool mixed_ok = half16 && rstage >= 0;  // x as stored fits wherever fp32 x does
   const bool batched_ok = rstage >= 0 || rowpair_ok;
@@ -274,10 +278,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         // stored.  Over rslices K slices (x too large to stage whole): grid.x CTAs per
         // slice, one CTA per SM in all, partial sums [slice][b][m], then a second pass.
         const int xs = v == GEMV_BATCHED_RING_MIXED ? GEMV_X_SMEM : rstage;
-        p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb);
+        p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb, dtype == GEMV_DTYPE_W4);
         p.x_staging = xs;
         p.unroll = 8 / p.rows_per_warp;
-        p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes);
+        p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes + rextra);
         p.splits = rslices;
         p.grid = num_sms / rslices > 0 ? num_sms / rslices : 1;
         p.workspace_bytes = rslices > 1 ? (int64_t)rslices * B * M * 4 : 0;

@@ -18,10 +18,12 @@ constexpr int64_t kStreamSmemMax = 96 * 1024;
 constexpr int kBatchedThreads = 512;
 // BATCHED ring kernel: R rows per warp and a per-thread cp.async ring of G = 8 / R
 // steps: 16 warps x 8 slots x 512 bytes after x.  R = 2 for 16 vectors (the
-// accumulators' registers), else 4.  SwiGLU: R = 2.
+// accumulators' registers) and for int4 (32 weights per chunk to decode), else 4.
+// SwiGLU: R = 2.
 constexpr int64_t kRingSmemMax = 227 * 1024;  // dynamic shared memory one CTA may use
 constexpr int64_t kRingBytes = 16 * 8 * 512;
-constexpr int ring_rows(int nb) { return nb == 16 ? 2 : 4; }
+constexpr int64_t kRingScaleBytes = 16 * 8 * 32 * 4;  // int4: a group scale per slot
+constexpr int ring_rows(int nb, bool grouped) { return (nb == 16 || grouped) ? 2 : 4; }
 constexpr int kStreamThreads = 512;
 // 16-byte chunks in flight per lane: warp-per-row and block-per-row kernels.
 constexpr int kUnrollWarpRow = 4;

@@ -233,8 +233,10 @@ def test_plan_batched_staging():
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
     assert g.plan_for("w8", 8192, 4096, 3)["smem_bytes"] == 4 * 4096 * 4 + ring
     assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
-    # int4 has no batched kernel
-    assert g.plan_for("w4", 8192, 8192, 4)["kernel"] != K["batched"]
+    # int4: the ring with a group-scale ring (16 KB) beside it, 2 rows per warp
+    p = g.plan_for("w4", 8192, 8192, 4)
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 2
+    assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + ring + 16 * 1024
 
 
 def test_plan_small_k_lanes():
@@ -314,8 +316,9 @@ def test_plan_w4():
     K = g.KERNELS
     p = g.plan_for("w4", 8192, 8192, 1)
     assert p["kernel"] == K["stream"] and p["x_staging"] == 1 and p["smem_bytes"] == 8192 * 2
-    for B in (2, 4, 9, 16):  # no batched shared-memory kernel for int4
-        assert g.plan_for("w4", 8192, 8192, B)["kernel"] == K["warp_per_row"]
+    for B, slices in ((2, 1), (4, 1), (9, 2), (16, 2)):  # the batched ring kernel
+        p = g.plan_for("w4", 8192, 8192, B)
+        assert p["kernel"] == K["batched"] and p["splits"] == slices, (B, p)
     # 32 weights per 16-byte chunk: K = 256 is 8 chunks -> 8 lanes per row
     p = g.plan_for("w4", 1000, 256, 1)
     assert p["kernel"] == K["rows_per_warp"] and p["lanes_per_row"] == 8

@@ -7,7 +7,7 @@
 * edges: K = 0, K not a multiple of the group (rejected), rows not 16-byte aligned
   (element-load kernel), guard bytes around y, closed forms;
 * the fused epilogues: gemv_ex with SiLU and an in-place residual, SwiGLU with one
-  vector (and its refusal for more).
+  and with three vectors.
 """
 from __future__ import annotations
 
@@ -50,7 +50,7 @@ def test_w4_config_full_size(name):
 
 SHAPES = [(1, 128), (37, 256), (300, 384), (1001, 1024), (77, 4224), (5, 20096)]
 FORCED = [("rows_per_warp", 0), ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0),
-          ("split_k", 3), ("scalar", 4), ("scalar", 32), ("stream", 0), ("auto", 0)]
+          ("split_k", 3), ("scalar", 4), ("scalar", 32), ("stream", 0), ("batched", 2), ("auto", 0)]
 
 
 @pytest.mark.parametrize("kernel,param", FORCED)
@@ -70,9 +70,8 @@ def test_w4_forced_kernel(kernel, param):
             y = U.run_gpu("w4", d, M, K, B)
             plan = g.last_plan()
             g.force_kernel("auto")
-            if kernel not in ("auto",) and not (kernel == "stream" and B > 1):
+            if kernel not in ("auto",) and not (kernel == "stream" and B > 1) and not (kernel == "batched" and B == 1):
                 assert plan["kernel_name"] == kernel, (plan, kernel)
-            assert plan["kernel_name"] != "batched"
             U.assert_close("w4", y, y_ref, absdot, with_rounding=True,
                            what=f"w4 {kernel}/{param} M={M} K={K} B={B} bias={bias}")
 
@@ -125,7 +124,8 @@ def test_w4_k_zero_and_bad_k():
 
 def test_w4_guard_bytes_untouched():
     for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("block_per_row", 0, 4), ("scalar", 32, 4),
-                             ("stream", 0, 1), ("warp_per_row", 0, 3), ("rows_per_warp", 2, 4)):
+                             ("stream", 0, 1), ("warp_per_row", 0, 3), ("rows_per_warp", 2, 4), ("batched", 2, 9),
+                             ("batched", 2, 3)):
         M, K = 333, 256
         w = W.small("w4", M, K, B, False, seed=400)
         d = U.to_device(W.make_inputs(w))
@@ -148,7 +148,7 @@ def test_w4_closed_forms():
     for byte, qv in ((0x11, 1), (0x88, -8), (0x77, 7)):
         A = torch.full((M, K // 2), byte, dtype=torch.uint8, device="cuda")
         for kernel, param, b in (("auto", 0, B), ("warp_per_row", 0, B), ("block_per_row", 0, B),
-                                 ("split_k", 5, B), ("scalar", 32, B), ("stream", 0, 1)):
+                                 ("split_k", 5, B), ("scalar", 32, B), ("stream", 0, 1), ("batched", 2, B)):
             y = torch.empty(b, M, dtype=torch.bfloat16, device="cuda")
             g.force_kernel(kernel, param)
             g.gemv_w4(A, sc, x[:b], None, y, M, K, b)
@@ -185,9 +185,14 @@ def test_w4_swiglu(I, K):
     y = torch.empty(1, I, dtype=torch.bfloat16, device="cuda")
     g.gemv_swiglu("w4", d["A"], d["scale"], d["x"], d["bias"], y, I, K, 1)
     U.assert_close_swiglu("w4", y, yr, gate, up, adg, adu, what=f"w4 swiglu I={I} K={K}")
-    # more than one vector needs the batched kernels, which int4 does not have
-    y2 = torch.empty(2, I, dtype=torch.bfloat16, device="cuda")
-    x2 = torch.zeros(2, K, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(g.GemvError) as e:
-        g.gemv_swiglu("w4", d["A"], d["scale"], x2, None, y2, I, K, 2)
-    assert e.value.status == g.ERR_UNSUPPORTED
+    # more than one vector: the batched ring kernel carries the gate/up row pairs
+    w3 = W.small("w4", 2 * I, K, 3, True, seed=700 + I)
+    inp3 = W.make_inputs(w3)
+    yr3, gate3, up3, adg3, adu3 = oracle.swiglu("w4", W.storage_bits(inp3["A"]), W.storage_bits(inp3["x"]),
+                                                W.storage_bits(inp3["bias"]), inp3["scale"].numpy(),
+                                                nthreads=U.threads())
+    d3 = U.to_device(inp3)
+    y3 = torch.empty(3, I, dtype=torch.bfloat16, device="cuda")
+    g.gemv_swiglu("w4", d3["A"], d3["scale"], d3["x"], d3["bias"], y3, I, K, 3)
+    assert g.last_plan()["kernel_name"] == "batched"
+    U.assert_close_swiglu("w4", y3, yr3, gate3, up3, adg3, adu3, what=f"w4 swiglu B=3 I={I} K={K}")
