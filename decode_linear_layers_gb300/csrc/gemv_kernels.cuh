@@ -100,6 +100,17 @@ __device__ __forceinline__ float2 f16x2_to_f2(uint32_t w) {
   return __half22float2(h);
 }
 
+// Four 16-bit x values in two words, widened to fp32 (exact for both types).
+__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __half) {
+  const float2 f0 = f16x2_to_f2(w0), f1 = f16x2_to_f2(w1);
+  f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
+}
+__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __nv_bfloat16) {
+  f[0] = bf16_lo(w0); f[1] = bf16_hi(w0); f[2] = bf16_lo(w1); f[3] = bf16_hi(w1);
+}
+__device__ __forceinline__ float2 widen2(uint32_t w, __half) { return f16x2_to_f2(w); }
+__device__ __forceinline__ float2 widen2(uint32_t w, __nv_bfloat16) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
 // int8 -> fp32 without a conversion instruction: with u = q + 128 (the byte with
 // its top bit flipped), the float whose bits are 0x4B0000uu is 2^23 + u exactly,
 // so subtracting 2^23 + 128 leaves q exactly.  PRMT builds the bits.
@@ -855,16 +866,20 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 // per warp, U chunks per lane in flight, double-buffered across row boundaries
 // (the next row's first loads are issued before the current row is reduced), so
 // a warp never waits on an empty pipeline between rows.  Rows are dealt to CTAs
-// round-robin so that every SM gets an equal share.  x is read through L1, or
-// from shared memory (XS) where the CTA copies it once.
+// round-robin so that every SM gets an equal share.  x is read through L1
+// (XSM = 0), or from shared memory where the CTA copies it once: as stored (1), or
+// widened to fp32 (2) in quad planes [w][c][4] (lanes read consecutive 16-byte
+// words), so that no lane widens an x element per row.
 // CTAs per SM the stream plan launches (4 for fp32 rows, 2 otherwise): the
 // register budget must let them all be resident.
 template <class Op>
 constexpr int stream_ctas_per_sm() { return sizeof(typename Op::TA) == 4 ? 4 : 2; }
 
-template <class Op, int U, int THREADS, bool XS, bool SW = false>
+template <class Op, int U, int THREADS, int XSM, bool SW = false>
 __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(const Args a) {
   extern __shared__ __align__(16) unsigned char xs[];
+  constexpr bool XS = XSM != 0;
+  static_assert(XSM != 2 || sizeof(typename Op::TX) == 2, "fp32 staging widens 16-bit x");
   constexpr int WARPS = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t M = a.M, K = a.K;
@@ -904,11 +919,34 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
   }
   // x is copied into shared memory (as stored) while those loads are in flight;
   // one barrier below covers it and the epilogue operands.
-  if (XS) {
+  if constexpr (XSM == 1) {
     const int64_t n16 = nch * Op::XCH;
     const char *src = reinterpret_cast<const char *>(a.x);
     for (int64_t i = threadIdx.x; i < n16; i += THREADS) cp_async16(xs + i * 16, src + i * 16);
     asm volatile("cp.async.commit_group;" ::: "memory");
+  } else if constexpr (XSM == 2) {
+    // quad q (elements 4q..4q+3) of chunk c = 4q / VEC, quad w = (4q % VEC) / 4 goes to
+    // plane w, word c; eight quads per thread in flight at a time
+    const int64_t nq = K / 4;
+    const uint2 *src = reinterpret_cast<const uint2 *>(a.x);
+    for (int64_t q0 = threadIdx.x; q0 < nq; q0 += 8 * THREADS) {
+      uint2 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t q = q0 + (int64_t)u * THREADS;
+        v[u] = q < nq ? src[q] : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t q = q0 + (int64_t)u * THREADS;
+        if (q < nq) {
+          float f[4];
+          widen4(v[u].x, v[u].y, f, typename Op::TX());
+          const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
+          *reinterpret_cast<float4 *>(xs + (w * nch + c) * 16) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+      }
+    }
   }
   // The epilogue operands of the CTA's first THREADS rows (pairs with SW) are
   // staged in shared memory too, so that no row waits on a bias, scale or residual
@@ -935,7 +973,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
       }
     }
   }
-  if (XS) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (XSM == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (XS || staged) __syncthreads();
   while (row_live(row)) {
     float e = 0.f, o = 0.f;
@@ -963,11 +1001,33 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
       for (int u = 0; u < U; ++u) {
         const int64_t c = cc + 32 * u;
         if (c < nch) {
-          uint4 xv[Op::XCH];
+          if constexpr (XSM == 2) {
+            // quads in element order, (even, odd) pairs: the same sums as dot_chunk
+            float2 acc = make_float2(0.f, 0.f);
+            if constexpr (!Op::GROUPED) acc = make_float2(e, o);
 #pragma unroll
-          for (int h = 0; h < Op::XCH; ++h)
-            xv[h] = XS ? *reinterpret_cast<const uint4 *>(xb + c * XB + h * 16) : ld_x16(xb + c * XB + h * 16);
-          dot_chunk<Op>(e, o, cur[u], xv, Op::GROUPED ? gcur[Op::GROUPED ? u : 0] : 1.f);
+            for (int w = 0; w < Op::VEC / 4; ++w) {
+              float2 q01, q23;
+              Op::quad2(cur[u], w, q01, q23);
+              const float4 xq = *reinterpret_cast<const float4 *>(xs + (w * nch + c) * 16);
+              acc = __ffma2_rn(q01, make_float2(xq.x, xq.y), acc);
+              acc = __ffma2_rn(q23, make_float2(xq.z, xq.w), acc);
+            }
+            if constexpr (Op::GROUPED) {
+              const float gs = gcur[Op::GROUPED ? u : 0];
+              e = fmaf(gs, acc.x, e);
+              o = fmaf(gs, acc.y, o);
+            } else {
+              e = acc.x;
+              o = acc.y;
+            }
+          } else {
+            uint4 xv[Op::XCH];
+#pragma unroll
+            for (int h = 0; h < Op::XCH; ++h)
+              xv[h] = XS ? *reinterpret_cast<const uint4 *>(xb + c * XB + h * 16) : ld_x16(xb + c * XB + h * 16);
+            dot_chunk<Op>(e, o, cur[u], xv, Op::GROUPED ? gcur[Op::GROUPED ? u : 0] : 1.f);
+          }
         }
       }
       if (nrow != row) break;
@@ -1056,17 +1116,6 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
 //   which lane l holds sum l (row l / NB, vector l % NB, replicated over 32 / (R*NB)
 //   lanes) and runs its epilogue, with the operands it loaded when the group began.
 // SW (R = 2): the two rows are SwiGLU's gate row g and up row g + half.
-
-// Four 16-bit x values in two words, widened to fp32 (exact for both types).
-__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __half) {
-  const float2 f0 = f16x2_to_f2(w0), f1 = f16x2_to_f2(w1);
-  f[0] = f0.x; f[1] = f0.y; f[2] = f1.x; f[3] = f1.y;
-}
-__device__ __forceinline__ void widen4(uint32_t w0, uint32_t w1, float (&f)[4], __nv_bfloat16) {
-  f[0] = bf16_lo(w0); f[1] = bf16_hi(w0); f[2] = bf16_lo(w1); f[3] = bf16_hi(w1);
-}
-__device__ __forceinline__ float2 widen2(uint32_t w, __half) { return f16x2_to_f2(w); }
-__device__ __forceinline__ float2 widen2(uint32_t w, __nv_bfloat16) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
 // The two 16-bit halves of a word (low half = lower element).
 __device__ __forceinline__ void split_halves(uint32_t w, unsigned short &lo, unsigned short &hi) {

@@ -108,18 +108,22 @@ cudaError_t launch_stream(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
   constexpr int T = kStreamThreads;
   const dim3 grid((unsigned)p.grid), block(T);
   const bool sw = a.half > 0;  // SwiGLU row pairs
-  if (p.x_staging == GEMV_X_SMEM) {
-    auto kern = sw ? k_stream<Op, 4, T, true, true>
-                   : (p.unroll == 2 ? k_stream<Op, 2, T, true> : k_stream<Op, 4, T, true>);
+  auto run = [&](auto kern) -> cudaError_t {
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
-  } else {
-    auto kern = sw ? (p.unroll == 2 ? k_stream<Op, 2, T, false, true> : k_stream<Op, 4, T, false, true>)
-                   : (p.unroll == 2 ? k_stream<Op, 2, T, false> : k_stream<Op, 4, T, false>);
-    kern<<<grid, block, 0, s>>>(a);
+    return cudaSuccess;
+  };
+  if (p.x_staging == GEMV_X_SMEM_FP32) {
+    if constexpr (sizeof(typename Op::TX) == 2) {
+      return sw ? run(k_stream<Op, 4, T, 2, true>) : run(k_stream<Op, 4, T, 2>);
+    }
+    return cudaErrorInvalidValue;
   }
-  return cudaSuccess;
+  if (p.x_staging == GEMV_X_SMEM)
+    return sw ? run(k_stream<Op, 4, T, 1, true>) : (p.unroll == 2 ? run(k_stream<Op, 2, T, 1>) : run(k_stream<Op, 4, T, 1>));
+  return sw ? (p.unroll == 2 ? run(k_stream<Op, 2, T, 0, true>) : run(k_stream<Op, 4, T, 0, true>))
+            : (p.unroll == 2 ? run(k_stream<Op, 2, T, 0>) : run(k_stream<Op, 4, T, 0>));
 }
 
 template <class Op, int NB, int J>

@@ -329,15 +329,23 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       break;
     }
     case GEMV_KERNEL_STREAM: {
-      // fp32 rows: x through L1, four CTAs per SM; 16-bit and int8 rows: x in
-      // shared memory (when it fits in 96 KB), two CTAs per SM, deeper unroll.
+      // fp32 rows: x through L1, four CTAs per SM; 16-bit, int8 and int4 rows: x in
+      // shared memory (when it fits in 96 KB; int4: widened to fp32), two CTAs per
+      // SM, deeper unroll.
       p.lanes_per_row = 32;
       p.rows_per_warp = 1;
       p.threads = kStreamThreads;
       const bool f32 = dtype == GEMV_DTYPE_F32;
       p.unroll = f32 ? 2 : 4;
       p.x_staging = (!f32 && K * sx <= kStreamSmemMax) ? GEMV_X_SMEM : GEMV_X_GLOBAL;
-      p.smem_bytes = p.x_staging == GEMV_X_SMEM ? (int)(K * sx) : 0;
+      // int4 decodes 32 weights per chunk: x widened once per CTA takes the widening
+      // off every row (8192x8192 22.5 us against 24.4; for the other types no gain)
+      if (dtype == GEMV_DTYPE_W4 && K * 4 <= kStreamSmemMax) p.x_staging = GEMV_X_SMEM_FP32;
+      // forced: param = x staging + 1 (GEMV_X_GLOBAL, GEMV_X_SMEM, GEMV_X_SMEM_FP32)
+      if (param == 1 + GEMV_X_GLOBAL) p.x_staging = GEMV_X_GLOBAL;
+      if (param == 1 + GEMV_X_SMEM && K * sx <= kStreamSmemMax) p.x_staging = GEMV_X_SMEM;
+      if (param == 1 + GEMV_X_SMEM_FP32 && !f32 && K * 4 <= kStreamSmemMax) p.x_staging = GEMV_X_SMEM_FP32;
+      p.smem_bytes = p.x_staging == GEMV_X_SMEM ? (int)(K * sx) : p.x_staging == GEMV_X_SMEM_FP32 ? (int)(K * 4) : 0;
       // Every CTA of the persistent grid is launched even when M needs fewer warps:
       // rows are dealt to CTAs round-robin, so each SM gets an equal share.
       const int64_t per_sm = f32 ? 4 : 2;

@@ -314,8 +314,10 @@ def test_w4_host_checks():
 
 def test_plan_w4():
     K = g.KERNELS
-    p = g.plan_for("w4", 8192, 8192, 1)
-    assert p["kernel"] == K["stream"] and p["x_staging"] == 1 and p["smem_bytes"] == 8192 * 2
+    p = g.plan_for("w4", 8192, 8192, 1)   # x widened to fp32 in shared memory
+    assert p["kernel"] == K["stream"] and p["x_staging"] == 2 and p["smem_bytes"] == 8192 * 4
+    p = g.plan_for("w4", 8192, 32768, 1)  # 128 KB of fp32 x: as stored
+    assert p["kernel"] == K["stream"] and p["x_staging"] == 1 and p["smem_bytes"] == 32768 * 2
     for B, slices in ((2, 1), (4, 1), (9, 2), (16, 2)):  # the batched ring kernel
         p = g.plan_for("w4", 8192, 8192, B)
         assert p["kernel"] == K["batched"] and p["splits"] == slices, (B, p)

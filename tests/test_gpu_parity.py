@@ -54,7 +54,7 @@ SHAPES = [  # (M, K) with several tiles and ragged tails for each kernel family
 FORCED = [("rows_per_warp", 0), ("rows_per_warp", 1), ("rows_per_warp", 16),
           ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0), ("split_k", 3),
           ("split_k", 7), ("batched", 1), ("batched", 2), ("batched", 3), ("scalar", 4), ("scalar", 32),
-          ("stream", 0), ("xsplit", 0)]
+          ("stream", 0), ("stream", 1), ("stream", 3), ("xsplit", 0)]
 
 
 def xsplit_feasible(dtype, K, B):

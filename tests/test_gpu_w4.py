@@ -50,7 +50,7 @@ def test_w4_config_full_size(name):
 
 SHAPES = [(1, 128), (37, 256), (300, 384), (1001, 1024), (77, 4224), (5, 20096)]
 FORCED = [("rows_per_warp", 0), ("warp_per_row", 0), ("block_per_row", 0), ("split_k", 0),
-          ("split_k", 3), ("scalar", 4), ("scalar", 32), ("stream", 0), ("batched", 2), ("auto", 0)]
+          ("split_k", 3), ("scalar", 4), ("scalar", 32), ("stream", 0), ("stream", 2), ("batched", 2), ("auto", 0)]
 
 
 @pytest.mark.parametrize("kernel,param", FORCED)
@@ -124,7 +124,8 @@ def test_w4_k_zero_and_bad_k():
 
 def test_w4_guard_bytes_untouched():
     for kernel, param, B in (("auto", 0, 4), ("split_k", 4, 4), ("block_per_row", 0, 4), ("scalar", 32, 4),
-                             ("stream", 0, 1), ("warp_per_row", 0, 3), ("rows_per_warp", 2, 4), ("batched", 2, 9),
+                             ("stream", 0, 1), ("stream", 2, 1), ("warp_per_row", 0, 3), ("rows_per_warp", 2, 4),
+                             ("batched", 2, 9),
                              ("batched", 2, 3)):
         M, K = 333, 256
         w = W.small("w4", M, K, B, False, seed=400)
