@@ -43,9 +43,7 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
 
 template <class Op, int NB>
 cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
-  if constexpr (NB < 2) {
-    return cudaErrorInvalidValue;  // not built for one vector; the planner never picks it
-  } else {
+  {
     constexpr int T = kBatchedThreads;
     static_assert(T == 512, "the ring kernel is built for 512 threads");
     const dim3 block(T);
@@ -73,7 +71,7 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
     constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
     switch (p.variant) {
       case GEMV_BATCHED_ROWPAIR:
-        if constexpr (!Op::GROUPED) {  // not built for int4's group scales
+        if constexpr (!Op::GROUPED && NB >= 2) {  // not built for int4's group scales
           auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
           cudaError_t e = allow_smem(kern, p.smem_bytes);
           if (e != cudaSuccess) return e;
@@ -91,7 +89,7 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
         return x32 ? ring(k_batch_ring<Op, NB, R, G, 4, false, MODE>) : ring(k_batch_ring<Op, NB, R, G, SX, false, MODE>);
       }
       case GEMV_BATCHED_RING_MIXED:
-        if constexpr (A16 && SX == 2 && Op::VEC == 8) {
+        if constexpr (A16 && SX == 2 && Op::VEC == 8 && NB >= 2) {
           if (p.rows_per_warp != 2 || p.x_staging != GEMV_X_SMEM) return cudaErrorInvalidValue;
           return sw ? ring(k_batch_ring<Op, NB, 2, 4, 2, true, kRingMixed>)
                     : ring(k_batch_ring<Op, NB, 2, 4, 2, false, kRingMixed>);

@@ -14,7 +14,8 @@
 //   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
 //   fp32, B == 2, x slice fits 64 registers, at least 16 rows per SM and
 //     M < 65536                           -> XSPLIT (K split over a CTA)
-//   B >= 2                                -> BATCHED: 4..16 vectors and at most
+//   B >= 2, or int8/int4 with B == 1, at least 16 rows per SM, M < 65536 and
+//     x staged whole                      -> BATCHED: 4..16 vectors and at most
 //     one row pair per warp -> ROWPAIR, otherwise the cp.async ring (mixed-
 //     precision FMAs for fp16/bf16 with 2 or 9..16 vectors), over K slices with a
 //     second pass when x[0..B) does not fit in shared memory whole
@@ -145,7 +146,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         ok = vec_ok && nch >= 2 && force_param >= 0;
         break;
       case GEMV_KERNEL_BATCHED:
-        ok = vec_ok && B >= 2 &&
+        ok = vec_ok && (B >= 2 || force_param == 1 + GEMV_BATCHED_RING) &&
              ((force_param == 0 && batched_ok) || (force_param == 1 + GEMV_BATCHED_RING && rstage >= 0) ||
               (force_param == 1 + GEMV_BATCHED_ROWPAIR && rowpair_ok) ||
               (force_param == 1 + GEMV_BATCHED_RING_MIXED && mixed_ok));
@@ -182,7 +183,12 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 8192x4096 26.6 us against 28.7 in the ring kernel; for 16-bit types and
       // more vectors the ring kernel is faster, with one vector the streaming one)
       kernel = GEMV_KERNEL_XSPLIT;
-    } else if (B > 1 && batched_ok && nch >= 32) {
+    } else if ((B > 1 || ((dtype == GEMV_DTYPE_W8 || dtype == GEMV_DTYPE_W4) && rslices == 1 &&
+                          M >= (int64_t)num_sms * 16 && M < 65536)) &&
+               batched_ok && nch >= 32) {
+      // (one vector of int8 or int4 weights too: the decode-bound rows gain from the
+      // ring's deeper prefetch and fp32 x; int8 8192x8192 18.8 us against 20.3 in the
+      // streaming kernel, int4 20.5 against 22.6)
       kernel = GEMV_KERNEL_BATCHED;
     } else if (M >= 65536) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;

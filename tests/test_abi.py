@@ -153,7 +153,9 @@ def test_plan_config_shapes():
         assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["stream"]
     p = g.plan_for("bf16", 128256, 4096, 1)
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
-    assert g.plan_for("w8", 8192, 8192, 1)["kernel"] == K["stream"]
+    p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["nb"] == 1
+    assert p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["smem_bytes"] == 8192 * 4 + 64 * 1024
     p = g.plan_for("w8", 8192, 8192, 4)     # the ring: fp32 x (128 KB) + the 64 KB ring
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["x_staging"] == 2
     assert p["rows_per_warp"] == 4 and p["unroll"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + 64 * 1024
@@ -314,10 +316,10 @@ def test_w4_host_checks():
 
 def test_plan_w4():
     K = g.KERNELS
-    p = g.plan_for("w4", 8192, 8192, 1)   # x widened to fp32 in shared memory
-    assert p["kernel"] == K["stream"] and p["x_staging"] == 2 and p["smem_bytes"] == 8192 * 4
-    p = g.plan_for("w4", 8192, 32768, 1)  # 128 KB of fp32 x: as stored
-    assert p["kernel"] == K["stream"] and p["x_staging"] == 1 and p["smem_bytes"] == 32768 * 2
+    p = g.plan_for("w4", 8192, 8192, 1)   # one vector: the ring (x fp32, group-scale ring)
+    assert p["kernel"] == K["batched"] and p["nb"] == 1 and p["smem_bytes"] == 8192 * 4 + 64 * 1024 + 16 * 1024
+    p = g.plan_for("w4", 65536, 8192, 1)  # 65536 rows and more: not the ring
+    assert p["kernel"] == K["warp_per_row"]
     for B, slices in ((2, 1), (4, 1), (9, 2), (16, 2)):  # the batched ring kernel
         p = g.plan_for("w4", 8192, 8192, B)
         assert p["kernel"] == K["batched"] and p["splits"] == slices, (B, p)
