@@ -10,8 +10,9 @@ events on the stream it runs on; the step time is the sum of the three.
     Q_min      = M*K*s_A + B*K*s_x + B*M*s_y                 (per GEMV)
     roofline   = the K = 4096 GEMV (the dominant kernel): its Q_min / its mean
                  event time, against the measured HBM copy bandwidth
-    e2e        = the same metric with A, x, bias copied from pinned host memory
-                 and y copied back inside the timed region, every step
+    e2e        = the same metric through gemv_host (the C-ABI call on host buffers):
+                 A, x, bias copied in from pinned host memory and y copied back,
+                 inside the timed region, every step
     cpu_baseline = the CPU oracle on the same step, on the host's cores
     sweep      = every configuration at its full size, timed the same way, plus
                  the int4 (group-scaled) workloads
@@ -337,12 +338,11 @@ def run_ours(args, rank, world, local_rank):
         e2e_steps = max(3, min(args.steps, 50))
 
         def e2e_step():
+            # the library's host-buffer call: it copies A, scale, x, bias in, runs the
+            # GEMV and copies y out (one cudaMemcpyAsync per buffer), all on the stream
             for (w, d, y), (hp, hy) in zip(items, pinned):
-                for k, v in hp.items():
-                    if v is not None:
-                        d[k].copy_(v, non_blocking=True)
-                call_gemv(g, w, d, y)
-                hy.copy_(y, non_blocking=True)
+                g.gemv_host(w.dtype, hp["A"], hp["scale"], hp["x"], hp["bias"], hy,
+                            d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
 
         for _ in range(2):
             e2e_step()

@@ -23,7 +23,7 @@ from .build import LIB as LIB_PATH, build
 
 __all__ = [
     "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_w4", "gemv_bf16_splitk_noalloc", "gemv_ex",
-    "gemv_swiglu", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
+    "gemv_swiglu", "gemv_host", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
     "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH", "device_status", "test_stall",
 ]
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.gemv_ex.restype = ci
         L.gemv_swiglu.argtypes = [ci, vp, vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_swiglu.restype = ci
+        L.gemv_host.argtypes = [ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, vp]
+        L.gemv_host.restype = ci
         L.gemv_status_string.argtypes = [ci]
         L.gemv_status_string.restype = ctypes.c_char_p
         L.gemv_last_cuda_error.argtypes = []
@@ -232,6 +234,39 @@ def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
     args = (_addr(A, 1, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, 2, nx, "x"),
             _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
     _check(lib().gemv_w8(*args, M, K, B, _stream(stream)))
+
+
+def _host_addr(t, elem_size: int, min_elems: int, what: str):
+    """Host address of a CPU tensor (checked) or of a raw int pointer (unchecked)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if getattr(t, "is_cuda", True):
+        raise ValueError(f"{what} must be a CPU tensor (pinned for asynchronous copies) or a host address")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.element_size() != elem_size:
+        raise ValueError(f"{what}: element size {t.element_size()} != {elem_size}")
+    if t.numel() < min_elems:
+        raise ValueError(f"{what}: {t.numel()} elements < {min_elems} needed")
+    return t.data_ptr()
+
+
+def gemv_host(dtype, h_A, h_scale, h_x, h_bias, h_y, d_A, d_scale, d_x, d_bias, d_y, M, K, B,
+              stream=None) -> None:
+    """The GEMV on host buffers: copies h_A, h_scale, h_x, h_bias (CPU tensors,
+    pinned for asynchronous copies; None skips a copy) into the device buffers d_*,
+    runs it there and copies y back into h_y, all enqueued on `stream`."""
+    M, K, B, _, nx, ny = _sizes(M, K, B)
+    sa = {"f32": 4, "f16": 2, "bf16": 2, "w8": 1, "w4": 1}[dtype]
+    sx = 4 if dtype == "f32" else 2
+    na, ns = _a_count(dtype, M, K)
+    hs = (_host_addr(h_A, sa, na, "h_A"), _host_addr(h_scale, 4, ns, "h_scale"), _host_addr(h_x, sx, nx, "h_x"),
+          _host_addr(h_bias, sx, M if h_bias is not None else 0, "h_bias"), _host_addr(h_y, sx, ny, "h_y"))
+    ds = (_addr(d_A, sa, na, "d_A"), _addr(d_scale, 4, ns, "d_scale"), _addr(d_x, sx, nx, "d_x"),
+          _addr(d_bias, sx, M if d_bias is not None else 0, "d_bias"), _addr(d_y, sx, ny, "d_y"))
+    _check(lib().gemv_host(DTYPE_CODES[dtype], *hs, *ds, M, K, B, _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024

@@ -286,6 +286,48 @@ gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_sc
   return run((int)dtype, A, row_scale, x, bias, nullptr, y, m2, K, B, GEMV_ACT_NONE, true, stream);
 }
 
+gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scale, const void *h_x,
+                        const void *h_bias, void *h_y, void *d_A, float *d_scale, void *d_x, void *d_bias,
+                        void *d_y, int64_t M, int64_t K, int B, gemv_stream_t stream) {
+  const int dt = (int)dtype;
+  if (dt < GEMV_DTYPE_F32 || dt > GEMV_DTYPE_W4 || M < 0 || K < 0 || B < 0) return GEMV_ERR_INVALID_VALUE;
+  const bool w4 = dt == GEMV_DTYPE_W4, scaled = dt == GEMV_DTYPE_W8 || w4;
+  const bool half16 = dt == GEMV_DTYPE_F16 || dt == GEMV_DTYPE_BF16;
+  if (w4 && K % GEMV_W4_GROUP != 0) return GEMV_ERR_INVALID_VALUE;
+  if (B > GEMV_MAX_BATCH && !(half16 && B <= GEMV_MAX_BATCH_TC)) return GEMV_ERR_UNSUPPORTED;
+  if (M == 0 || B == 0) return GEMV_SUCCESS;
+  if (h_y == nullptr || d_y == nullptr) return GEMV_ERR_INVALID_VALUE;
+  if (K > 0 && (h_x == nullptr || d_x == nullptr)) return GEMV_ERR_INVALID_VALUE;
+  if ((h_A != nullptr && d_A == nullptr) || (h_scale != nullptr && d_scale == nullptr) ||
+      (h_bias != nullptr && d_bias == nullptr))
+    return GEMV_ERR_INVALID_VALUE;
+  if (!scaled && (h_scale != nullptr || d_scale != nullptr)) return GEMV_ERR_INVALID_VALUE;
+  const int sa = gemv::elem_bytes_a(dt), sx = gemv::elem_bytes_x(dt);
+  int64_t mk, a_bytes, bk, x_bytes, bm, y_bytes, b_bytes;
+  if (!mul_ok(M, K, &mk) || !mul_ok(mk, sa, &a_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (w4) a_bytes /= 2;
+  const int64_t s_bytes = scaled ? (w4 ? M * (K / GEMV_W4_GROUP) : M) * 4 : 0;
+  if (!mul_ok(B, K, &bk) || !mul_ok(bk, sx, &x_bytes)) return GEMV_ERR_INVALID_VALUE;
+  if (!mul_ok(B, M, &bm) || !mul_ok(bm, sx, &y_bytes) || !mul_ok(M, sx, &b_bytes)) return GEMV_ERR_INVALID_VALUE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // inputs host -> device, one copy per buffer, in stream order before the GEMV
+  auto h2d = [&](void *dst, const void *src, int64_t n) -> cudaError_t {
+    if (src == nullptr || n == 0) return cudaSuccess;
+    return cudaMemcpyAsync(dst, src, (size_t)n, cudaMemcpyHostToDevice, s);
+  };
+  cudaError_t e = h2d(d_A, h_A, K > 0 ? a_bytes : 0);
+  if (e == cudaSuccess) e = h2d(d_scale, h_scale, K > 0 ? s_bytes : 0);
+  if (e == cudaSuccess) e = h2d(d_x, h_x, x_bytes);
+  if (e == cudaSuccess) e = h2d(d_bias, h_bias, b_bytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const gemv_status_t st = run(dt, d_A, d_scale, d_x, h_bias != nullptr || d_bias != nullptr ? d_bias : nullptr,
+                               nullptr, d_y, M, K, B, GEMV_ACT_NONE, false, stream);
+  if (st != GEMV_SUCCESS) return st;
+  e = cudaMemcpyAsync(h_y, d_y, (size_t)y_bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GEMV_SUCCESS;
+}
+
 const char *gemv_status_string(gemv_status_t s) {
   switch (s) {
     case GEMV_SUCCESS: return "GEMV_SUCCESS";

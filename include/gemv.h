@@ -176,13 +176,37 @@ gemv_status_t gemv_ex(gemv_dtype_t dtype, const void *A, const float *row_scale,
  * One launch; the gate and up sums of an output meet in registers, so the 2I
  * intermediate values never reach memory.  Needs 16-byte aligned rows with at least
  * one 16-byte chunk per lane of a warp, and for B > 1 x[0..B) small enough to stage
- * in shared memory and a storage type other than GEMV_DTYPE_W4; otherwise
- * GEMV_ERR_UNSUPPORTED and nothing is launched. */
+ * in shared memory whole (one K slice); otherwise GEMV_ERR_UNSUPPORTED and nothing is
+ * launched. */
 gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_scale, const void *x,
                           const void *bias, void *y, int64_t I, int64_t K, int B,
                           gemv_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
+/* End to end on host buffers: the GEMV of gemv_f32 .. gemv_w4 (chosen by dtype) with
+ * its operands in host memory.  On `stream` it copies each host input into the
+ * caller's device buffer of the same size (one cudaMemcpyAsync per buffer), runs the
+ * GEMV on the device buffers, and copies y back into h_y.
+ *   h_A / d_A      A: M x K elements (int4: M x K / 2 bytes).  h_A == NULL skips the
+ *                  copy (weights already resident in d_A).
+ *   h_scale / d_scale  int8: M fp32 row scales; int4: M x K / GEMV_W4_GROUP fp32
+ *                  group scales; NULL for the other types.  h_scale == NULL skips
+ *                  the copy (scales resident in d_scale).
+ *   h_x / d_x      x: B x K (required when K > 0).
+ *   h_bias / d_bias  bias: M entries, or both NULL.
+ *   h_y / d_y      y: B x M (required).
+ * Ownership: all buffers are the caller's; the library allocates nothing beyond what
+ * the device GEMV needs.  Host buffers should be pinned: with pageable memory the
+ * copies synchronise the host.  The call returns after enqueueing; h_y holds y once
+ * `stream` has drained.  Errors: bad sizes, a device buffer missing for a host buffer
+ * given, or a missing x or y are GEMV_ERR_INVALID_VALUE and B beyond the type's limit
+ * GEMV_ERR_UNSUPPORTED, all before any copy; a failed copy is GEMV_ERR_CUDA; the
+ * device GEMV's own checks (alignment, overlap, shapes its kernels cannot run) come
+ * after the input copies are enqueued, and then y is not copied back. */
+gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scale, const void *h_x,
+                        const void *h_bias, void *h_y, void *d_A, float *d_scale, void *d_x, void *d_bias,
+                        void *d_y, int64_t M, int64_t K, int B, gemv_stream_t stream);
+
 const char *gemv_status_string(gemv_status_t status);
 
 /* The cudaError_t of this thread's last GEMV_ERR_CUDA (0 if none). */
