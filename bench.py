@@ -474,6 +474,21 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
     iso = time_gemvs(torch, g, items, flush, iters, 3)
     iso_ms = sum(statistics.median(t) for t in iso)
     fused = decode_layer_fused(torch, g, dev, items, timed)
+    # the same layer with plain launches (no programmatic dependent launch)
+    g.set_launch_overlap("off")
+    try:
+        plain_eager_ms = timed(run)
+        side2 = torch.cuda.Stream()
+        side2.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side2):
+            run()
+        torch.cuda.current_stream().wait_stream(side2)
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2):
+            run()
+        plain_graph_ms = timed(graph2.replay)
+    finally:
+        g.set_launch_overlap("launch")
     return {"layer": "bf16 B=1: " + ", ".join(f"{n} {M}x{K}" for n, M, K in DECODE_LAYER),
             "bytes": layer_bytes, "kernels": launches,
             "eager_us": round(eager_ms * 1e3, 2), "graph_us": round(graph_ms * 1e3, 2),
@@ -481,6 +496,8 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
             "eager_gbs": round(layer_bytes / (eager_ms * 1e-3) / 1e9, 1),
             "graph_gbs": round(layer_bytes / (graph_ms * 1e-3) / 1e9, 1),
             "graph_frac_of_peak": round(layer_bytes / (graph_ms * 1e-3) / 1e9 / peak, 4),
+            "launch_overlap": "programmatic dependent launch (the library's default)",
+            "plain_launches": {"eager_us": round(plain_eager_ms * 1e3, 2), "graph_us": round(plain_graph_ms * 1e3, 2)},
             "fused": dict(fused, graph_frac_of_peak=round(fused["graph_gbs"] / peak, 4))}
 
 

@@ -23,7 +23,7 @@ from .build import LIB as LIB_PATH, build
 
 __all__ = [
     "gemv_f32", "gemv_f16", "gemv_bf16", "gemv_w8", "gemv_w4", "gemv_bf16_splitk_noalloc", "gemv_ex",
-    "gemv_swiglu", "gemv_host", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
+    "gemv_swiglu", "gemv_host", "set_launch_overlap", "ACT_NONE", "ACT_SILU", "GemvError", "Plan", "plan_for",
     "status_string", "launch_count", "last_cuda_error", "force_kernel", "last_plan",
     "KERNELS", "DTYPE_CODES", "lib", "build", "LIB_PATH", "device_status", "test_stall",
 ]
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.gemv_swiglu.restype = ci
         L.gemv_host.argtypes = [ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, vp]
         L.gemv_host.restype = ci
+        L.gemv_set_launch_overlap.argtypes = [ci]
+        L.gemv_set_launch_overlap.restype = ci
         L.gemv_status_string.argtypes = [ci]
         L.gemv_status_string.restype = ctypes.c_char_p
         L.gemv_last_cuda_error.argtypes = []
@@ -234,6 +236,17 @@ def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
     args = (_addr(A, 1, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, 2, nx, "x"),
             _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
     _check(lib().gemv_w8(*args, M, K, B, _stream(stream)))
+
+
+OVERLAP = {"off": 0, "launch": 1, "weights": 2}
+
+
+def set_launch_overlap(mode: str) -> None:
+    """Launch overlap for this thread's later calls: "off", "launch" (programmatic
+    dependent launches, every access after the previous kernel; the default) or
+    "weights" (the first weight loads before that wait; only for weights the
+    preceding work does not write)."""
+    _check(lib().gemv_set_launch_overlap(OVERLAP[mode]))
 
 
 def _host_addr(t, elem_size: int, min_elems: int, what: str):

@@ -23,6 +23,9 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local gemv_plan_t t_last_plan = {};
 thread_local bool t_have_plan = false;
+// gemv_set_launch_overlap; programmatic dependent launches by default (they change
+// no result: every kernel waits for its predecessor before touching memory)
+thread_local int t_overlap = GEMV_OVERLAP_LAUNCH;
 
 std::atomic<uint64_t> g_launches{0};
 int g_force_kernel = GEMV_KERNEL_AUTO;  // test-only override (not thread-safe)
@@ -171,6 +174,7 @@ gemv_status_t run(int dtype, const void *A, const float *scale, const void *x, c
   args.residual = residual;
   args.act = act;
   args.half = swiglu ? M / 2 : 0;
+  args.pdl = t_overlap;
   if (p.kernel == GEMV_KERNEL_TC) {
     st = status_word(&args.status);
     if (st != GEMV_SUCCESS) return st;
@@ -238,6 +242,7 @@ bool tc_tensor_maps(int dtype, const void *A, const void *x, int64_t M, int64_t 
 // CUDA error and the launch counter in one place.
 void record_cuda_error(int e) { t_last_cuda_error = e; }
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+int launch_overlap() { return t_overlap; }
 }  // namespace gemv
 
 extern "C" {
@@ -325,6 +330,13 @@ gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scal
   if (st != GEMV_SUCCESS) return st;
   e = cudaMemcpyAsync(h_y, d_y, (size_t)y_bytes, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e);
+  return GEMV_SUCCESS;
+}
+
+gemv_status_t gemv_set_launch_overlap(int mode) {
+  if (mode != GEMV_OVERLAP_OFF && mode != GEMV_OVERLAP_LAUNCH && mode != GEMV_OVERLAP_WEIGHTS)
+    return GEMV_ERR_INVALID_VALUE;
+  t_overlap = mode;
   return GEMV_SUCCESS;
 }
 

@@ -60,7 +60,26 @@ struct Args {
   int *status = nullptr;
   int64_t timeout_ns = 2000000000;
   int test_stall = 0;
+  // programmatic dependent launch: 0 off; 1 the kernel lets the next one launch
+  // early and waits for the previous one before touching memory; 2 as 1, but the
+  // first loads of A (and its scales) go out before that wait
+  int pdl = 0;
 };
+
+// Programmatic dependent launch (a no-op in a kernel launched without it).
+// Lets the next kernel on the stream be scheduled as SMs free up.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until the previous kernel on the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Start of a kernel: trigger, and wait unless the kernel may prefetch its weights.
+__device__ __forceinline__ void pdl_enter(const Args &a, bool may_prefetch) {
+  pdl_trigger();
+  if (!(may_prefetch && a.pdl == 2)) pdl_wait();
+}
+// After a kernel's weight prefetch: the wait it put off.
+__device__ __forceinline__ void pdl_after_prefetch(const Args &a) {
+  if (a.pdl == 2) pdl_wait();
+}
 
 // ------------------------------------------------------------------ memory access
 // A is read exactly once: skip L1 and mark the L2 lines evict-first so x, y and
@@ -581,6 +600,7 @@ __device__ __forceinline__ float group_sum(float v) {
 // reach the butterfly, with rows past M contributing zeros.
 template <class Op, int TPR, int NB, int U, bool VEC, int THREADS = kThreads>
 __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
+  pdl_enter(a, false);
   constexpr int TEAMS = THREADS / TPR;
   const int sub = threadIdx.x & (TPR - 1);
   const int team = threadIdx.x / TPR;
@@ -666,6 +686,7 @@ __global__ void __launch_bounds__(THREADS) k_rowteam(const Args a) {
 template <class Op, int NB, int U>
 __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *partial,
                                                        int64_t chunks_per_split) {
+  pdl_enter(a, false);
   __shared__ float red[NB][kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t M = a.M, K = a.K;
@@ -737,6 +758,7 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
 template <class Op>
 __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const float *partial,
                                                             int splits) {
+  pdl_enter(a, false);  // the partial sums come from the kernel before
   const int64_t M = a.M;
   const int64_t total = M * a.B;
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
@@ -759,6 +781,7 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
 // fp32 accumulator) for the 16-bit types.
 template <class Op, int NB, int R, int U, int THREADS, bool SW = false>
 __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
+  pdl_enter(a, true);
   static_assert(!SW || R == 2, "SwiGLU pairs the gate and up row of one output");
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr int WARPS = THREADS / 32;
@@ -788,6 +811,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
                                                      : make_uint4(0, 0, 0, 0);
     }
+  pdl_after_prefetch(a);
   {
     const int64_t n16 = (xstride * B) / 16, nz16 = (xstride * NB) / 16;
     const char *src = reinterpret_cast<const char *>(a.x);
@@ -877,6 +901,7 @@ constexpr int stream_ctas_per_sm() { return sizeof(typename Op::TA) == 4 ? 4 : 2
 
 template <class Op, int U, int THREADS, int XSM, bool SW = false>
 __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(const Args a) {
+  pdl_enter(a, true);
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr bool XS = XSM != 0;
   static_assert(XSM != 2 || sizeof(typename Op::TX) == 2, "fp32 staging widens 16-bit x");
@@ -917,6 +942,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
     if constexpr (Op::GROUPED) gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
   }
+  pdl_after_prefetch(a);
   // x is copied into shared memory (as stored) while those loads are in flight;
   // one barrier below covers it and the epilogue operands.
   if constexpr (XSM == 1) {
@@ -1142,6 +1168,7 @@ template <class Op, int NB, int R, int G, int XE, bool SW, int MODE = (NB >= 8 ?
           int THREADS = 512>
 __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *partial,
                                                            int64_t chunks_per_split) {
+  pdl_enter(a, true);
   constexpr int WARPS = THREADS / 32;
   constexpr bool PAIRS = MODE == kRingPairs;
   static_assert(MODE != kRingMixed || (XE == 2 && Op::VEC == 8), "mixed FMAs take 16-bit A and x");
@@ -1220,7 +1247,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   const unsigned char *xsrc = reinterpret_cast<const unsigned char *>(a.x) + k0 * SX;
   const int64_t nq = nch * Op::VEC / 4;  // quads per vector in the slice
   constexpr bool XCOPY = !PAIRS && XE == SX;
-  if constexpr (XCOPY) {
+  // (with weight prefetch before the launch dependency is resolved, A's first steps go
+  // out first and x's copy after the wait, as the newest group)
+  const bool x_first = a.pdl != 2;
+  auto copy_x = [&]() {
     for (int64_t i = tid; i < (int64_t)B * nq; i += THREADS) {
       const int64_t b = i / nq, q = i - b * nq;
       const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
@@ -1234,12 +1264,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
     asm volatile("cp.async.commit_group;" ::: "memory");
     for (int64_t i = (int64_t)B * PPV * pstride / 16 + tid; i < xbytes / 16; i += THREADS)
       reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);  // vectors B..NB-1
-  }
+  };
+  if (XCOPY && x_first) copy_x();
 #pragma unroll
   for (int s = 0; s < G; ++s) issue(s);
+  pdl_after_prefetch(a);
 
   if constexpr (XCOPY) {
-    asm volatile("cp.async.wait_group %0;" ::"n"(G) : "memory");  // x's group (the oldest)
+    if (x_first) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(G) : "memory");  // x's group (the oldest)
+    } else {
+      copy_x();
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
   } else {
     // quad q of vector b (zero past B), as 4 fp32 values or 2 words of 16-bit values
     auto load_quad = [&](int64_t b, int64_t q) -> uint4 {
@@ -1455,6 +1492,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
 
 template <class Op, int NB, int J, int P, int G>
 __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
+  pdl_enter(a, true);
   static_assert(NB == 1 || NB == 2 || NB == 4, "NB");
   static_assert(kXsT % P == 0, "a barrier batch is whole groups");
   constexpr int D = P * G;  // rows in the ring
@@ -1489,6 +1527,7 @@ __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
   };
 #pragma unroll
   for (int gi = 0; gi < G; ++gi) issue(gi);
+  pdl_after_prefetch(a);
 
   float2 xr[J][NB][PV];
 #pragma unroll

@@ -5,12 +5,35 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <utility>
 
 #include "gemv_kernels.cuh"
 #include "gemv_plan.h"
 #include "gemv_tc.cuh"
 
 namespace gemv {
+
+// Every launch goes through cudaLaunchKernelEx: with a.pdl it is a programmatic
+// dependent launch, which the GPU may start while the previous kernel on the stream
+// is finishing (the kernel then waits for it with griddepcontrol.wait, see
+// pdl_enter, before touching memory that kernel could have written).
+template <class... P, class... A2>
+cudaError_t launch_k(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int pdl,
+                     A2 &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl != 0) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A2>(args)...);
+}
 
 // Dynamic shared memory above 48 KB has to be allowed per kernel.
 template <typename Kern>
@@ -24,18 +47,18 @@ cudaError_t launch_rowteam(const gemv_plan_t &p, const Args &a, cudaStream_t s) 
   const dim3 grid((unsigned)p.grid), block(kThreads);
   if (p.kernel == GEMV_KERNEL_SCALAR) {
     switch (p.lanes_per_row) {
-      case 4: k_rowteam<Op, 4, NB, 1, false><<<grid, block, 0, s>>>(a); break;
-      default: k_rowteam<Op, 32, NB, 1, false><<<grid, block, 0, s>>>(a); break;
+      case 4: return launch_k(k_rowteam<Op, 4, NB, 1, false>, grid, block, 0, s, a.pdl, a);
+      default: return launch_k(k_rowteam<Op, 32, NB, 1, false>, grid, block, 0, s, a.pdl, a);
     }
     return cudaSuccess;
   }
   switch (p.lanes_per_row) {
-    case 1: k_rowteam<Op, 1, NB, 1, true><<<grid, block, 0, s>>>(a); break;
-    case 2: k_rowteam<Op, 2, NB, 1, true><<<grid, block, 0, s>>>(a); break;
-    case 4: k_rowteam<Op, 4, NB, 1, true><<<grid, block, 0, s>>>(a); break;
-    case 8: k_rowteam<Op, 8, NB, 1, true><<<grid, block, 0, s>>>(a); break;
-    case 16: k_rowteam<Op, 16, NB, 1, true><<<grid, block, 0, s>>>(a); break;
-    case 32: k_rowteam<Op, 32, NB, kUnrollWarpRow, true><<<grid, block, 0, s>>>(a); break;
+    case 1: return launch_k(k_rowteam<Op, 1, NB, 1, true>, grid, block, 0, s, a.pdl, a);
+    case 2: return launch_k(k_rowteam<Op, 2, NB, 1, true>, grid, block, 0, s, a.pdl, a);
+    case 4: return launch_k(k_rowteam<Op, 4, NB, 1, true>, grid, block, 0, s, a.pdl, a);
+    case 8: return launch_k(k_rowteam<Op, 8, NB, 1, true>, grid, block, 0, s, a.pdl, a);
+    case 16: return launch_k(k_rowteam<Op, 16, NB, 1, true>, grid, block, 0, s, a.pdl, a);
+    case 32: return launch_k(k_rowteam<Op, 32, NB, kUnrollWarpRow, true>, grid, block, 0, s, a.pdl, a);
     default: return cudaErrorInvalidValue;
   }
   return cudaSuccess;
@@ -57,15 +80,14 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
     auto ring = [&](auto kern) -> cudaError_t {
       cudaError_t e = allow_smem(kern, p.smem_bytes);
       if (e != cudaSuccess) return e;
-      kern<<<dim3((unsigned)p.grid, (unsigned)p.splits), block, (size_t)p.smem_bytes, s>>>(
-          a, p.splits > 1 ? ws : nullptr, cps);
-      e = cudaGetLastError();
+      e = launch_k(kern, dim3((unsigned)p.grid, (unsigned)p.splits), block, (size_t)p.smem_bytes, s, a.pdl, a,
+                   p.splits > 1 ? ws : nullptr, cps);
       if (e != cudaSuccess || p.splits == 1) return e;
       const int64_t total = a.M * a.B;
       int64_t g = (total + kThreads - 1) / kThreads;
       if (g > 65535) g = 65535;
-      k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
-      return cudaSuccess;
+      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
+                      p.splits);
     };
     constexpr int SX = (int)sizeof(typename Op::TX);
     constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
@@ -75,8 +97,7 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
           auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
           cudaError_t e = allow_smem(kern, p.smem_bytes);
           if (e != cudaSuccess) return e;
-          kern<<<dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s>>>(a);
-          return cudaSuccess;
+          return launch_k(kern, dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s, a.pdl, a);
         }
         return cudaErrorInvalidValue;
       case GEMV_BATCHED_RING: {
@@ -109,8 +130,7 @@ cudaError_t launch_stream(const gemv_plan_t &p, const Args &a, cudaStream_t s) {
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block, (size_t)p.smem_bytes, s>>>(a);
-    return cudaSuccess;
+    return launch_k(kern, grid, block, (size_t)p.smem_bytes, s, a.pdl, a);
   };
   if (p.x_staging == GEMV_X_SMEM_FP32) {
     if constexpr (sizeof(typename Op::TX) == 2) {
@@ -132,8 +152,7 @@ cudaError_t launch_xsplit_j(const gemv_plan_t &p, const Args &a, cudaStream_t s)
     auto kern = k_xsplit<Op, NB, J, xsplit_rows_per_group(J), kXsplitGroups>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)p.grid), dim3(kXsThreads), (size_t)p.smem_bytes, s>>>(a);
-    return cudaSuccess;
+    return launch_k(kern, dim3((unsigned)p.grid), dim3(kXsThreads), (size_t)p.smem_bytes, s, a.pdl, a);
   }
 }
 
@@ -155,21 +174,19 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
     case GEMV_KERNEL_SCALAR:
       return launch_rowteam<Op, NB>(p, a, s);
     case GEMV_KERNEL_BLOCK_PER_ROW:
-      k_blockrow<Op, NB, kUnrollBlockRow><<<dim3((unsigned)p.grid, 1), dim3(kThreads), 0, s>>>(
-          a, nullptr, a.K / Op::VEC);
-      return cudaSuccess;
+      return launch_k(k_blockrow<Op, NB, kUnrollBlockRow>, dim3((unsigned)p.grid, 1), dim3(kThreads), 0, s, a.pdl,
+                      a, (float *)nullptr, (int64_t)(a.K / Op::VEC));
     case GEMV_KERNEL_SPLIT_K: {
       const int64_t nch = a.K / Op::VEC;
       const int64_t per = (nch + p.splits - 1) / p.splits;
-      k_blockrow<Op, NB, kUnrollBlockRow><<<dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kThreads), 0, s>>>(
-          a, ws, per);
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = launch_k(k_blockrow<Op, NB, kUnrollBlockRow>, dim3((unsigned)p.grid, (unsigned)p.splits),
+                               dim3(kThreads), 0, s, a.pdl, a, ws, per);
       if (e != cudaSuccess) return e;
       const int64_t total = a.M * a.B;
       int64_t g = (total + kThreads - 1) / kThreads;
       if (g > 65535) g = 65535;
-      k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
-      return cudaSuccess;
+      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
+                      p.splits);
     }
     case GEMV_KERNEL_BATCHED:
       return launch_batched<Op, NB>(p, a, ws, s);
@@ -202,16 +219,14 @@ cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
     auto kern = ka == 2 ? k_tc<Op, 2> : k_tc<Op, 1>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kTcThreads), (size_t)p.smem_bytes, s>>>(
-        map_a, map_x, a, p.splits > 1 ? ws : nullptr, (int64_t)p.unroll, p.nb, stages);
-    if (p.splits == 1) return cudaSuccess;
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    e = launch_k(kern, dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kTcThreads), (size_t)p.smem_bytes, s, a.pdl,
+                 map_a, map_x, a, p.splits > 1 ? ws : nullptr, (int64_t)p.unroll, p.nb, stages);
+    if (e != cudaSuccess || p.splits == 1) return e;
     const int64_t total = a.M * a.B;
     int64_t g = (total + kThreads - 1) / kThreads;
     if (g > 65535) g = 65535;
-    k_splitk_reduce<Op><<<dim3((unsigned)g), dim3(kThreads), 0, s>>>(a, ws, p.splits);
-    return cudaSuccess;
+    return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
+                    p.splits);
   }
 }
 

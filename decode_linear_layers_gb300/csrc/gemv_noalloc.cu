@@ -107,6 +107,7 @@ extern "C" gemv_status_t gemv_bf16_splitk_noalloc(const uint16_t *A, const uint1
   a.M = M;
   a.K = K;
   a.B = B;
+  a.pdl = gemv::launch_overlap();
   cudaError_t e = gemv::launch_bf16(p, a, scratch, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -67,6 +67,7 @@ int chunk_elems(int dtype);
 // Defined in gemv_api.cu.
 void record_cuda_error(int e);
 void count_launches(int n);
+int launch_overlap();  // the calling thread's gemv_set_launch_overlap mode
 
 gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int num_sms,
                    int force_kernel, int force_param, gemv_plan_t *out);

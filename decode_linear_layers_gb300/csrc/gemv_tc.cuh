@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;                                  // set by either role on timeout
   __shared__ long long sh_loaded, sh_consumed, sh_committed;  // for the drain after an abort
+  pdl_enter(a, false);  // every read (TMA included) after the kernel before has finished
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t M = a.M, K = a.K;
   const int B = a.B;

@@ -207,6 +207,26 @@ gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scal
                         const void *h_bias, void *h_y, void *d_A, float *d_scale, void *d_x, void *d_bias,
                         void *d_y, int64_t M, int64_t K, int B, gemv_stream_t stream);
 
+/* Launch overlap for the calling thread's later calls (initially GEMV_OVERLAP_LAUNCH).
+ * Programmatic dependent launch: a GEMV's kernels may be scheduled while the kernel
+ * before them on the stream is finishing, so that back-to-back GEMVs (a decode layer,
+ * a CUDA graph of them) lose less time between kernels.
+ *   GEMV_OVERLAP_OFF      plain launches.
+ *   GEMV_OVERLAP_LAUNCH   each kernel waits for the previous kernel on the stream
+ *                         (griddepcontrol.wait) before it reads or writes any memory:
+ *                         results and ordering are those of plain launches.  Kernels
+ *                         of other libraries after a GEMV are launched as usual.
+ *   GEMV_OVERLAP_WEIGHTS  as GEMV_OVERLAP_LAUNCH, but the persistent kernels issue their
+ *                         first loads of A (and of its scales) before that wait.  Only
+ *                         for weights that the work queued before on the stream does not
+ *                         write.
+ * Works under CUDA graph capture (the dependency becomes a programmatic edge).
+ * GEMV_ERR_INVALID_VALUE for another mode. */
+#define GEMV_OVERLAP_OFF 0
+#define GEMV_OVERLAP_LAUNCH 1
+#define GEMV_OVERLAP_WEIGHTS 2
+gemv_status_t gemv_set_launch_overlap(int mode);
+
 const char *gemv_status_string(gemv_status_t status);
 
 /* The cudaError_t of this thread's last GEMV_ERR_CUDA (0 if none). */

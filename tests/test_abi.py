@@ -362,3 +362,13 @@ def test_plan_tensor_cores():
         g.plan_for("bf16", 100, 64, 257)
     with pytest.raises(g.GemvError):       # more than 16 vectors needs 16-byte rows
         g.plan_for("bf16", 100, 60, 17)
+
+
+def test_launch_overlap_modes():
+    # host-only setting of the calling thread: modes 0..2, anything else refused
+    L = g.lib()
+    for m in (1, 2, 0):
+        assert L.gemv_set_launch_overlap(m) == 0
+    assert L.gemv_set_launch_overlap(3) == g.ERR_INVALID_VALUE
+    assert L.gemv_set_launch_overlap(-1) == g.ERR_INVALID_VALUE
+    g.set_launch_overlap("launch")  # the default
