@@ -38,13 +38,13 @@ constexpr int kThreads = 256;  // every kernel runs 8 warps per CTA
 constexpr int kWarps = kThreads / 32;
 
 struct Args {
-  const void *A;
-  const void *x;
-  const void *bias;     // nullptr: no bias
-  const float *scale;   // w8 row scale, nullptr otherwise
-  void *y;
-  int64_t M, K;
-  int B;
+  const void *A = nullptr;
+  const void *x = nullptr;
+  const void *bias = nullptr;   // nullptr: no bias
+  const float *scale = nullptr; // w8 row scale, nullptr otherwise
+  void *y = nullptr;
+  int64_t M = 0, K = 0;
+  int B = 0;
   // fused epilogue (all kernels): activation, then residual[b][m] (y's type, B x M,
   // may be y itself).  SwiGLU (half > 0): A is [gate rows 0..half-1; up rows
   // half..2*half-1], M = 2*half, and y[b][m] = silu(gate_m) * up_m is B x half.
@@ -899,9 +899,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 template <class Op>
 constexpr int stream_ctas_per_sm() { return sizeof(typename Op::TA) == 4 ? 4 : 2; }
 
-template <class Op, int U, int THREADS, int XSM, bool SW = false>
-__global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(const Args a) {
-  pdl_enter(a, true);
+template <class Op, int U, int THREADS, int XSM, bool SW = false, int CPS = stream_ctas_per_sm<Op>()>
+__global__ void __launch_bounds__(THREADS, CPS) k_stream(const Args a) {
+  // (fp32 rows run at the 32-register cap: they take no weight prefetch, which
+  // would cost registers across the prologue)
+  constexpr bool kPrefetch = sizeof(typename Op::TA) != 4;
+  pdl_enter(a, kPrefetch);
   extern __shared__ __align__(16) unsigned char xs[];
   constexpr bool XS = XSM != 0;
   static_assert(XSM != 2 || sizeof(typename Op::TX) == 2, "fp32 staging widens 16-bit x");
@@ -942,7 +945,7 @@ __global__ void __launch_bounds__(THREADS, stream_ctas_per_sm<Op>()) k_stream(co
     buf[u] = (row_live(row) && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol) : make_uint4(0, 0, 0, 0);
     if constexpr (Op::GROUPED) gbuf[u] = (row_live(row) && c < nch) ? chunk_scale<Op>(a, row, c) : 0.f;
   }
-  pdl_after_prefetch(a);
+  if constexpr (kPrefetch) pdl_after_prefetch(a);
   // x is copied into shared memory (as stored) while those loads are in flight;
   // one barrier below covers it and the epilogue operands.
   if constexpr (XSM == 1) {

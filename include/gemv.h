@@ -216,10 +216,10 @@ gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scal
  *                         (griddepcontrol.wait) before it reads or writes any memory:
  *                         results and ordering are those of plain launches.  Kernels
  *                         of other libraries after a GEMV are launched as usual.
- *   GEMV_OVERLAP_WEIGHTS  as GEMV_OVERLAP_LAUNCH, but the persistent kernels issue their
- *                         first loads of A (and of its scales) before that wait.  Only
- *                         for weights that the work queued before on the stream does not
- *                         write.
+ *   GEMV_OVERLAP_WEIGHTS  as GEMV_OVERLAP_LAUNCH, but the persistent kernels of 16-bit
+ *                         and quantised weights issue their first loads of A (and of its
+ *                         scales) before that wait.  Only for weights that the work
+ *                         queued before on the stream does not write.
  * Works under CUDA graph capture (the dependency becomes a programmatic edge).
  * GEMV_ERR_INVALID_VALUE for another mode. */
 #define GEMV_OVERLAP_OFF 0
