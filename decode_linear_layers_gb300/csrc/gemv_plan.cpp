@@ -300,11 +300,15 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       if (B <= GEMV_MAX_BATCH) p.nb = (B + 15) / 16 * 16;
       const int64_t tiles = ceil_div(M, kTcPlanTileM);
       const int64_t ktiles = K > 0 ? ceil_div(K, (int64_t)kTcPlanTileK * tc_plan_atoms(p.nb)) : 1;
-      // K slices so that all CTAs run in one wave (as many per SM as shared memory allows)
-      // a deep ring (one CTA per SM) while the tiles leave SMs free, else two CTAs
-      // per SM (measured: 14336 rows B = 32 30.7 us with the deep ring against 35.6;
-      // 28672 rows 45.1 us with two CTAs per SM against 57.3)
-      const int ring_kb = tiles < num_sms ? 200 : 100;
+      // K slices so that all CTAs run in one wave (as many per SM as shared memory
+      // allows).  A deep ring (one CTA per SM) for up to 64 vectors while the tiles
+      // cover half the SMs or more but not all of them; otherwise two CTAs per SM,
+      // which for few tiles doubles the K slices (measured, us: 14336 rows B = 32
+      // 30.7 deep against 33.6, B = 64 33.5 against 37.7, B = 128 49.1 against 46.3;
+      // 4096 rows B = 64 23.3 against 21.4; 28672 rows B = 32 57.3 against 45.1)
+      // (forced: param >= 32 is the ring size in KB)
+      const bool deep = p.nb <= 64 && tiles < num_sms && 2 * tiles >= num_sms;
+      const int ring_kb = param >= 32 && param <= 220 ? param : deep ? 200 : 100;
       const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb) * tc_plan_stage_bytes(p.nb) + 1024;
       int64_t per_sm = kSmemPerSm / (smem + 1024);
       if (per_sm < 1) per_sm = 1;

@@ -300,7 +300,8 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
  * (lanes_per_row, rows_per_warp or splits; 0 = the dispatcher's choice) when the
  * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  STREAM needs
  * B == 1; BATCHED needs x[0..B) to fit in shared memory and takes the variant + 1
- * (GEMV_BATCHED_*; the mixed-precision ring only for fp16/bf16).  A forced kernel
+ * (GEMV_BATCHED_*; the mixed-precision ring only for fp16/bf16); TC takes the ring
+ * size in KB (32..220; smaller values keep the dispatcher's choice).  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);

@@ -336,12 +336,18 @@ def test_plan_tensor_cores():
     p = g.plan_for("bf16", 4096, 4096, 32)
     assert p["kernel"] == K["tc"] and p["nb"] == 32 and p["threads"] == 128 and p["grid"] == 32
     # N <= 64: stages of two 64-column atoms (128 + N rows x 256 bytes); 32 row tiles
-    # leave SMs free, so the deep ring: as many stages as fit in 200 KB (at most 8),
-    # + 1024 bytes to align them, one CTA per SM
-    assert p["smem_bytes"] == 5 * (128 + 32) * 256 + 1024
-    # split-K so that all CTAs run in one wave: 4 slices of 8 k-tiles of 128
-    assert p["splits"] == 4 and p["unroll"] == 8 and p["workspace_bytes"] == 4 * 32 * 4096 * 4
-    assert p["grid"] * p["splits"] <= 152
+    # cover less than half the SMs: two CTAs per SM, as many stages as fit in 100 KB
+    # (at most 8), + 1024 bytes to align them
+    assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024
+    # split-K so that all CTAs run in one wave: 8 slices of 4 k-tiles of 128
+    assert p["splits"] == 8 and p["unroll"] == 4 and p["workspace_bytes"] == 8 * 32 * 4096 * 4
+    assert p["grid"] * p["splits"] <= 2 * 152
+    # tiles covering half the SMs or more (but not all), up to 64 vectors: the deep
+    # ring (200 KB, one CTA per SM)
+    p = g.plan_for("bf16", 14336, 4096, 32)
+    assert p["grid"] == 112 and p["splits"] == 1 and p["smem_bytes"] == 5 * (128 + 32) * 256 + 1024
+    p = g.plan_for("bf16", 14336, 4096, 128)  # 128 vectors: two CTAs per SM, 2 K slices
+    assert p["splits"] == 2 and p["smem_bytes"] == 3 * (128 + 128) * 128 + 1024
     p = g.plan_for("f16", 4096, 4096, 17)
     assert p["kernel"] == K["tc"] and p["nb"] == 32
     # at least as many row tiles as SMs: two CTAs per SM, a 100 KB ring
