@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--sweep-iters", type=int, default=30)
+    ap.add_argument("--sweep-iters", type=int, default=100)
     ap.add_argument("--only", default=None, help="sweep only these comma-separated configs")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-configuration sweep (e.g. under ncu); prints one JSON line")
@@ -407,17 +407,20 @@ def sweep(args, torch, g, dev, flush, peak):
         y = torch.empty((w.B, w.M), dtype=out_dtype(torch, w.dtype), device=dev)
         t = time_gemvs(torch, g, [(w, d, y)], flush, args.sweep_iters, 3)[0]
         plan = g.last_plan()
-        med = statistics.median(t)
+        # single event intervals come in steps of about 2 us on GB300, so a median
+        # snaps to a step; the mean over the launches is the figure reported
+        mean = statistics.mean(t)
         ts = sorted(t)
-        gbs = w.qmin_bytes / (med * 1e-3) / 1e9
-        out.append({"config": n, "kernel": plan["kernel_name"], "us_median": round(med * 1e3, 3),
+        gbs = w.qmin_bytes / (mean * 1e-3) / 1e9
+        out.append({"config": n, "kernel": plan["kernel_name"], "us_mean": round(mean * 1e3, 3),
+                    "us_median": round(statistics.median(t) * 1e3, 3),
                     "us_p10": round(ts[len(ts) // 10] * 1e3, 3), "us_p90": round(ts[(9 * len(ts)) // 10] * 1e3, 3),
                     "qmin_bytes": w.qmin_bytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                    "gflops": round(w.flops / (med * 1e-3) / 1e9, 1),
+                    "gflops": round(w.flops / (mean * 1e-3) / 1e9, 1),
                     "roofline_us": round(w.qmin_bytes / (peak * 1e9) * 1e6, 3)})
         if plan["kernel_name"] == "tc":  # a contraction on the tensor cores: its own roofline too
             tp, _ = measured_tensor_peak_tflops()
-            out[-1]["frac_of_tensor_peak"] = round(w.flops / (med * 1e-3) / 1e12 / tp, 4)
+            out[-1]["frac_of_tensor_peak"] = round(w.flops / (mean * 1e-3) / 1e12 / tp, 4)
         del d, y
         torch.cuda.empty_cache()
     return out
@@ -457,7 +460,7 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
             torch.cuda.synchronize()
             if i >= 3:
                 out.append(e0.elapsed_time(e1))
-        return statistics.median(out)
+        return statistics.mean(out)  # event intervals come in ~2 us steps: the mean, not a median
 
     eager_ms = timed(run)
     side = torch.cuda.Stream()
@@ -472,7 +475,7 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
     launches = g.launch_count() - n0
     graph_ms = timed(graph.replay)
     iso = time_gemvs(torch, g, items, flush, iters, 3)
-    iso_ms = sum(statistics.median(t) for t in iso)
+    iso_ms = sum(statistics.mean(t) for t in iso)
     fused = decode_layer_fused(torch, g, dev, items, timed)
     # the same layer with plain launches (no programmatic dependent launch)
     g.set_launch_overlap("off")

@@ -1387,6 +1387,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
       const int64_t c = 32 * j + lane;
       if (c >= nch) continue;
       const uint32_t xc = xs_s + (uint32_t)(c * WB);
+      // int4 with few sums per row group: the chunk's unscaled sums, scaled once
+      // after the chunk (one packed FMA per sum pair instead of scaling every weight)
+      constexpr bool CSC = GRP && !PAIRS;
+      float2 cacc[CSC ? R : 1][CSC ? NA : 1];
+      if constexpr (CSC) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int i = 0; i < NA; ++i) cacc[r][i] = make_float2(0.f, 0.f);
+      }
+      auto sum = [&](int r, int i) -> float2 & {
+        if constexpr (CSC) return cacc[r][i]; else return acc[r][i];
+      };
 #pragma unroll
       for (int w = 0; w < QW; ++w) {
         if constexpr (MODE == kRingMixed) {
@@ -1415,7 +1428,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           Op::quad2(av[r], w, q01[r], q23[r]);
-          if constexpr (GRP) {  // int4: the chunk's group scale, applied to the weights
+          if constexpr (GRP && !CSC) {  // int4: the chunk's group scale, applied to the weights
             q01[r] = __fmul2_rn(q01[r], make_float2(gsc[r], gsc[r]));
             q23[r] = __fmul2_rn(q23[r], make_float2(gsc[r], gsc[r]));
           }
@@ -1440,10 +1453,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-              acc[r][p] = __ffma2_rn(make_float2(q01[r].x, q01[r].x), X[0], acc[r][p]);
-              acc[r][p] = __ffma2_rn(make_float2(q01[r].y, q01[r].y), X[1], acc[r][p]);
-              acc[r][p] = __ffma2_rn(make_float2(q23[r].x, q23[r].x), X[2], acc[r][p]);
-              acc[r][p] = __ffma2_rn(make_float2(q23[r].y, q23[r].y), X[3], acc[r][p]);
+              float2 &t = sum(r, p);
+              t = __ffma2_rn(make_float2(q01[r].x, q01[r].x), X[0], t);
+              t = __ffma2_rn(make_float2(q01[r].y, q01[r].y), X[1], t);
+              t = __ffma2_rn(make_float2(q23[r].x, q23[r].x), X[2], t);
+              t = __ffma2_rn(make_float2(q23[r].y, q23[r].y), X[3], t);
             }
           }
         } else {
@@ -1464,11 +1478,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-              acc[r][b] = __ffma2_rn(q01[r], x01, acc[r][b]);
-              acc[r][b] = __ffma2_rn(q23[r], x23, acc[r][b]);
+              float2 &t = sum(r, b);
+              t = __ffma2_rn(q01[r], x01, t);
+              t = __ffma2_rn(q23[r], x23, t);
             }
           }
         }
+      }
+      if constexpr (CSC) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int i = 0; i < NA; ++i) acc[r][i] = __ffma2_rn(cacc[r][i], make_float2(gsc[r], gsc[r]), acc[r][i]);
       }
     }
     float v[V];

@@ -284,7 +284,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         // stored.  Over rslices K slices (x too large to stage whole): grid.x CTAs per
         // slice, one CTA per SM in all, partial sums [slice][b][m], then a second pass.
         const int xs = v == GEMV_BATCHED_RING_MIXED ? GEMV_X_SMEM : rstage;
-        p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb, dtype == GEMV_DTYPE_W4);
+        p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb, dtype == GEMV_DTYPE_W4, dtype == GEMV_DTYPE_F32);
         p.x_staging = xs;
         p.unroll = 8 / p.rows_per_warp;
         p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes + rextra);

@@ -18,12 +18,18 @@ constexpr int64_t kStreamSmemMax = 96 * 1024;
 constexpr int kBatchedThreads = 512;
 // BATCHED ring kernel: R rows per warp and a per-thread cp.async ring of G = 8 / R
 // steps: 16 warps x 8 slots x 512 bytes after x.  R = 2 for 16 vectors (the
-// accumulators' registers) and for int4 (32 weights per chunk to decode), else 4.
-// SwiGLU: R = 2.
+// accumulators' registers), for int4 with 3 or more vectors (32 weights per chunk to
+// decode) and for fp32 with 4 vectors, else 4 (measured on GB300, event means in us:
+// int4 8192x8192 B = 1 18.8 with R = 4 against 19.6 with R = 2, int4 14336x4096
+// B = 1 16.7 against 18.3, B = 4 33.2 either way; fp32 8192x4096 B = 4 27.0 against
+// 28.6; bf16 14336x4096 B = 4 29.3 against 27.1 and int8 8192x8192 B = 4 32.8
+// against 32.5 keep R = 4).  SwiGLU: R = 2.
 constexpr int64_t kRingSmemMax = 227 * 1024;  // dynamic shared memory one CTA may use
 constexpr int64_t kRingBytes = 16 * 8 * 512;
 constexpr int64_t kRingScaleBytes = 16 * 8 * 32 * 4;  // int4: a group scale per slot
-constexpr int ring_rows(int nb, bool grouped) { return (nb == 16 || grouped) ? 2 : 4; }
+constexpr int ring_rows(int nb, bool grouped, bool a32) {
+  return nb == 16 ? 2 : grouped ? (nb <= 2 ? 4 : 2) : (a32 && nb == 4) ? 2 : 4;
+}
 constexpr int kStreamThreads = 512;
 // 16-byte chunks in flight per lane: warp-per-row and block-per-row kernels.
 constexpr int kUnrollWarpRow = 4;

@@ -239,6 +239,12 @@ def test_plan_batched_staging():
     p = g.plan_for("w4", 8192, 8192, 4)
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 2
     assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + ring + 16 * 1024
+    # one or two vectors of int4 (and fp32 with 4 vectors, 2 rows): rows per warp as measured
+    for B in (1, 2):
+        p = g.plan_for("w4", 14336, 4096, B)
+        assert p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 4 and p["unroll"] == 2
+    p = g.plan_for("f32", 8192, 4096, 4)
+    assert p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 2 and p["unroll"] == 4
 
 
 def test_plan_small_k_lanes():
