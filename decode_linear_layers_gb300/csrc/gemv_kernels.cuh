@@ -771,6 +771,28 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
   }
 }
 
+// NB values per lane summed over the 32 lanes of a warp.  The first log2(NB)
+// steps halve the values each lane carries (it keeps one half and receives the
+// partner's copy of it), the rest are plain xor steps.  Lane l ends with the total
+// of value l >> (5 - log2 NB).
+template <int NB>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
+#pragma unroll
+  for (int h = NB / 2, m = 16; h >= 1; h >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = upper ? v[i] : v[i + h];
+      const float keep = upper ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int m = 16 / NB; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+  return t;
+}
+
 // ------------------------------------------------------------------ k_batched2
 // 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored, with
 // vectors B..NB-1 zero, so the inner loops run over all NB vectors without a
@@ -802,15 +824,33 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   // row groups of R rows dealt to CTAs round-robin: every SM gets an equal share
   int64_t g = blockIdx.x + (int64_t)gridDim.x * warp;
   int64_t base = 0;  // first chunk of the step, the same in every lane of the warp
-  uint4 nxt[U][R];
-#pragma unroll
-  for (int u = 0; u < U; ++u)
+  // the rows of the group being prefetched: this lane's chunk-0 address in each and
+  // which exist, set once per row group
+  const char *nrow[R];
+  uint32_t nlive = 0;
+  auto set_rows = [&](int64_t gg) {
+    nlive = 0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int64_t row = row_of(g, r), c = base + lane + 32 * u;
-      nxt[u][r] = (g < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
-                                                     : make_uint4(0, 0, 0, 0);
+      const int64_t row = row_of(gg, r);
+      const bool ok = gg < groups && row < M;
+      nlive |= (ok ? 1u : 0u) << r;
+      nrow[r] = A + (ok ? row * rowb : 0) + lane * 16;
     }
+  };
+  auto prefetch = [&](uint4 (&dst)[U][R]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool in = base + lane + 32 * u < nch;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        dst[u][r] = (in && (nlive & (1u << r))) ? ld_stream16(nrow[r] + (base + 32 * u) * 16, pol)
+                                                : make_uint4(0, 0, 0, 0);
+    }
+  };
+  set_rows(g);
+  uint4 nxt[U][R];
+  prefetch(nxt);
   pdl_after_prefetch(a);
   {
     const int64_t n16 = (xstride * B) / 16, nz16 = (xstride * NB) / 16;
@@ -838,15 +878,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       const int64_t cb = base + lane;
       ng = g;
       base += 32 * U;
-      if (base >= nch) { ng = g + gstride; base = 0; }
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int64_t row = row_of(ng, r), c = base + lane + 32 * u;
-          nxt[u][r] = (ng < groups && row < M && c < nch) ? ld_stream16(A + row * rowb + c * 16, pol)
-                                                          : make_uint4(0, 0, 0, 0);
-        }
+      if (base >= nch) {
+        ng = g + gstride;
+        base = 0;
+        set_rows(ng);
+      }
+      prefetch(nxt);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = cb + 32 * u;
@@ -864,22 +901,26 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       }
       if (ng != g) break;
     }
+    // the R * NB sums by one reduce-scatter butterfly: lane l ends with sum
+    // l >> (5 - log2 V) (row / NB, vector % NB), replicated over 32 / V lanes
+    constexpr int V = R * NB;
+    constexpr int LOGV = V == 32 ? 5 : V == 16 ? 4 : V == 8 ? 3 : V == 4 ? 2 : 1;
+    static_assert((1 << LOGV) == V, "R * NB must be a power of two up to 32");
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b];
+    const float part = warp_reduce_scatter<V>(v, lane);
+    const int idx = lane >> (5 - LOGV);
+    const bool owner = (lane & ((32 >> LOGV) - 1)) == 0;
     if constexpr (SW) {
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const float s0 = group_sum<32>(acc[0][b]);
-        const float s1 = group_sum<32>(acc[1][b]);
-        if (lane == 0 && b < B) epilogue_swiglu<Op>(a, b, g, s0, s1);
-      }
+      // gate sum b (row 0) sits at lane b * 32 / V, its up sum (row 1) 16 lanes above
+      const float up = __shfl_down_sync(0xffffffffu, part, 16);
+      if (owner && idx < NB && idx < B) epilogue_swiglu<Op>(a, idx, g, part, up);
     } else {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float s = group_sum<32>(acc[r][b]);
-          if (lane == 0 && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, s);
-        }
-      }
+      const int r = idx / NB, b = idx % NB;
+      if (owner && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, part);
     }
     g = ng;
   }
@@ -1099,28 +1140,6 @@ constexpr int kXsThreads = 512;
 constexpr int kXsWarps = kXsThreads / 32;
 constexpr int kXsT = 16;  // rows per barrier (a multiple of P)
 
-// NB values per lane summed over the 32 lanes of a warp.  The first log2(NB)
-// steps halve the values each lane carries (it keeps one half and receives the
-// partner's copy of it), the rest are plain xor steps.  Lane l ends with the total
-// of value l >> (5 - log2 NB).
-template <int NB>
-__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
-#pragma unroll
-  for (int h = NB / 2, m = 16; h >= 1; h >>= 1, m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-      const float send = upper ? v[i] : v[i + h];
-      const float keep = upper ? v[i + h] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-    }
-  }
-  float t = v[0];
-#pragma unroll
-  for (int m = 16 / NB; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
-  return t;
-}
-
 // ------------------------------------------------------------------ k_batch_ring
 // 2 <= B <= 16 (NB in {2, 4, 8, 16}).  One 512-thread CTA per SM, persistent; each
 // warp carries R rows at a time (row groups dealt round-robin over CTAs and warps,
@@ -1209,6 +1228,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
 
   // shared memory: x planes, then the ring [warp][stage][row][lane] of 16-byte slots
   const int64_t pstride = nch * WB;  // bytes per plane
+  const uint32_t ps32 = (uint32_t)pstride;  // shared-memory offsets fit 32 bits
   const int64_t xbytes = (int64_t)(PAIRS ? NP : NB) * PPV * pstride;
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t ring_s = xs_s + (uint32_t)xbytes + (uint32_t)((warp * G * R * 32 + lane) * 16);
@@ -1218,28 +1238,61 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
                         (uint32_t)((warp * G * R * 32 + lane) * 4);
   const int64_t gpr = K >> a.gshift;  // groups per row (int4)
 
-  // producer position: row group pg, step pj (chunks 32 pj + lane)
+  // producer position: row group pg, step pj (chunks 32 pj + lane).  Which rows of
+  // group pg exist is set once per row group; with few vectors (registers to spare)
+  // so are the rows' addresses of this lane's step-0 chunk (and int4 group-scale
+  // rows), and a step costs one add per row.
+  constexpr bool CACHE = NB <= 4;
   int64_t pg = blockIdx.x + (int64_t)gridDim.x * warp, pj = 0;
-  auto issue = [&](int stage) {
-    if (pg < groups) {
-      const int64_t c = 32 * pj + lane;
-      if (c < nch) {
+  const char *pa[CACHE ? R : 1];
+  const float *pscale[CACHE && GRP ? R : 1];
+  uint32_t plive = 0;  // bit r: row r of group pg exists (none once pg >= groups)
+  auto set_rows = [&]() {
+    plive = 0;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int64_t row = row_of(pg, r);
-          if (row < M) {
-            const uint32_t dst = ring_s + (uint32_t)((stage * R + r) * 32 * 16);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(A + row * rowb + c * 16)
-                         : "memory");
-            if constexpr (GRP) {
-              const float *gs = a.gscale + row * gpr + (((c0 + c) * Op::VEC) >> a.gshift);
-              asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sc_s + (uint32_t)((stage * R + r) * 32 * 4)),
-                           "l"(gs) : "memory");
-            }
+    for (int r = 0; r < R; ++r) {
+      const int64_t row = row_of(pg, r);
+      const bool ok = pg < groups && row < M;
+      plive |= (ok ? 1u : 0u) << r;
+      if constexpr (CACHE) {
+        pa[r] = A + (ok ? row * rowb : 0) + lane * 16;
+        if constexpr (GRP) pscale[r] = a.gscale + (ok ? row * gpr : 0);
+      }
+    }
+  };
+  set_rows();
+  auto issue = [&](int stage) {
+    const int64_t c = 32 * pj + lane;
+    if (plive != 0 && c < nch) {
+      const uint32_t dst = ring_s + (uint32_t)(stage * R * 32 * 16);
+      const int64_t aoff = pj * (32 * 16);
+      [[maybe_unused]] int64_t goff = 0;
+      if constexpr (GRP) goff = ((c0 + c) * Op::VEC) >> a.gshift;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (plive & (1u << r)) {
+          const char *src;
+          [[maybe_unused]] const float *gsrc = nullptr;
+          if constexpr (CACHE) {
+            src = pa[r] + aoff;
+            if constexpr (GRP) gsrc = pscale[r] + goff;
+          } else {
+            const int64_t row = row_of(pg, r);
+            src = A + row * rowb + c * 16;
+            if constexpr (GRP) gsrc = a.gscale + row * gpr + goff;
           }
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + (uint32_t)(r * 32 * 16)), "l"(src)
+                       : "memory");
+          if constexpr (GRP)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sc_s + (uint32_t)((stage * R + r) * 32 * 4)),
+                         "l"(gsrc) : "memory");
         }
       }
-      if (++pj == nsteps) { pj = 0; pg += gstride; }
+    }
+    if (pg < groups && ++pj == nsteps) {
+      pj = 0;
+      pg += gstride;
+      set_rows();
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
@@ -1386,7 +1439,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
       stage = stage + 1 == G ? 0 : stage + 1;
       const int64_t c = 32 * j + lane;
       if (c >= nch) continue;
-      const uint32_t xc = xs_s + (uint32_t)(c * WB);
+      const uint32_t xc = xs_s + (uint32_t)c * (uint32_t)WB;
       // int4 with few sums per row group: the chunk's unscaled sums, scaled once
       // after the chunk (one packed FMA per sum pair instead of scaling every weight)
       constexpr bool CSC = GRP && !PAIRS;
@@ -1413,7 +1466,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
           }
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
-            const uint2 h = lds8(xc + (uint32_t)((b * PPV + w) * pstride));
+            const uint2 h = lds8(xc + (uint32_t)(b * PPV + w) * ps32);
             unsigned short xh[4];
             split_halves(h.x, xh[0], xh[1]);
             split_halves(h.y, xh[2], xh[3]);
@@ -1438,14 +1491,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
           for (int p = 0; p < NP; ++p) {
             float2 X[4];
             if constexpr (XE == 4) {
-              const uint4 u0 = lds16(xc + (uint32_t)((p * PPV + 2 * w) * pstride));
-              const uint4 u1 = lds16(xc + (uint32_t)((p * PPV + 2 * w + 1) * pstride));
+              const uint4 u0 = lds16(xc + (uint32_t)(p * PPV + 2 * w) * ps32);
+              const uint4 u1 = lds16(xc + (uint32_t)(p * PPV + 2 * w + 1) * ps32);
               X[0] = make_float2(__uint_as_float(u0.x), __uint_as_float(u0.y));
               X[1] = make_float2(__uint_as_float(u0.z), __uint_as_float(u0.w));
               X[2] = make_float2(__uint_as_float(u1.x), __uint_as_float(u1.y));
               X[3] = make_float2(__uint_as_float(u1.z), __uint_as_float(u1.w));
             } else {
-              const uint4 u = lds16(xc + (uint32_t)((p * PPV + w) * pstride));
+              const uint4 u = lds16(xc + (uint32_t)(p * PPV + w) * ps32);
               X[0] = widen2(u.x, typename Op::TX());
               X[1] = widen2(u.y, typename Op::TX());
               X[2] = widen2(u.z, typename Op::TX());
@@ -1463,7 +1516,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
         } else {
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
-            const uint32_t xa = xc + (uint32_t)((b * PPV + w) * pstride);
+            const uint32_t xa = xc + (uint32_t)(b * PPV + w) * ps32;
             float2 x01, x23;
             if constexpr (XE == 4) {
               const uint4 u = lds16(xa);
