@@ -258,17 +258,31 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // x[0..NB) is staged (vectors B..NB-1 zero): the inner loops have no branch
       p.threads = kBatchedThreads;
       p.grid = num_sms;
-      // variant: forced (param = variant + 1), else the row-pair kernel for 4..16
-      // vectors with at most one row pair per warp (nothing to amortise a ring's
-      // fill on: f16 4096x4096 B = 4 14.3 us against 16.4, bf16 4096x14336 B = 4
-      // 30.7 against 36.9), else the ring, with mixed-precision FMAs for fp16/bf16
-      // with 2 or 9..16 vectors (bf16 14336x4096 B = 16 63.5 us against 65.5 with
-      // packed FMAs and 72.9 in the row-pair kernel; B = 2 24.0 against 26.6) and
-      // packed FMAs otherwise (B = 8 34.8 us against 38.9 mixed and 44.0 row-pair)
+      // variant: forced (param = variant + 1), else the row-pair kernel where it
+      // measured faster (GB300, event means in us, clean-L2 flush), else the ring,
+      // with mixed-precision FMAs for fp16/bf16 with 2 vectors (bf16 14336x4096
+      // B = 2 23.9 against 26.6 packed) and packed FMAs otherwise.  Row pair:
+      // - 4..16 vectors with at most one ring row group per warp, fp32 excepted
+      //   (int8 8192x8192 B = 4 28.6 against 30.7 ring, f16 6144x4096 B = 8 20.6
+      //   against 22.5; fp32 8192x4096 B = 8 32.9 against 30.6 ring);
+      // - 16 vectors of fp16/bf16/fp32 whenever x fits (bf16 14336x4096 53.2 against
+      //   61.4 mixed ring, 128256x4096 409.6 against 450.6, fp32 32768x2048 75.8
+      //   against 82.0; int8 14336x4096 is a tie and keeps the ring);
+      // - 8 vectors of fp16/bf16 whose ring would read x as stored (f16 16384x6144
+      //   53.2 against 59.4; with fp32 x the ring wins at scale: bf16 28672x4096
+      //   55.3 against 59.4);
+      // - x too large for the ring, or for its whole K (the ring's slices).
+      const int64_t ring_group_rows = ring_rows(p.nb, dtype == GEMV_DTYPE_W4, dtype == GEMV_DTYPE_F32);
+      const bool one_group_per_warp = M <= (int64_t)num_sms * 16 * ring_group_rows;
       int v;
       if (param != 0) {
         v = param - 1;
-      } else if (rstage < 0 || (rowpair_ok && (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2)))) {
+      } else if (rstage < 0 ||
+                 (rowpair_ok &&
+                  (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2) ||
+                   (p.nb >= 4 && dtype != GEMV_DTYPE_F32 && one_group_per_warp) ||
+                   (p.nb == 16 && dtype != GEMV_DTYPE_W8) ||
+                   (p.nb == 8 && half16 && rstage == GEMV_X_SMEM)))) {
         v = GEMV_BATCHED_ROWPAIR;
       } else {
         v = (half16 && (p.nb == 16 || p.nb == 2) && mixed_ok) ? GEMV_BATCHED_RING_MIXED : GEMV_BATCHED_RING;

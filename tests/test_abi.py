@@ -156,7 +156,10 @@ def test_plan_config_shapes():
     p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["nb"] == 1
     assert p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["smem_bytes"] == 8192 * 4 + 64 * 1024
-    p = g.plan_for("w8", 8192, 8192, 4)     # the ring: fp32 x (128 KB) + the 64 KB ring
+    p = g.plan_for("w8", 8192, 8192, 4)     # at most one ring row group per warp: the row pairs
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1
+    assert p["rows_per_warp"] == 2 and p["smem_bytes"] == 4 * 8192 * 2
+    p = g.plan_for("w8", 16384, 8192, 4)    # the ring: fp32 x (128 KB) + the 64 KB ring
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["x_staging"] == 2
     assert p["rows_per_warp"] == 4 and p["unroll"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + 64 * 1024
 
@@ -194,9 +197,9 @@ def test_plan_batched_staging():
     K = g.KERNELS
     ring = 64 * 1024
     # the ring: fp32 x when x and the 64 KB ring fit in 227 KB, else x as stored
-    p = g.plan_for("w8", 8192, 8192, 4)
+    p = g.plan_for("w8", 16384, 8192, 4)
     assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + ring
-    p = g.plan_for("bf16", 8192, 16384, 4)
+    p = g.plan_for("bf16", 16384, 16384, 4)
     assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 1 and p["smem_bytes"] == 4 * 16384 * 2 + ring
     assert p["rows_per_warp"] == 4 and p["unroll"] == 2
     # at most one row pair per warp (M <= 2 x 16 warps x 152 SMs) and 4..16 vectors:
@@ -205,16 +208,20 @@ def test_plan_batched_staging():
     assert p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1 and p["smem_bytes"] == 4 * 14336 * 2
     assert g.plan_for("f16", 4096, 4096, 2)["variant"] == g.BATCHED_RING_MIXED
     assert g.plan_for("w8", 4096, 4096, 2)["variant"] == g.BATCHED_RING
-    p = g.plan_for("bf16", 8192, 4096, 8)   # vector pairs, 4 rows per warp, 2-step ring
+    p = g.plan_for("bf16", 16384, 4096, 8)  # vector pairs, 4 rows per warp, 2-step ring
     assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["unroll"] == 2
-    # 9..16 vectors of fp16/bf16: the mixed-precision ring with many rows, the row-pair
-    # kernel with at most one row pair per warp
+    # up to one ring row group per warp (M <= 4 x 16 x 152), fp32 excepted: the row pairs
+    assert g.plan_for("bf16", 8192, 4096, 8)["variant"] == g.BATCHED_ROWPAIR
+    assert g.plan_for("f32", 8192, 4096, 8)["variant"] == g.BATCHED_RING
+    # 8 vectors of fp16/bf16 whose ring would read x as stored (fp32 x 192 KB): row pairs
+    assert g.plan_for("f16", 16384, 6144, 8)["variant"] == g.BATCHED_ROWPAIR
+    # 9..16 vectors of fp16/bf16/fp32 wherever x fits: the row pairs (int8 keeps the ring)
     p = g.plan_for("bf16", 14336, 4096, 16)
-    assert p["variant"] == g.BATCHED_RING_MIXED and p["x_staging"] == 1 and p["smem_bytes"] == 16 * 4096 * 2 + ring
-    p = g.plan_for("f16", 4864, 4096, 9)
-    assert p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 4096 * 2
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1 and p["smem_bytes"] == 16 * 4096 * 2
     p = g.plan_for("f16", 4866, 4096, 9)
-    assert p["variant"] == g.BATCHED_RING_MIXED and p["rows_per_warp"] == 2 and p["unroll"] == 4
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 4096 * 2
+    assert g.plan_for("f32", 32768, 2048, 16)["variant"] == g.BATCHED_ROWPAIR
+    assert g.plan_for("w8", 14336, 4096, 16)["variant"] == g.BATCHED_RING
     # x too large for the ring but within 200 KB: the row-pair kernel
     p = g.plan_for("bf16", 20000, 6144, 16)
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR and p["smem_bytes"] == 16 * 6144 * 2
@@ -233,7 +240,7 @@ def test_plan_batched_staging():
     p = g.plan_for("bf16", 4096, 14336, 4)    # the row-pair kernel's x fits (115 KB)
     assert p["variant"] == g.BATCHED_ROWPAIR and p["splits"] == 1
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors
-    assert g.plan_for("w8", 8192, 4096, 3)["smem_bytes"] == 4 * 4096 * 4 + ring
+    assert g.plan_for("w8", 16384, 4096, 3)["smem_bytes"] == 4 * 4096 * 4 + ring
     assert g.plan_for("f16", 4096, 4096, 9)["smem_bytes"] == 16 * 4096 * 2
     # int4: the ring with a group-scale ring (16 KB) beside it, 2 rows per warp
     p = g.plan_for("w4", 8192, 8192, 4)
