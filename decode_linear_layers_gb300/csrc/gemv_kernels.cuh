@@ -771,6 +771,11 @@ __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const 
   }
 }
 
+// The two 16-bit halves of a word (low half = lower element).
+__device__ __forceinline__ void split_halves(uint32_t w, unsigned short &lo, unsigned short &hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+
 // NB values per lane summed over the 32 lanes of a warp.  The first log2(NB)
 // steps halve the values each lane carries (it keeps one half and receives the
 // partner's copy of it), the rest are plain xor steps.  Lane l ends with the total
@@ -811,6 +816,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   const int64_t M = a.M, K = a.K;
   const int B = a.B;
   constexpr int XB = Op::XCH * 16;  // smem bytes of x per A chunk
+  constexpr bool kMixed16 = sizeof(typename Op::TA) == 2 && sizeof(typename Op::TX) == 2;
   const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
   const uint64_t pol = evict_first_policy();
   const int64_t nch = K / Op::VEC;
@@ -888,14 +894,40 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       for (int u = 0; u < U; ++u) {
         const int64_t c = cb + 32 * u;
         if (c < nch) {
+          if constexpr (kMixed16) {
+            // 16-bit A and x: each A half split out once per row, each x half once
+            // per vector, then one mixed-precision FMA per product, in element order
+            unsigned short ah[R][8];
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            const unsigned char *xp = xs + b * xstride + c * XB;
-            uint4 xv[Op::XCH];
+            for (int r = 0; r < R; ++r) {
+              split_halves(cur[u][r].x, ah[r][0], ah[r][1]);
+              split_halves(cur[u][r].y, ah[r][2], ah[r][3]);
+              split_halves(cur[u][r].z, ah[r][4], ah[r][5]);
+              split_halves(cur[u][r].w, ah[r][6], ah[r][7]);
+            }
 #pragma unroll
-            for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
+            for (int b = 0; b < NB; ++b) {
+              const uint4 xv = *reinterpret_cast<const uint4 *>(xs + b * xstride + c * XB);
+              unsigned short xh[8];
+              split_halves(xv.x, xh[0], xh[1]);
+              split_halves(xv.y, xh[2], xh[3]);
+              split_halves(xv.z, xh[4], xh[5]);
+              split_halves(xv.w, xh[6], xh[7]);
 #pragma unroll
-            for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], cur[u][r], xv);
+              for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) Op::fma_mixed(acc[r][b], ah[r][e], xh[e]);
+            }
+          } else {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              const unsigned char *xp = xs + b * xstride + c * XB;
+              uint4 xv[Op::XCH];
+#pragma unroll
+              for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
+#pragma unroll
+              for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], cur[u][r], xv);
+            }
           }
         }
       }
@@ -1164,11 +1196,6 @@ constexpr int kXsT = 16;  // rows per barrier (a multiple of P)
 //   which lane l holds sum l (row l / NB, vector l % NB, replicated over 32 / (R*NB)
 //   lanes) and runs its epilogue, with the operands it loaded when the group began.
 // SW (R = 2): the two rows are SwiGLU's gate row g and up row g + half.
-
-// The two 16-bit halves of a word (low half = lower element).
-__device__ __forceinline__ void split_halves(uint32_t w, unsigned short &lo, unsigned short &hi) {
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
-}
 
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   uint4 v;
