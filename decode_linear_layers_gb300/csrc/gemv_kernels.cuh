@@ -817,6 +817,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   const int B = a.B;
   constexpr int XB = Op::XCH * 16;  // smem bytes of x per A chunk
   constexpr bool kMixed16 = sizeof(typename Op::TA) == 2 && sizeof(typename Op::TX) == 2;
+  // fp32 and int8 rows with up to 8 vectors: (even, odd) accumulator pairs and packed
+  // FMAs (int8 with the packed magic-number decode); 16 vectors keep one accumulator
+  constexpr bool kF32 = sizeof(typename Op::TA) == 4;
+  constexpr bool kPacked = (kF32 || (sizeof(typename Op::TA) == 1 && !Op::GROUPED)) && NB <= 8;
   const int64_t xstride = K * (int64_t)sizeof(typename Op::TX);
   const uint64_t pol = evict_first_policy();
   const int64_t nch = K / Op::VEC;
@@ -870,10 +874,17 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 
   while (g < groups) {
     float acc[R][NB];
+    float2 acc2[kPacked ? R : 1][kPacked ? NB : 1];  // kPacked: (even, odd) element sums
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+    if constexpr (kPacked) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc2[r][b] = make_float2(0.f, 0.f);
+    }
     int64_t ng;
     for (;;) {
       uint4 cur[U][R];
@@ -926,7 +937,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 #pragma unroll
               for (int h = 0; h < Op::XCH; ++h) xv[h] = reinterpret_cast<const uint4 *>(xp)[h];
 #pragma unroll
-              for (int r = 0; r < R; ++r) Op::dot1(acc[r][b], cur[u][r], xv);
+              for (int r = 0; r < R; ++r) {
+                if constexpr (kPacked && kF32) {
+                  const uint4 &av = cur[u][r];
+                  acc2[r][b] = __ffma2_rn(make_float2(__uint_as_float(av.x), __uint_as_float(av.y)),
+                                          make_float2(__uint_as_float(xv[0].x), __uint_as_float(xv[0].y)), acc2[r][b]);
+                  acc2[r][b] = __ffma2_rn(make_float2(__uint_as_float(av.z), __uint_as_float(av.w)),
+                                          make_float2(__uint_as_float(xv[0].z), __uint_as_float(xv[0].w)), acc2[r][b]);
+                } else if constexpr (kPacked) {
+                  Op::dot(acc2[r][b].x, acc2[r][b].y, cur[u][r], xv);  // int8: packed decode and FMAs
+                } else {
+                  Op::dot1(acc[r][b], cur[u][r], xv);
+                }
+              }
             }
           }
         }
@@ -942,7 +965,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b];
+      for (int b = 0; b < NB; ++b) v[r * NB + b] = kPacked ? acc2[r][b].x + acc2[r][b].y : acc[r][b];
     const float part = warp_reduce_scatter<V>(v, lane);
     const int idx = lane >> (5 - LOGV);
     const bool owner = (lane & ((32 >> LOGV) - 1)) == 0;
