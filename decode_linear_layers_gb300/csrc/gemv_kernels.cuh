@@ -17,7 +17,8 @@
 //               kernel), optionally over one K slice of it (split-K pass 1).
 //   k_splitk_reduce  split-K pass 2: sums the slices in slice order.
 //   k_batched2  2 <= B <= 16 (row pairs): x in shared memory as stored, 2 rows per
-//               warp, the next loads in registers, mixed-precision FMAs.
+//               warp, the next loads in registers; mixed-precision FMAs for 16-bit
+//               rows, packed FMAs for int8/fp32 rows with up to 8 vectors.
 //   k_batch_ring  2 <= B <= 16: A through a per-thread cp.async ring, x in shared
 //               memory (fp32 where it fits), R rows per warp, packed FMAs.
 //   k_xsplit    B <= 4: the CTA splits K, x in fp32 registers.
@@ -799,13 +800,15 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NB], int lane) {
 }
 
 // ------------------------------------------------------------------ k_batched2
-// 5 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored, with
+// 2 <= B <= 16.  x[0..B) copied once per CTA into shared memory as stored, with
 // vectors B..NB-1 zero, so the inner loops run over all NB vectors without a
 // branch.  Each warp carries R rows and takes U chunks of each per step; the
 // next step's loads (possibly of the warp's next row group) are in flight while
 // the current step is used.  Every x chunk read from shared memory feeds R rows.
-// One fp32 accumulator per (row, vector); mixed-precision FMAs (16-bit operands,
-// fp32 accumulator) for the 16-bit types.
+// fp16/bf16: one fp32 accumulator per (row, vector) and mixed-precision FMAs (16-bit
+// operands, fp32 accumulator).  int8/fp32 with up to 8 vectors: an (even, odd) fp32
+// pair per (row, vector) and packed FMAs; with 16, one accumulator and scalar FMAs.
+// The R * NB sums meet in one reduce-scatter butterfly.
 template <class Op, int NB, int R, int U, int THREADS, bool SW = false>
 __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
   pdl_enter(a, true);
