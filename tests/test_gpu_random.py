@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 VEC = {"f32": 4, "f16": 8, "bf16": 8, "w8": 16, "w4": 32}
 
 
-def _cases(n=96, seed=2027):
+def _cases(n=192, seed=2027):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
