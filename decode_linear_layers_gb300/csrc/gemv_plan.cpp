@@ -184,16 +184,25 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // more vectors the ring kernel is faster, with one vector the streaming one)
       kernel = GEMV_KERNEL_XSPLIT;
     } else if ((B > 1 || ((dtype == GEMV_DTYPE_W8 || dtype == GEMV_DTYPE_W4) && rslices == 1 &&
-                          M >= (int64_t)num_sms * 16 && M < 65536)) &&
+                          M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_W8 ? 48 : 16) && M < 65536)) &&
                batched_ok && nch >= 32) {
       // (one vector of int8 or int4 weights too: the decode-bound rows gain from the
-      // ring's deeper prefetch and fp32 x; int8 8192x8192 18.8 us against 20.3 in the
-      // streaming kernel, int4 20.5 against 22.6)
+      // ring's deeper prefetch and fp32 x; int8 8192x8192 18.4 us against 20.4 in the
+      // streaming kernel, int4 20.5 against 22.6.  int8 with fewer than 48 rows per SM
+      // leaves most ring warps without a row group: 4096x16384 20.5 us streaming
+      // against 22.5, 4096x28672 30.2 against 33.3, 4096x8192 a tie)
       kernel = GEMV_KERNEL_BATCHED;
     } else if (M >= 65536) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;
     } else if (B == 1 && M >= (int64_t)num_sms * 16) {
-      kernel = GEMV_KERNEL_STREAM;
+      // fp32 rows of 8192 or more elements whose row walk would leave the streaming
+      // warps unbalanced (rows per warp well short of a whole number): one warp per row
+      // instead (4096x8192 29.2 us against 35.0, 12288x8192 67.4 against 73.5,
+      // 4096x32768 90.5 against 122.6; 8192x8192 and 16384x4096 stream)
+      const int64_t walkers = (int64_t)num_sms * 4 * (kStreamThreads / 32);  // 4 fp32 CTAs per SM
+      const int64_t turns = ceil_div(M, walkers);
+      const bool unbalanced = dtype == GEMV_DTYPE_F32 && nch >= 2048 && 4 * M < 3 * turns * walkers;
+      kernel = unbalanced ? GEMV_KERNEL_WARP_PER_ROW : GEMV_KERNEL_STREAM;
     } else if (M >= (int64_t)num_sms * 16 || nch <= kPlanThreads) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;  // many rows, or rows of at most 4 KB
     } else if (M >= (int64_t)num_sms * 2 || nch < 2 * kPlanThreads) {

@@ -153,6 +153,12 @@ def test_plan_config_shapes():
         assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["stream"]
     p = g.plan_for("bf16", 128256, 4096, 1)
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
+    # one vector of fp32 on long rows the streaming warps would share unevenly: warp per row
+    assert g.plan_for("f32", 4096, 8192, 1)["kernel"] == K["warp_per_row"]
+    assert g.plan_for("f32", 12288, 8192, 1)["kernel"] == K["warp_per_row"]
+    assert g.plan_for("f32", 8192, 8192, 1)["kernel"] == K["stream"]
+    # one vector of int8 with fewer than 48 rows per SM: the streaming kernel
+    assert g.plan_for("w8", 4096, 16384, 1)["kernel"] == K["stream"]
     p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["nb"] == 1
     assert p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["smem_bytes"] == 8192 * 4 + 64 * 1024
