@@ -178,10 +178,17 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       kernel = GEMV_KERNEL_SCALAR;
     } else if (nch <= 16) {
       kernel = GEMV_KERNEL_ROWS_PER_WARP;
-    } else if (xs_ok && dtype == GEMV_DTYPE_F32 && B == 2 && M >= (int64_t)num_sms * 16 && M < 65536) {
+    } else if (xs_ok && dtype == GEMV_DTYPE_F32 && B == 1 && M >= (int64_t)num_sms * 8 && M <= 12288) {
+      // fp32, one vector, up to 12288 rows of at most 8192 elements: the K-split kernel
+      // (4096x4096 16.4 us against 20.6 streaming, 4096x8192 24.9 against 29.4 warp
+      // per row, 8192x8192 43.4 against 47.6, 12288x8192 62.5 against 69.2,
+      // 2048x8192 16.4 against 22.6)
+      kernel = GEMV_KERNEL_XSPLIT;
+    } else if (xs_ok && dtype == GEMV_DTYPE_F32 && B == 2 && M >= (int64_t)num_sms * 8 && M < 65536) {
       // fp32 with 2 vectors: K split over a CTA, x in registers (measured: fp32
-      // 8192x4096 26.6 us against 28.7 in the ring kernel; for 16-bit types and
-      // more vectors the ring kernel is faster, with one vector the streaming one)
+      // 8192x4096 26.6 us against 28.7 in the ring kernel, 2048x8192 16.7 against
+      // 28.8; for 16-bit types and more vectors the ring kernel is faster, with one
+      // vector the streaming one)
       kernel = GEMV_KERNEL_XSPLIT;
     } else if ((B > 1 || ((dtype == GEMV_DTYPE_W8 || dtype == GEMV_DTYPE_W4) && rslices == 1 &&
                           M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_W8 ? 48 : 16) && M < 65536)) &&
@@ -194,7 +201,9 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       kernel = GEMV_KERNEL_BATCHED;
     } else if (M >= 65536) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;
-    } else if (B == 1 && M >= (int64_t)num_sms * 16) {
+    } else if (B == 1 && M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_F32 ? 16 : 12)) {
+      // (16-bit and int8 rows stream from 12 rows per SM: bf16 2048x8192 12.4 us
+      // against 14.2 block per row, int8 10.3 against 12.3)
       // fp32 rows of 8192 or more elements whose row walk would leave the streaming
       // warps unbalanced (rows per warp well short of a whole number): one warp per row
       // instead (4096x8192 29.2 us against 35.0, 12288x8192 67.4 against 73.5,
@@ -271,9 +280,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // measured faster (GB300, event means in us, clean-L2 flush), else the ring,
       // with mixed-precision FMAs for fp16/bf16 with 2 vectors (bf16 14336x4096
       // B = 2 23.9 against 26.6 packed) and packed FMAs otherwise.  Row pair:
-      // - 4..16 vectors with at most one ring row group per warp, fp32 excepted
-      //   (int8 8192x8192 B = 4 28.6 against 30.7 ring, f16 6144x4096 B = 8 20.6
-      //   against 22.5; fp32 8192x4096 B = 8 32.9 against 30.6 ring);
+      // - 4..16 vectors (int8: 2..16) with at most one ring row group per warp, fp32
+      //   excepted (int8 8192x8192 B = 4 28.6 against 30.7 ring, 4096x4096 B = 2 10.3
+      //   against 12.3, f16 6144x4096 B = 8 20.6 against 22.5; fp32 8192x4096 B = 8
+      //   32.9 against 30.6 ring);
       // - 16 vectors of fp16/bf16/fp32 whenever x fits (bf16 14336x4096 53.2 against
       //   61.4 mixed ring, 128256x4096 409.6 against 450.6, fp32 32768x2048 75.8
       //   against 82.0; int8 14336x4096 is a tie and keeps the ring);
@@ -289,7 +299,8 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       } else if (rstage < 0 ||
                  (rowpair_ok &&
                   (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2) ||
-                   (p.nb >= 4 && dtype != GEMV_DTYPE_F32 && one_group_per_warp) ||
+                   ((p.nb >= 4 || (dtype == GEMV_DTYPE_W8 && p.nb >= 2)) && dtype != GEMV_DTYPE_F32 &&
+                    one_group_per_warp) ||
                    (p.nb == 16 && dtype != GEMV_DTYPE_W8) ||
                    (p.nb == 8 && half16 && rstage == GEMV_X_SMEM)))) {
         v = GEMV_BATCHED_ROWPAIR;

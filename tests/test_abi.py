@@ -154,9 +154,15 @@ def test_plan_config_shapes():
     p = g.plan_for("bf16", 128256, 4096, 1)
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
     # one vector of fp32 on long rows the streaming warps would share unevenly: warp per row
-    assert g.plan_for("f32", 4096, 8192, 1)["kernel"] == K["warp_per_row"]
-    assert g.plan_for("f32", 12288, 8192, 1)["kernel"] == K["warp_per_row"]
-    assert g.plan_for("f32", 8192, 8192, 1)["kernel"] == K["stream"]
+    assert g.plan_for("f32", 4096, 32768, 1)["kernel"] == K["warp_per_row"]
+    # ... and up to 12288 rows of at most 8192 elements: the K-split kernel
+    for M in (2048, 4096, 8192, 12288):
+        assert g.plan_for("f32", M, 8192, 1)["kernel"] == K["xsplit"]
+    assert g.plan_for("f32", 16384, 4096, 1)["kernel"] == K["stream"]
+    # one vector of 16-bit or int8 rows from 12 rows per SM: the streaming kernel
+    assert g.plan_for("bf16", 2048, 8192, 1)["kernel"] == K["stream"]
+    # fp32 with 2 vectors from 8 rows per SM: the K-split kernel
+    assert g.plan_for("f32", 2048, 8192, 2)["kernel"] == K["xsplit"]
     # one vector of int8 with fewer than 48 rows per SM: the streaming kernel
     assert g.plan_for("w8", 4096, 16384, 1)["kernel"] == K["stream"]
     p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp
@@ -213,7 +219,8 @@ def test_plan_batched_staging():
     p = g.plan_for("bf16", 4096, 14336, 4)
     assert p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1 and p["smem_bytes"] == 4 * 14336 * 2
     assert g.plan_for("f16", 4096, 4096, 2)["variant"] == g.BATCHED_RING_MIXED
-    assert g.plan_for("w8", 4096, 4096, 2)["variant"] == g.BATCHED_RING
+    assert g.plan_for("w8", 4096, 4096, 2)["variant"] == g.BATCHED_ROWPAIR  # up to one ring group per warp
+    assert g.plan_for("w8", 14336, 4096, 2)["variant"] == g.BATCHED_RING
     p = g.plan_for("bf16", 16384, 4096, 8)  # vector pairs, 4 rows per warp, 2-step ring
     assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["unroll"] == 2
     # up to one ring row group per warp (M <= 4 x 16 x 152), fp32 excepted: the row pairs

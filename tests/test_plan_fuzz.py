@@ -67,7 +67,8 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
         assert B >= 2 or dtype in ("w8", "w4"), p
         v = p["variant"]
         assert v in (g.BATCHED_ROWPAIR, g.BATCHED_RING, g.BATCHED_RING_MIXED)
-        assert p["threads"] == 512 and p["grid"] * p["splits"] <= sms
+        # one CTA per SM in all, unless x needs more K slices than the device has SMs
+        assert p["threads"] == 512 and p["grid"] * p["splits"] <= max(sms, p["splits"])
         if v == g.BATCHED_ROWPAIR:
             assert dtype != "w4" and p["splits"] == 1 and p["smem_bytes"] == p["nb"] * K * SX[dtype]
         else:
@@ -96,7 +97,7 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
     elif kern == K_["stream"]:
         assert B == 1 and p["threads"] == 512
     elif kern == K_["xsplit"]:
-        assert dtype == "f32" and B == 2 and p["smem_bytes"] == 128 * 1024
+        assert dtype == "f32" and B in (1, 2) and p["smem_bytes"] == 128 * 1024
     elif kern == K_["scalar"]:
         assert p["lanes_per_row"] in (4, 32)
     else:
