@@ -92,3 +92,16 @@ def test_inputs_are_seeded_and_shaped():
     assert int(a["A"].min()) >= -127 and int(a["A"].max()) <= 127
     s = a["scale"].numpy()
     assert s.min() >= 1e-3 and s.max() <= 1e-2
+
+
+def test_traffic_record_matches_kernel_sources():
+    # profiles/traffic.txt carries the ncu DRAM traffic of the benchmark's dominant
+    # kernel for the kernel sources it was captured from; the record must be for the
+    # sources as committed (else the benchmark reports traffic as unknown), and the
+    # captured bytes must be the workload's Q_min within a few percent (no re-reads)
+    import bench
+
+    t = bench.read_traffic("f32_16384x4096_b1_bias")
+    assert t is not None, "profiles/traffic.txt was captured from other kernel sources"
+    q = W.BY_NAME["f32_16384x4096_b1_bias"].qmin_bytes
+    assert 0.99 * q <= t <= 1.03 * q, (t, q)
