@@ -190,6 +190,13 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 28.8; for 16-bit types and more vectors the ring kernel is faster, with one
       // vector the streaming one)
       kernel = GEMV_KERNEL_XSPLIT;
+    } else if (xs_ok && K >= 8192 && M >= num_sms &&
+               ((half16 && B == 2 && M <= 4096) || (dtype == GEMV_DTYPE_F32 && B == 4 && M <= 8192))) {
+      // long rows, few of them: the K-split kernel for 2 fp16/bf16 vectors (bf16
+      // 1024x16384 14.4 us against 20.5 in the mixed ring, 4096x14336 25.2 against
+      // 26.6) and 4 fp32 vectors (8192x8192 46.4 against 52.1 in the ring, 2048x8192
+      // 18.5 against 28.5 in the row pairs)
+      kernel = GEMV_KERNEL_XSPLIT;
     } else if ((B > 1 || ((dtype == GEMV_DTYPE_W8 || dtype == GEMV_DTYPE_W4) && rslices == 1 &&
                           M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_W8 ? 48 : 16) && M < 65536)) &&
                batched_ok && nch >= 32) {
@@ -204,13 +211,13 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
     } else if (B == 1 && M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_F32 ? 16 : 12)) {
       // (16-bit and int8 rows stream from 12 rows per SM: bf16 2048x8192 12.4 us
       // against 14.2 block per row, int8 10.3 against 12.3)
-      // fp32 rows of 8192 or more elements whose row walk would leave the streaming
+      // fp32 rows of 4096 or more elements whose row walk would leave the streaming
       // warps unbalanced (rows per warp well short of a whole number): one warp per row
-      // instead (4096x8192 29.2 us against 35.0, 12288x8192 67.4 against 73.5,
-      // 4096x32768 90.5 against 122.6; 8192x8192 and 16384x4096 stream)
+      // instead (14336x4096 38.9 us against 41.4, 4096x32768 90.5 against 122.6;
+      // 16384x4096 streams)
       const int64_t walkers = (int64_t)num_sms * 4 * (kStreamThreads / 32);  // 4 fp32 CTAs per SM
       const int64_t turns = ceil_div(M, walkers);
-      const bool unbalanced = dtype == GEMV_DTYPE_F32 && nch >= 2048 && 4 * M < 3 * turns * walkers;
+      const bool unbalanced = dtype == GEMV_DTYPE_F32 && nch >= 1024 && 4 * M < 3 * turns * walkers;
       kernel = unbalanced ? GEMV_KERNEL_WARP_PER_ROW : GEMV_KERNEL_STREAM;
     } else if (M >= (int64_t)num_sms * 16 || nch <= kPlanThreads) {
       kernel = GEMV_KERNEL_WARP_PER_ROW;  // many rows, or rows of at most 4 KB

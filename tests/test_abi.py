@@ -155,6 +155,11 @@ def test_plan_config_shapes():
     assert p["kernel"] == K["warp_per_row"] and p["grid"] == 152 * 32
     # one vector of fp32 on long rows the streaming warps would share unevenly: warp per row
     assert g.plan_for("f32", 4096, 32768, 1)["kernel"] == K["warp_per_row"]
+    assert g.plan_for("f32", 14336, 4096, 1)["kernel"] == K["warp_per_row"]
+    # long rows, few of them: the K-split kernel for 2 16-bit or 4 fp32 vectors
+    assert g.plan_for("bf16", 1024, 16384, 2)["kernel"] == K["xsplit"]
+    assert g.plan_for("f32", 8192, 8192, 4)["kernel"] == K["xsplit"]
+    assert g.plan_for("bf16", 4096, 4096, 2)["kernel"] == K["batched"]
     # ... and up to 12288 rows of at most 8192 elements: the K-split kernel
     for M in (2048, 4096, 8192, 12288):
         assert g.plan_for("f32", M, 8192, 1)["kernel"] == K["xsplit"]

@@ -97,7 +97,7 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
     elif kern == K_["stream"]:
         assert B == 1 and p["threads"] == 512
     elif kern == K_["xsplit"]:
-        assert dtype == "f32" and B in (1, 2) and p["smem_bytes"] == 128 * 1024
+        assert (dtype == "f32" and B in (1, 2, 4)) or (half16 and B == 2)
     elif kern == K_["scalar"]:
         assert p["lanes_per_row"] in (4, 32)
     else:
