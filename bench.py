@@ -1,21 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of libgemv on GB300: achieved HBM GB/s (cold L2) and % of the measured peak.
 
-One step = one pass of the fp32 workload with bias at M = 16384 over K in
-{16, 32, 4096}: three GEMVs back to back, inputs resident in HBM, L2 flushed
-(a write, then a read, of twice the L2 size) before every GEMV.  Each GEMV is timed with CUDA
-events on the stream it runs on; the step time is the sum of the three.
+One step = one GEMV of the largest single-GPU configuration: bf16 y = A.x with A
+128256 x 4096 (1.05 GB of weights, the Llama-3 vocabulary projection), one vector,
+no bias.  Inputs are resident in HBM; L2 is flushed (a write, then a read, of
+twice the L2 size) before every GEMV; each GEMV is timed with CUDA events on the
+stream it runs on.
 
-    value      = sum of Q_min bytes of the step / step time   (GB/s, whole job)
-    Q_min      = M*K*s_A + B*K*s_x + B*M*s_y                 (per GEMV)
-    roofline   = the K = 4096 GEMV (the dominant kernel): its Q_min / its mean
-                 event time, against the measured HBM copy bandwidth
+    value      = Q_min of the step / mean step time            (GB/s, whole job)
+    Q_min      = M*K*s_A + B*K*s_x + B*M*s_y                   (per GEMV)
+    roofline   = the step's kernel: its Q_min / its mean event time, against the
+                 measured HBM copy bandwidth; traffic = DRAM bytes read + written
+                 per launch from a committed ncu capture of the same kernel source
     e2e        = the same metric through gemv_host (the C-ABI call on host buffers):
-                 A, x, bias copied in from pinned host memory and y copied back,
+                 A and x copied in from pinned host memory and y copied back,
                  inside the timed region, every step
-    cpu_baseline = the CPU oracle on the same step, on the host's cores
+    cpu_baseline = the CPU oracle on the same GEMV, on all host cores and on one
+    fp32_step  = the fp32 configurations with bias at M = 16384 over K in
+                 {16, 32, 4096}: three GEMVs, timed the same way
     sweep      = every configuration at its full size, timed the same way, plus
-                 the int4 (group-scaled) workloads
+                 the int4 and tensor-core workloads, with the vendor library's
+                 time for the same product (torch.matmul, i.e. cuBLAS) beside
+                 the floating-point ones without bias
     decode_layer = a Llama-3-8B-shaped bf16 layer's four GEMVs, eager and from a
                  CUDA graph, and again with the residual adds and SwiGLU fused
                  into the GEMV epilogues
@@ -31,6 +37,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -47,10 +54,11 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # the kernel code and its launch configuration: the DRAM traffic of a committed
-# ncu capture is reported only while these are unchanged
+# ncu capture is reported only while their code (comments aside) is unchanged
 KERNEL_SOURCES = ["gemv_kernels.cuh", "gemv_launch.cuh", "gemv_plan.cpp"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
-HEADLINE_DESC = "f32 GEMV + bias at M=16384 over K in {16, 32, 4096}: 3 GEMVs per step"
+HEADLINE_DESC = "bf16 GEMV y = A.x, A 128256x4096 row-major (1.05 GB), B = 1, no bias: 1 GEMV per step"
+FP32_STEP_DESC = "f32 GEMV + bias at M=16384 over K in {16, 32, 4096}: 3 GEMVs per step"
 
 
 def parse_args(argv=None):
@@ -92,11 +100,19 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed: what the
+    compiler sees, so that an edit to a comment does not change the hash."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_linear_layers_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "decode_linear_layers_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -284,10 +300,7 @@ def run_ours(args, rank, world, local_rank):
 
     head = [W.BY_NAME[n] for n in W.HEADLINE]
     host_inputs = [W.make_inputs(w) for w in head]
-    items = []
-    for w, inp in zip(head, host_inputs):
-        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
-        items.append((w, d, torch.empty((w.B, w.M), dtype=out_dtype(torch, w.dtype), device=dev)))
+    items = device_items(torch, dev, head, host_inputs)
 
     # ---- device-resident timed region (the clock sampler starts before the warm-up,
     # so that starting nvidia-smi does not land in a timed launch)
@@ -328,35 +341,10 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end: host buffers, copies inside the timed region
     e2e = None
     if rank == 0 or world > 1:
-        pinned = []
-        for (w, d, y), inp in zip(items, host_inputs):
-            hp = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
-            hy = torch.empty((w.B, w.M), dtype=y.dtype).pin_memory()
-            pinned.append((hp, hy))
-        h2d = sum(sum(v.numel() * v.element_size() for v in hp.values() if v is not None) for hp, _ in pinned)
-        d2h = sum(hy.numel() * hy.element_size() for _, hy in pinned)
-        e2e_steps = max(3, min(args.steps, 50))
+        e2e = end_to_end(args, torch, g, items, host_inputs, barrier, allmax, world)
 
-        def e2e_step():
-            # the library's host-buffer call: it copies A, scale, x, bias in, runs the
-            # GEMV and copies y out (one cudaMemcpyAsync per buffer), all on the stream
-            for (w, d, y), (hp, hy) in zip(items, pinned):
-                g.gemv_host(w.dtype, hp["A"], hp["scale"], hp["x"], hp["bias"], hy,
-                            d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
-
-        for _ in range(2):
-            e2e_step()
-        barrier()
-        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s_ev.record()
-        for _ in range(e2e_steps):
-            e2e_step()
-        e_ev.record()
-        torch.cuda.synchronize()
-        e2e_ms = allmax(s_ev.elapsed_time(e_ev) / e2e_steps)
-        e2e = {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "steps": e2e_steps}
+    # ---- the fp32 three-GEMV step (rows per warp, warp per row, long rows)
+    fp32 = fp32_step(args, torch, g, dev, flush, peak)
 
     if rank != 0:
         if pg is not None:
@@ -367,11 +355,9 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded PCG64: A ~ N(0, 1/K), x ~ N(0, 1), bias ~ N(0, 1))",
-        "config": {"workload": HEADLINE_DESC, "M": 16384, "K": [16, 32, 4096], "B": 1, "bias": True,
-                   "dtype": "f32", "l2": "flushed before every GEMV (write then read of a 2x L2 buffer)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64: A ~ N(0, 0.02^2), x ~ N(0, 1), rounded to bf16)",
+        "config": headline_config(world),
         "per_gemv_us": {w.name: round(t * 1e3, 3) for w, t in zip(head, per_gemv_ms)},
         # the distribution behind each mean: one slow launch moves a mean of 200
         "per_gemv_us_median": {w.name: round(statistics.median(t) * 1e3, 3) for w, t in zip(head, times)},
@@ -379,6 +365,7 @@ def run_ours(args, rank, world, local_rank):
         "per_gemv_kernel": {w.name: p["kernel_name"] for w, p in zip(head, plans)},
         "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed_region": round(t1 - t0, 3),
+        "fp32_step": fp32,
     }
 
     if not args.no_sweep:
@@ -390,6 +377,70 @@ def run_ours(args, rank, world, local_rank):
     if pg is not None:
         pg.barrier()
     return line
+
+
+def device_items(torch, dev, ws, host_inputs):
+    """(workload, device inputs, device y) per workload."""
+    items = []
+    for w, inp in zip(ws, host_inputs):
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        items.append((w, d, torch.empty((w.B, w.M), dtype=out_dtype(torch, w.dtype), device=dev)))
+    return items
+
+
+def end_to_end(args, torch, g, items, host_inputs, barrier, allmax, world):
+    """The step through gemv_host: every input copied in from pinned host memory and
+    y copied back to it, inside the timed region (one CUDA-event interval over all
+    steps)."""
+    pinned = []
+    for (w, d, y), inp in zip(items, host_inputs):
+        hp = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+        hy = torch.empty((w.B, w.M), dtype=y.dtype).pin_memory()
+        pinned.append((hp, hy))
+    h2d = sum(sum(v.numel() * v.element_size() for v in hp.values() if v is not None) for hp, _ in pinned)
+    d2h = sum(hy.numel() * hy.element_size() for _, hy in pinned)
+    steps = max(3, min(args.steps, 50))
+    step_bytes = sum(w.qmin_bytes for (w, _, _) in items)
+
+    def e2e_step():
+        # the library's host-buffer call: it copies A, scale, x, bias in, runs the
+        # GEMV and copies y out (one cudaMemcpyAsync per buffer), all on the stream
+        for (w, d, y), (hp, hy) in zip(items, pinned):
+            g.gemv_host(w.dtype, hp["A"], hp["scale"], hp["x"], hp["bias"], hy,
+                        d["A"], d["scale"], d["x"], d["bias"], y, w.M, w.K, w.B)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record()
+    for _ in range(steps):
+        e2e_step()
+    e_ev.record()
+    torch.cuda.synchronize()
+    ms = allmax(s_ev.elapsed_time(e_ev) / steps)
+    return {"value": round(whole_job_gbs(world, step_bytes, ms), 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "steps": steps}
+
+
+def fp32_step(args, torch, g, dev, flush, peak):
+    """The three fp32 GEMVs with bias at M = 16384 (K = 16, 32, 4096), each timed
+    like the headline: Q_min of the three over the sum of their mean times."""
+    ws = [W.BY_NAME[n] for n in W.FP32_STEP]
+    items = device_items(torch, dev, ws, [W.make_inputs(w) for w in ws])
+    times = time_gemvs(torch, g, items, flush, max(20, min(args.steps, 200)), 3)
+    means = [statistics.mean(t) for t in times]
+    kernels = []
+    for (w, d, y) in items:
+        call_gemv(g, w, d, y)
+        kernels.append(g.last_plan()["kernel_name"])
+    nbytes = sum(w.qmin_bytes for w in ws)
+    gbs = nbytes / (sum(means) * 1e-3) / 1e9
+    return {"workload": FP32_STEP_DESC, "value": round(gbs, 2), "unit": UNIT,
+            "ms_per_step": round(sum(means), 5), "frac_of_peak": round(gbs / peak, 4),
+            "per_gemv_us": {w.name: round(t * 1e3, 3) for w, t in zip(ws, means)},
+            "per_gemv_kernel": {w.name: k for w, k in zip(ws, kernels)}}
 
 
 def sweep(args, torch, g, dev, flush, peak):
@@ -421,9 +472,33 @@ def sweep(args, torch, g, dev, flush, peak):
         if plan["kernel_name"] == "tc":  # a contraction on the tensor cores: its own roofline too
             tp, _ = measured_tensor_peak_tflops()
             out[-1]["frac_of_tensor_peak"] = round(w.flops / (mean * 1e-3) / 1e12 / tp, 4)
+        if w.dtype in ("f32", "f16", "bf16") and not w.bias:
+            # context: the vendor library's time for the same product on the same
+            # tensors (torch.matmul -> cuBLAS), timed the same way
+            out[-1]["torch_linear_us"] = round(library_linear_us(torch, d, y, flush, args.sweep_iters) * 1e3, 3)
         del d, y
         torch.cuda.empty_cache()
     return out
+
+
+def library_linear_us(torch, d, y, flush, iters):
+    """Mean CUDA-event time (ms) of the vendor library's product y = x A^T (B x M)
+    on the same device tensors (torch.matmul into y: cuBLAS), L2 flushed before
+    each call."""
+    x, A = d["x"], d["A"]
+    for _ in range(3):
+        l2_flush(flush)
+        torch.matmul(x, A.t(), out=y)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    stream = torch.cuda.current_stream()
+    for e0, e1 in ev:
+        l2_flush(flush)
+        e0.record(stream)
+        torch.matmul(x, A.t(), out=y)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 # A Llama-3-8B-shaped decode layer (bf16, one token): fused QKV, output
@@ -540,25 +615,58 @@ def decode_layer_fused(torch, g, dev, items, timed):
             "graph_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
-def cpu_baseline(head, host_inputs, budget_s=10.0):
-    """The oracle (as it stands) on the same step, on all host cores."""
+def headline_config(world: int) -> dict:
+    """The `config` object of both arms' lines (the same workload, the same keys)."""
+    w = W.BY_NAME[W.HEADLINE[0]]
+    return {"workload": HEADLINE_DESC, "M": w.M, "K": w.K, "B": w.B, "bias": w.bias, "dtype": w.dtype,
+            "l2": "flushed before every GEMV (write then read of a 2x L2 buffer)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+def oracle_rate(ws, inputs, nthreads, budget_s, max_reps=50, rows=None):
+    """GB/s (over Q_min) of the oracle on the workloads, on the first `rows` rows of
+    each (all rows if None), repeated until `budget_s` seconds have passed."""
     import oracle
 
-    cores = host_cores()
-    bits = [(w, W.storage_bits(i["A"]), W.storage_bits(i["x"]), W.storage_bits(i["bias"])) for w, i in zip(head, host_inputs)]
+    bits = []
+    for w, i in zip(ws, inputs):
+        r = w.M if rows is None else min(rows, w.M)
+        bias = None if i["bias"] is None else i["bias"][:r]
+        scale = None if i["scale"] is None else i["scale"][:r]
+        bits.append((w, r, W.storage_bits(i["A"][:r]), W.storage_bits(i["x"]), W.storage_bits(bias),
+                     None if scale is None else scale.numpy()))
     reps = 0
     t0 = time.perf_counter()
     while True:
-        for (w, A, x, b) in bits:
-            oracle.gemv(w.dtype, A, x, b, nthreads=cores)
+        for (w, r, A, x, b, sc) in bits:
+            oracle.gemv(w.dtype, A, x, b, scale=sc, nthreads=nthreads)
         reps += 1
-        if time.perf_counter() - t0 >= budget_s or reps >= 50:
+        if time.perf_counter() - t0 >= budget_s or reps >= max_reps:
             break
     dt = (time.perf_counter() - t0) / reps
-    step_bytes = sum(w.qmin_bytes for w in head)
-    return {"value": round(step_bytes / dt / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the full step ({HEADLINE_DESC}), {reps} repetitions, fp64 C, OpenMP over rows",
-            "ms_per_step": round(dt * 1e3, 3)}
+    nbytes = sum(W.qmin_bytes(w.dtype, r, w.K, w.B) for (w, r, *_rest) in bits)
+    return nbytes / dt / 1e9, dt, reps, [r for (_, r, *_rest) in bits]
+
+
+def cpu_baseline(head, host_inputs, budget_s=10.0):
+    """The oracle (as it stands) on the same GEMV: on all host cores (OpenMP over
+    rows) over the whole matrix, and on one core over its first rows (a bounded
+    sample of the same matrix, about one second per repetition)."""
+    cores = host_cores()
+    gbs, dt, reps, _ = oracle_rate(head, host_inputs, cores, budget_s)
+    # one core: size the row sample from a short probe
+    w = head[0]
+    probe_rows = min(w.M, 2048)
+    g1, d1, _, _ = oracle_rate(head, host_inputs, 1, 0.0, max_reps=1, rows=probe_rows)
+    rows = int(max(256, min(w.M, probe_rows * 1.0 / max(d1, 1e-6))))
+    g1, d1, reps1, _ = oracle_rate(head, host_inputs, 1, budget_s, rows=rows)
+    return {"value": round(gbs, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the full GEMV ({HEADLINE_DESC}), {reps} repetitions, fp64 C, OpenMP over rows",
+            "ms_per_step": round(dt * 1e3, 3),
+            "single_thread": {"value": round(g1, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                              "sample": f"the first {rows} of the {w.M} rows of the same matrix, {reps1} "
+                                        f"repetitions, fp64 C, one thread",
+                              "ms_per_repetition": round(d1 * 1e3, 3)}}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -571,46 +679,25 @@ def run_reference(args, rank, world):
     oracle.build()
     cores = host_cores()
     head = [W.BY_NAME[n] for n in W.HEADLINE]
-    # a sample: the first `rows` rows of each GEMV of the step (same K, same values)
     full = [W.make_inputs(w) for w in head]
-
-    def sample(rows):
-        out = []
-        for w, inp in zip(head, full):
-            r = min(rows, w.M)
-            out.append((w, r, W.storage_bits(inp["A"][:r]), W.storage_bits(inp["x"]),
-                        W.storage_bits(inp["bias"][:r])))
-        return out
-
-    def step(smp):
-        for (w, r, A, x, b) in smp:
-            oracle.gemv(w.dtype, A, x, b, nthreads=cores)
-
-    rows = 1024
-    smp = sample(rows)
-    t0 = time.perf_counter()
-    step(smp)
-    one = time.perf_counter() - t0
-    budget = 90.0 / max(1, args.steps + args.warmup)  # the whole run within ~1.5 minutes
+    # a sample: the first `rows` rows of the GEMV (same K, same values), sized so
+    # that the whole run ends within about 1.5 minutes
+    rows = 4096
+    _, one, _, _ = oracle_rate(head, full, cores, 0.0, max_reps=1, rows=rows)
+    budget = 90.0 / max(1, args.steps + args.warmup)
     if one > 0:
-        rows = int(max(64, min(16384, rows * budget / one)))
-    smp = sample(rows)
-    for _ in range(args.warmup):
-        step(smp)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step(smp)
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
-    sbytes = sum(W.qmin_bytes(w.dtype, r, w.K, w.B) for (w, r, *_rest) in smp)
-    value = sbytes / dt / 1e9
-    desc = f"first {rows} rows of each of the 3 GEMVs of the step ({HEADLINE_DESC})"
+        rows = int(max(256, min(head[0].M, rows * budget / one)))
+    if args.warmup > 0:
+        oracle_rate(head, full, cores, 0.0, max_reps=args.warmup, rows=rows)
+    value, dt, _, _ = oracle_rate(head, full, cores, float("inf"), max_reps=max(1, args.steps), rows=rows)
+    desc = (f"the first {rows} of the {head[0].M} rows of the step's GEMV ({HEADLINE_DESC}), "
+            f"fp64 C, OpenMP over rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded PCG64)",
-        "config": {"workload": HEADLINE_DESC, "M": 16384, "K": [16, 32, 4096], "B": 1, "bias": True,
-                   "dtype": "f32", "sample_rows": rows},
+        "data": "synthetic (seeded PCG64: A ~ N(0, 0.02^2), x ~ N(0, 1), rounded to bf16)",
+        "config": headline_config(world),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

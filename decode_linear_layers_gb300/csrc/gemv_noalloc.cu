@@ -19,7 +19,9 @@
 //     rejected with GEMV_ERR_UNSUPPORTED before anything is launched.
 //   * The first call on each device looks up the array's device address with
 //     cudaGetSymbolAddress (with that device current) and keeps it; make that first
-//     call before capturing a stream into a CUDA graph.
+//     call before capturing a stream into a CUDA graph.  The kept address belongs to
+//     the device's primary context: after cudaDeviceReset it is stale, so this entry
+//     point must not be used on a device that was reset in the same process.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

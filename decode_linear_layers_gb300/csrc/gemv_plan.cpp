@@ -7,22 +7,30 @@
 // short rows, a CTA per row for long ones; the NPU MatMul post, sections 1.3 and
 // 3.4, asks for the kernel to be picked from (M, N, K, dtype, hardware) at run time.
 //
-// Rules used here (per call, from dtype, M, K, B, alignment and the SM count;
-// the thresholds come from timing every kernel on the GB300 configurations):
+// Rules used here, in the order they are tried (per call, from dtype, M, K, B,
+// alignment and the SM count; the thresholds come from timing every kernel on
+// GB300).  "Chunk" is 16 bytes of a row; rows/SM is M over the SM count.
 //   fp16/bf16 with 17..256 vectors        -> TC (tcgen05 small-N GEMM)
 //   rows not 16-byte aligned              -> SCALAR (element loads)
-//   row <= 16 chunks of 16 bytes          -> ROWS_PER_WARP, lanes = next pow2 of chunks
-//   fp32, B == 2, x slice fits 64 registers, at least 16 rows per SM and
-//     M < 65536                           -> XSPLIT (K split over a CTA)
-//   B >= 2, or int8/int4 with B == 1, at least 16 rows per SM, M < 65536 and
-//     x staged whole                      -> BATCHED: 4..16 vectors and at most
-//     one row pair per warp -> ROWPAIR, otherwise the cp.async ring (mixed-
-//     precision FMAs for fp16/bf16 with 2 or 9..16 vectors), over K slices with a
-//     second pass when x[0..B) does not fit in shared memory whole
+//   rows of <= 16 chunks                  -> ROWS_PER_WARP, lanes = next pow2 of chunks
+//   XSPLIT (K split over a CTA, x in registers; x slice within the register budget):
+//     fp32, B == 1, 8 rows/SM <= M <= 12288
+//     fp32, B == 2, >= 8 rows/SM, M < 65536
+//     K >= 8192, M >= one row/SM: fp16/bf16 with B == 2 and M <= 4096, or fp32
+//     with B == 4 and M <= 8192
+//   BATCHED, when x[0..B) can be staged and rows have >= 32 chunks, for B >= 2,
+//     and for B == 1 of int8 (>= 48 rows/SM) or int4 (>= 16 rows/SM) below 65536
+//     rows with x staged whole: the row-pair kernel for 4..16 vectors with at most
+//     one ring row group per warp, 16 vectors of 16-bit/fp32 rows, 8 vectors of
+//     16-bit rows whose ring would stage x as stored, and x too large for the ring;
+//     otherwise the cp.async ring (mixed-precision FMAs for fp16/bf16 with 2 or 16
+//     vectors), over K slices with a second pass when x does not fit whole
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
-//   B == 1 and at least 16 rows per SM    -> STREAM (persistent warps)
-//   at least 16 rows per SM, or <= 4 KB   -> WARP_PER_ROW
-//   at least 2 rows per SM                -> BLOCK_PER_ROW
+//   B == 1, >= 16 rows/SM (fp32) or >= 12 (other types) -> STREAM (persistent
+//     warps), except fp32 rows of >= 1024 chunks whose row walk would leave the
+//     streaming warps below 75% busy -> WARP_PER_ROW
+//   >= 16 rows/SM, or rows of <= 512 chunks -> WARP_PER_ROW
+//   >= 2 rows/SM, or rows of < 1024 chunks  -> BLOCK_PER_ROW
 //   fewer rows                            -> SPLIT_K over enough K slices to give
 //                                            every SM about four CTAs
 #include <stdint.h>
@@ -112,12 +120,9 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   // more than 16 vectors: only the tensor-core kernel, which needs 16-byte rows
   if (B > GEMV_MAX_BATCH && !vec_ok) return GEMV_ERR_UNSUPPORTED;
   const bool tc_ok = half16 && vec_ok;
-  // the batched shared-memory kernels are not built for int4 (grouped scales)
-  // the batched kernels are not built for int4 (grouped scales)
   // the ring kernel over rslices K slices (x staged per slice), the row-pair kernel
-  // over all of K
-  // (int4: the ring also carries each slot's group scale; the row-pair kernel is not
-  // built for grouped scales)
+  // over all of K (int4: the ring also carries each slot's group scale; the row-pair
+  // kernel is not built for grouped scales)
   const int64_t rextra = dtype == GEMV_DTYPE_W4 ? kRingScaleBytes : 0;
   const int rslices = nch == 0 ? 0 : ring_slices(p.nb, nch, vec, sx, rextra);
   const int64_t rcps = rslices > 0 ? ceil_div(nch, rslices) : 0;  // chunks per slice

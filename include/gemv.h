@@ -102,7 +102,9 @@ gemv_status_t gemv_f32(const float *A, const float *x, const float *bias, float 
 gemv_status_t gemv_f16(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
                        uint16_t *y, int64_t M, int64_t K, int B, gemv_stream_t stream);
 
-/* bf16 storage, fp32 accumulation, bf16 output. */
+/* bf16 storage, fp32 accumulation, bf16 output: the arithmetic-intensity glossary
+ * page's 16-bit weights and activations with an fp32 accumulator (its dtype notes),
+ * written back once to the storage type (NPU MatMul post, section 1.2). */
 gemv_status_t gemv_bf16(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
                         uint16_t *y, int64_t M, int64_t K, int B, gemv_stream_t stream);
 
@@ -122,8 +124,10 @@ gemv_status_t gemv_w8(const int8_t *A, const float *row_scale, const uint16_t *x
  *     y[b][m] = sum_k group_scale[m][k / GEMV_W4_GROUP] * A[m][k] * x[b][k] + bias[m]
  * Each 16-byte chunk (32 weights, inside one group) is summed in fp32 and scaled
  * once.  K must be a multiple of GEMV_W4_GROUP (GEMV_ERR_INVALID_VALUE otherwise);
- * group_scale is required when M * K > 0.  B >= 2 runs the warp-per-row kernels
- * (the batched shared-memory kernels are for the other types). */
+ * group_scale is required when M * K > 0.  B >= 2, and B == 1 with 16 or more rows
+ * per SM (below 65536 rows), run in the batched cp.async ring kernel, whose ring
+ * slots carry each chunk's group scale; the other shapes run in the streaming,
+ * warp-per-row, block-per-row or split-K kernels. */
 gemv_status_t gemv_w4(const uint8_t *A, const float *group_scale, const uint16_t *x,
                       const uint16_t *bias, uint16_t *y, int64_t M, int64_t K, int B,
                       gemv_stream_t stream);
@@ -142,7 +146,9 @@ gemv_status_t gemv_w4(const uint8_t *A, const float *group_scale, const uint16_t
  *   - All calls share the one array: calls whose kernels overlap on the GPU race
  *     and give wrong results; order them on one stream.
  *   - The first call on each device looks up the array's address (cudaGetSymbolAddress
- *     with that device current); make it before any stream capture. */
+ *     with that device current); make it before any stream capture.  The address is
+ *     kept for the life of the process: do not use this entry point on a device after
+ *     cudaDeviceReset there (the reset discards the context the address belongs to). */
 #define GEMV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
 gemv_status_t gemv_bf16_splitk_noalloc(const uint16_t *A, const uint16_t *x, const uint16_t *bias,
                                        uint16_t *y, int64_t M, int64_t K, int B,
@@ -182,7 +188,6 @@ gemv_status_t gemv_swiglu(gemv_dtype_t dtype, const void *A, const float *row_sc
                           const void *bias, void *y, int64_t I, int64_t K, int B,
                           gemv_stream_t stream);
 
-/* Human-readable name of a status code (static storage, never NULL). */
 /* End to end on host buffers: the GEMV of gemv_f32 .. gemv_w4 (chosen by dtype) with
  * its operands in host memory.  On `stream` it copies each host input into the
  * caller's device buffer of the same size (one cudaMemcpyAsync per buffer), runs the
@@ -227,6 +232,7 @@ gemv_status_t gemv_host(gemv_dtype_t dtype, const void *h_A, const float *h_scal
 #define GEMV_OVERLAP_WEIGHTS 2
 gemv_status_t gemv_set_launch_overlap(int mode);
 
+/* Human-readable name of a status code (static storage, never NULL). */
 const char *gemv_status_string(gemv_status_t status);
 
 /* The cudaError_t of this thread's last GEMV_ERR_CUDA (0 if none). */

@@ -72,3 +72,23 @@ def test_xsplit_epilogue(dtype):
     g.gemv_ex(dtype, d["A"], d["scale"], d["x"], d["bias"], y, y, M, K, B, 1)
     assert g.last_plan()["kernel_name"] == "xsplit"
     U.assert_close_ex(dtype, y, y_ref, absdot, 1, what=f"{dtype} xsplit silu + residual in place")
+
+
+# Shapes the dispatcher itself sends to the K-split kernel (no forcing): two long
+# 16-bit rows per call, four long fp32 ones, and the fp32 one- and two-vector
+# ranges.  A reordering of the dispatcher's rules that moved them elsewhere, or a
+# fault on their launch configuration, fails here.
+AUTO_XSPLIT = [("bf16", 1024, 16384, 2), ("f16", 4096, 8192, 2), ("f32", 2048, 8192, 4),
+               ("f32", 4096, 4096, 1), ("f32", 8192, 4096, 2)]
+
+
+@pytest.mark.parametrize("dtype,M,K,B", AUTO_XSPLIT)
+def test_auto_dispatch_takes_xsplit(dtype, M, K, B):
+    w = W.small(dtype, M, K, B, True, seed=M + B)
+    inp = W.make_inputs(w)
+    y_ref, absdot = U.oracle_for(dtype, inp)
+    d = U.to_device(inp)
+    y = U.run_gpu(dtype, d, M, K, B)
+    assert g.last_plan()["kernel_name"] == "xsplit", (dtype, M, K, B, g.last_plan()["kernel_name"])
+    torch.cuda.synchronize()
+    U.assert_close(dtype, y, y_ref, absdot, with_rounding=True, what=f"auto {dtype} {M}x{K} B={B}")
