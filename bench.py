@@ -366,6 +366,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
         "wall_s_timed_region": round(t1 - t0, 3),
         "fp32_step": fp32,
+        "launch_floor_us": round(launch_floor_us(torch, g, dev, flush), 3),
     }
 
     if not args.no_sweep:
@@ -476,9 +477,62 @@ def sweep(args, torch, g, dev, flush, peak):
             # context: the vendor library's time for the same product on the same
             # tensors (torch.matmul -> cuBLAS), timed the same way
             out[-1]["torch_linear_us"] = round(library_linear_us(torch, d, y, flush, args.sweep_iters) * 1e3, 3)
+        b2b = back_to_back_us(torch, g, w, d, y, flush)
+        out[-1]["us_back_to_back"] = round(b2b["us"], 3)
+        out[-1]["frac_of_peak_back_to_back"] = round(w.qmin_bytes / (b2b["us"] * 1e-6) / 1e9 / peak, 4)
+        out[-1]["back_to_back_copies"] = b2b["copies"]
         del d, y
         torch.cuda.empty_cache()
     return out
+
+
+def launch_floor_us(torch, g, dev, flush, iters=100):
+    """Mean CUDA-event time of the library's least-work launch (fp32, M = 1, K = 0:
+    one CTA writes y = 0), timed like every GEMV: the fixed cost of a single launch
+    between two events on this GPU, which no kernel design can remove."""
+    y = torch.empty((1, 1), dtype=torch.float32, device=dev)
+    for _ in range(5):
+        g.gemv_f32(None, None, None, y, 1, 0, 1)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    stream = torch.cuda.current_stream()
+    for e0, e1 in ev:
+        l2_flush(flush)
+        e0.record(stream)
+        g.gemv_f32(None, None, None, y, 1, 0, 1)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+
+
+def back_to_back_us(torch, g, w, d, y, flush, rounds=3):
+    """Per-GEMV time (us) of the workload launched back to back, as a decode loop
+    runs its GEMVs: A rotates over enough device copies that together they exceed
+    twice the L2 size (so every launch reads its weights from HBM), x and y stay;
+    one CUDA-event interval over 8 passes of the copies, mean over `rounds`."""
+    twice_l2 = flush.numel() * flush.element_size()  # the flush buffer is twice the L2 size
+    abytes = d["A"].numel() * d["A"].element_size()
+    copies = max(1, min(16, -(-twice_l2 // abytes)))
+    As = [d["A"]] + [d["A"].clone() for _ in range(copies - 1)]
+    n = max(8, 8 * copies)
+    dd = dict(d)
+
+    def run():
+        for i in range(n):
+            dd["A"] = As[i % copies]
+            call_gemv(g, w, dd, y)
+
+    run()
+    times = []
+    for _ in range(rounds):
+        l2_flush(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / n)
+    del As
+    return {"us": statistics.mean(times), "copies": copies}
 
 
 def library_linear_us(torch, d, y, flush, iters):

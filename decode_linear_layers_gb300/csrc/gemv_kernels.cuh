@@ -1620,37 +1620,52 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// 16-byte global -> shared copy to a shared-memory address given as a 32-bit offset.
+__device__ __forceinline__ void cp_async16_s(uint32_t s, const void *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// The ring holds G groups of P rows: group gi sits in slots (gi % G) * P + q, so a
+// group's slots are free again once the group G before it has been read.  All
+// indexes inside the CTA's block of rows are 32-bit and the slot addresses are
+// 32-bit shared-memory offsets: the only 64-bit arithmetic per group is one pointer
+// to its first row.
 template <class Op, int NB, int J, int P, int G>
 __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
   pdl_enter(a, true);
   static_assert(NB == 1 || NB == 2 || NB == 4, "NB");
-  static_assert(kXsT % P == 0, "a barrier batch is whole groups");
-  constexpr int D = P * G;  // rows in the ring
-  extern __shared__ __align__(16) unsigned char ring[];  // [D][J][512] 16-byte slots
+  static_assert(kXsT % P == 0 && (kXsT & (kXsT - 1)) == 0, "a barrier batch is whole groups");
+  static_assert((G & (G - 1)) == 0, "G is a power of two");
+  extern __shared__ __align__(16) unsigned char ring[];  // [G][P][J][512] 16-byte slots
   __shared__ float red[2][kXsT][kXsWarps][NB];
-  constexpr int LOGNB = NB == 4 ? 2 : NB == 2 ? 1 : 0;
-  constexpr int PV = Op::VEC / 2;  // fp32 pairs per chunk
+  constexpr int PV = Op::VEC / 2;               // fp32 pairs per chunk
+  constexpr uint32_t kSlot = kXsThreads * 16;  // bytes between one thread's consecutive slots
+  constexpr int LOGT = kXsT == 16 ? 4 : kXsT == 8 ? 3 : kXsT == 4 ? 2 : kXsT == 2 ? 1 : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t M = a.M, K = a.K, nch = K / Op::VEC;
   const int B = a.B;
   const int64_t rowb = row_bytes<Op>(K);
   const int64_t r0 = M * blockIdx.x / gridDim.x, r1 = M * (blockIdx.x + 1) / gridDim.x;
-  const int64_t n = r1 - r0;
-  const int64_t ngroups = (n + P - 1) / P;
-  const char *A = reinterpret_cast<const char *>(a.A) + r0 * rowb;
+  const int n = (int)(r1 - r0);  // rows of this CTA
+  const int ngroups = (n + P - 1) / P;
+  bool cj[J];  // does this thread own chunk tid + 512 j of a row?
+#pragma unroll
+  for (int j = 0; j < J; ++j) cj[j] = tid + (int64_t)kXsThreads * j < nch;
+  // this thread's chunk 0 of the CTA's first row; chunk tid + 512 j is j * kSlot further
+  const char *At = reinterpret_cast<const char *>(a.A) + r0 * rowb + (int64_t)tid * 16;
+  const uint32_t ring_t = (uint32_t)__cvta_generic_to_shared(ring) + (uint32_t)tid * 16;
 
-  // this thread's chunks of rows g*P .. g*P+P-1 into their slots; one commit group
-  // per call (empty past the last row, so every iteration waits on the same count)
-  auto issue = [&](int64_t gi) {
+  // this thread's chunks of group gi's rows into their slots; one commit group per
+  // call (empty past the last row, so every iteration waits on the same count)
+  auto issue = [&](int gi) {
+    const char *pg = At + (int64_t)gi * P * rowb;
+    const uint32_t sg = ring_t + (uint32_t)((gi & (G - 1)) * P * J) * kSlot;
 #pragma unroll
     for (int q = 0; q < P; ++q) {
-      const int64_t i = gi * P + q;
-      if (i < n) {
+      if (gi * P + q < n) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int64_t c = tid + (int64_t)kXsThreads * j;
-          if (c < nch) cp_async16(ring + ((size_t)((i % D) * J + j) * kXsThreads + tid) * 16, A + i * rowb + c * 16);
-        }
+        for (int j = 0; j < J; ++j)
+          if (cj[j]) cp_async16_s(sg + (uint32_t)(q * J + j) * kSlot, pg + q * rowb + (int64_t)j * kSlot);
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -1681,9 +1696,10 @@ __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
   constexpr int V = P * NB;  // values one group reduces (row q, vector b at q * NB + b)
   constexpr int LOGV = V == 16 ? 4 : V == 8 ? 3 : V == 4 ? 2 : V == 2 ? 1 : 0;
   static_assert((1 << LOGV) == V && V <= 32, "P * NB must be a power of two up to 32");
-  for (int64_t gi = 0; gi < ngroups; ++gi) {
-    const int64_t i0 = gi * P;
-    if (i0 % kXsT == 0 && tid < kXsT * NB) {
+  for (int gi = 0; gi < ngroups; ++gi) {
+    const int i0 = gi * P;
+    const int t0 = i0 & (kXsT - 1);  // the group's first row within its barrier batch
+    if (t0 == 0 && tid < kXsT * NB) {
       const int64_t row = r0 + i0 + tid / NB;
       const int b = tid % NB;
       const bool live = row < r1 && b < B;
@@ -1692,19 +1708,18 @@ __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
     }
     asm volatile("cp.async.wait_group %0;" ::"n"(G - 1) : "memory");  // group gi has landed
     // the group's P rows (rows past n contribute zeros), then one reduction for all
+    const uint32_t sg = ring_t + (uint32_t)((gi & (G - 1)) * P * J) * kSlot;
     float v[V];
 #pragma unroll
     for (int q = 0; q < P; ++q) {
-      const int s = (int)((i0 + q) % D);
       float2 acc[NB];
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[b] = make_float2(0.f, 0.f);
       if (i0 + q < n) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-          const int64_t c = tid + (int64_t)kXsThreads * j;
-          if (c < nch) {
-            const uint4 av = *reinterpret_cast<const uint4 *>(ring + ((size_t)(s * J + j) * kXsThreads + tid) * 16);
+          if (cj[j]) {
+            const uint4 av = lds16(sg + (uint32_t)(q * J + j) * kSlot);
 #pragma unroll
             for (int w = 0; w < Op::VEC / 4; ++w) {
               float2 q01, q23;
@@ -1723,13 +1738,13 @@ __global__ void __launch_bounds__(kXsThreads, 1) k_xsplit(const Args a) {
     }
     issue(gi + G);  // the group's slots are free again (this thread read them above)
     const float part = warp_reduce_scatter<V>(v, lane);
-    const int hb = (int)((i0 / kXsT) & 1);
+    const int hb = (i0 >> LOGT) & 1;
     if ((lane & ((32 >> LOGV) - 1)) == 0) {
       const int idx = lane >> (5 - LOGV);
-      red[hb][(int)(i0 % kXsT) + idx / NB][warp][idx % NB] = part;
+      red[hb][t0 + idx / NB][warp][idx % NB] = part;
     }
-    const int64_t ilast = min(i0 + P, n) - 1;  // the group's last real row
-    const int t = (int)(ilast % kXsT);
+    const int ilast = min(i0 + P, n) - 1;  // the group's last real row
+    const int t = ilast & (kXsT - 1);
     if (t == kXsT - 1 || ilast == n - 1) {
       __syncthreads();
       if (tid < (t + 1) * NB) {

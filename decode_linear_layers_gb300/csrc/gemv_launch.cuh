@@ -35,6 +35,37 @@ cudaError_t launch_k(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cud
   return cudaLaunchKernelEx(&cfg, kern, std::forward<A2>(args)...);
 }
 
+// The same, as clusters of (1, cy, 1) CTAs.
+template <typename... P, typename... A2>
+cudaError_t launch_k_cluster(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int pdl,
+                             int cy, int policy, A2 &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[3];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)cy;
+  attr[0].val.clusterDim.z = 1;
+  int na = 1;
+  if (pdl != 0) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (policy == 1 || policy == 2) {
+    attr[na].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[na].val.clusterSchedulingPolicyPreference =
+        policy == 1 ? cudaClusterSchedulingPolicySpread : cudaClusterSchedulingPolicyLoadBalancing;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A2>(args)...);
+}
+
 // Dynamic shared memory above 48 KB has to be allowed per kernel.
 template <typename Kern>
 cudaError_t allow_smem(Kern kern, int bytes) {
@@ -200,15 +231,15 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
   }
 }
 
-// fp16/bf16 with more than 16 vectors (or forced): the tensor-core kernel, then the
-// split-K reduction when the K range is split.
+// fp16/bf16 with more than 16 vectors (or forced): the tensor-core kernel; a split K
+// range runs as clusters of the tile's slices, reduced inside the kernel.
 template <class Op>
-cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *ws, cudaStream_t s) {
+cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *, cudaStream_t s) {
   if constexpr (!TcFormat<Op>::ok) {
     return cudaErrorInvalidValue;  // the planner never picks it for these types
   } else {
-    if (p.nb < 16 || p.nb > kTcMaxN || p.nb % 16 != 0 || p.splits < 1) return cudaErrorInvalidValue;
-    if (p.splits > 1 && ws == nullptr) return cudaErrorInvalidValue;
+    if (p.nb < 16 || p.nb > kTcMaxN || p.nb % 16 != 0 || p.splits < 1 || p.splits > kTcMaxCluster)
+      return cudaErrorInvalidValue;
     const int ka = tc_atoms(p.nb), sb = tc_stage_bytes(p.nb, ka), stages = (p.smem_bytes - 1024) / sb;
     if (stages < 2 || stages > kTcMaxStages || p.smem_bytes != stages * sb + 1024) return cudaErrorInvalidValue;
     CUtensorMap map_a, map_x;
@@ -219,14 +250,12 @@ cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
     auto kern = ka == 2 ? k_tc<Op, 2> : k_tc<Op, 1>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    e = launch_k(kern, dim3((unsigned)p.grid, (unsigned)p.splits), dim3(kTcThreads), (size_t)p.smem_bytes, s, a.pdl,
-                 map_a, map_x, a, p.splits > 1 ? ws : nullptr, (int64_t)p.unroll, p.nb, stages);
-    if (e != cudaSuccess || p.splits == 1) return e;
-    const int64_t total = a.M * a.B;
-    int64_t g = (total + kThreads - 1) / kThreads;
-    if (g > 65535) g = 65535;
-    return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
-                    p.splits);
+    const dim3 grid((unsigned)p.grid, (unsigned)p.splits);
+    if (p.splits == 1)
+      return launch_k(kern, grid, dim3(kTcThreads), (size_t)p.smem_bytes, s, a.pdl, map_a, map_x, a,
+                      (int64_t)p.unroll, p.nb, stages);
+    return launch_k_cluster(kern, grid, dim3(kTcThreads), (size_t)p.smem_bytes, s, a.pdl, p.splits, p.variant, map_a,
+                            map_x, a, (int64_t)p.unroll, p.nb, stages);
   }
 }
 

@@ -354,13 +354,20 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 4096 rows B = 64 23.3 against 21.4; 28672 rows B = 32 57.3 against 45.1)
       // (forced: param >= 32 is the ring size in KB)
       const bool deep = p.nb <= 64 && tiles < num_sms && 2 * tiles >= num_sms;
-      const int ring_kb = param >= 32 && param <= 220 ? param : deep ? 200 : 100;
+      // (forced: param % 1000 in 32..220 is the ring size in KB, param / 1000 % 10 in
+      // 1..8 the number of K slices, param / 10000 % 10 the cluster scheduling
+      // preference: 1 spread, 2 load balancing)
+      const int pk = param % 1000, ps = param / 1000 % 10;
+      const int ring_kb = pk >= 32 && pk <= 220 ? pk : deep ? 200 : 100;
       const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb) * tc_plan_stage_bytes(p.nb) + 1024;
       int64_t per_sm = kSmemPerSm / (smem + 1024);
       if (per_sm < 1) per_sm = 1;
+      // (the slices of a tile run as one cluster and are summed inside the kernel, so
+      // they are at most the cluster size)
       int64_t s = (int64_t)num_sms * per_sm / tiles;
+      if (ps >= 1 && ps <= kTcMaxCluster) s = ps;
       if (s > ktiles) s = ktiles;
-      if (s > 65535) s = 65535;
+      if (s > kTcMaxCluster) s = kTcMaxCluster;
       if (s < 1) s = 1;
       const int64_t per = ceil_div(ktiles, s);
       s = ceil_div(ktiles, per);  // no empty slice
@@ -370,7 +377,8 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       p.unroll = (int)per;
       p.lanes_per_row = kTcPlanThreads;
       p.smem_bytes = (int)smem;
-      p.workspace_bytes = s > 1 ? s * (int64_t)B * M * 4 : 0;
+      p.workspace_bytes = 0;
+      p.variant = param / 10000 % 10;  // (forced only) cluster scheduling preference
       break;
     }
     case GEMV_KERNEL_XSPLIT: {

@@ -48,6 +48,8 @@ constexpr int xsplit_depth(int J) { return xsplit_rows_per_group(J) * kXsplitGro
 // swizzle atoms along K; as many stages (at most 8) as fit in the ring, plus 1024
 // bytes to align them.
 constexpr int kTcPlanThreads = 128;
+// K slices of one row tile run as one thread-block cluster (the portable maximum size)
+constexpr int kTcMaxCluster = 8;
 constexpr int kTcPlanTileM = 128;
 constexpr int kTcPlanTileK = 64;
 // 64-column atoms per stage: two for N <= 64, one above.

@@ -3,9 +3,14 @@
 // the 5th-generation tensor cores: Y^T (M x N) = A (M x K) . X^T (K x N), N = B
 // rounded up to a multiple of 16, fp32 accumulation in tensor memory.
 //
-// One CTA of 128 threads per 128-row tile of A (and per K slice when the tiles are
-// too few to occupy the SMs: split-K, the slices summed in index order by
-// k_splitk_reduce).  Two threads run the pipeline.  A producer (lane 0 of warp 0)
+// One CTA of 128 threads per 128-row tile of A, and per K slice when the tiles are
+// too few to occupy the SMs (split-K).  The S slices of a tile run as one thread-block
+// cluster: CTA r owns rows [ceil(128 r / S), ceil(128 (r + 1) / S)) of the tile, and
+// every CTA stores its partial sums of those rows into the owner's shared memory
+// (distributed shared memory stores, one slot per slice); after a cluster barrier
+// each owner adds its rows' S partial sums in slice order from its own shared memory
+// (deterministic, no atomics, no second kernel, no global workspace).  Two threads
+// run the pipeline.  A producer (lane 0 of warp 0)
 // has the tensor-memory accelerator (TMA) copy each k-tile (128 x 64 or 128 x 128
 // of A and N x 64/128 of x, 128-byte swizzle, zeros outside the matrix) into a free
 // stage, completing on the stage's "full" mbarrier; an MMA issuer (lane 0 of warp 1)
@@ -30,6 +35,7 @@ constexpr int kTcM = 128;        // rows per tile (the MMA's M)
 constexpr int kTcK = 64;         // K per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kTcMaxStages = 8;
 constexpr int kTcMaxN = 256;
+constexpr int kTcMaxSlices = 8;  // K slices of a tile: one cluster (the portable maximum size)
 
 // device status bits (ORed into *Args::status)
 constexpr int kTcStatusMma = 16;   // a copy or an MMA commit did not arrive in time
@@ -157,18 +163,39 @@ __host__ __device__ constexpr int tc_stage_bytes(int n, int ka) { return (kTcM +
 // should carry at least ~24 KB.
 __host__ __device__ constexpr int tc_atoms(int n) { return n <= 64 ? 2 : 1; }
 
-// grid (ceil(M / 128), splits); k-tiles [y * kt_per_split, ...) of K.  partial ==
-// nullptr: finish the outputs here (epilogue); otherwise write the slice's sums to
-// partial[(y * B + b) * M + m] for k_splitk_reduce.  map_a: A as (K, M) 16-bit
-// values, box 64 x 128; map_x: x as (K, B), box 64 x N; both 128-byte swizzle.
+// Distributed shared memory: four floats into the shared memory of the cluster's CTA
+// `rank`, at the same offset as `p` has in this CTA.  A store: it does not wait for a
+// reply.
+__device__ __forceinline__ void tc_st_dsmem4(const float *p, uint32_t rank, float a, float b, float c, float d) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(tc_smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tc_st_dsmem_int(const int *p, uint32_t rank, int v) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(tc_smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+// Every thread of every CTA of the cluster: writes before it are visible to the
+// cluster's reads after it.
+__device__ __forceinline__ void tc_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// grid (ceil(M / 128), S); k-tiles [y * kt_per_split, ...) of K.  S > 1: launched as
+// clusters of (1, S, 1), the slices of a tile reduced through distributed shared
+// memory (above).  map_a: A as (K, M) 16-bit values, box 64 x 128; map_x: x as (K,
+// B), box 64 x N; both 128-byte swizzle.
 template <class Op, int KA>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_x, const Args a,
-         float *partial, int64_t kt_per_split, int N, int stages) {
+         int64_t kt_per_split, int N, int stages) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full[kTcMaxStages], empty[kTcMaxStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;                                  // set by either role on timeout
+  __shared__ int abort_of[kTcMaxSlices];                      // the cluster's abort flags, by rank
   __shared__ long long sh_loaded, sh_consumed, sh_committed;  // for the drain after an abort
   pdl_enter(a, false);  // every read (TMA included) after the kernel before has finished
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -187,12 +214,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t x_atom = (uint32_t)N * kTcK * 2, a_bytes = a_atom * KA, st_bytes = (a_atom + x_atom) * KA;
   const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
 
-  if (nt <= 0) {  // K == 0: the empty sum
+  if (nt <= 0) {  // K == 0: the empty sum (one slice; every CTA of a cluster has K == 0)
     const int64_t m = m0 + tid;
-    for (int b = 0; b < B && m < M; ++b) {
-      if (partial != nullptr) partial[((int64_t)blockIdx.y * B + b) * M + m] = 0.f;
-      else epilogue_store<Op>(a, b, m, 0.f);
-    }
+    for (int b = 0; b < B && m < M && blockIdx.y == 0; ++b) epilogue_store<Op>(a, b, m, 0.f);
     return;
   }
   if (warp == 0) {
@@ -266,7 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sh_committed = committed;
   }
   __syncthreads();
-  if (abort_flag) {
+  const bool aborted = abort_flag != 0;
+  if (aborted) {
     // nothing may be in flight when the CTA frees its tensor memory and exits: the
     // last committed MMAs (their commit covers all earlier ones) and every copy
     // issued but not waited for
@@ -279,16 +304,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         drained = tc_mbar_wait(&full[t % S], (uint32_t)((t / S) & 1), a.timeout_ns);
       if (!drained && a.status != nullptr) atomicOr(a.status, kTcStatusDrain);
     }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
-    return;
   }
 
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const int64_t m = m0 + warp * 32 + lane;  // this thread's row: TMEM lane 32 * warp + lane
-  for (int c0 = 0; c0 < N; c0 += 16) {
-    uint32_t r[16];
+  const int row = warp * 32 + lane;  // this thread's tile row: TMEM lane 32 * warp + lane
+  const int64_t m = m0 + row;
+  // 16 accumulator columns c0 .. c0 + 15 of this thread's row
+  auto tmem_ld16 = [&](int c0, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15}, [%16];"
@@ -296,16 +319,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (m < M) {
+  };
+  const int nslices = (int)gridDim.y;
+  if (nslices == 1) {
+    if (!aborted) {
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(c0, r);
+        if (m < M) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int b = c0 + j;
-        if (b < B) {
-          const float v = __uint_as_float(r[j]);
-          if (partial != nullptr) partial[((int64_t)blockIdx.y * B + b) * M + m] = v;
-          else epilogue_store<Op>(a, b, m, v);
+          for (int j = 0; j < 16; ++j) {
+            const int b = c0 + j;
+            if (b < B) epilogue_store<Op>(a, b, m, __uint_as_float(r[j]));
+          }
         }
       }
+    }
+  } else {
+    // The cluster's slices of this tile.  The stages are idle now (every copy has
+    // landed and every MMA has completed, or the CTA drained them above), so they hold
+    // the owner buffers, CW columns at a time: part[slice][owned row][c], rows padded
+    // to CW + 4 floats (16-byte rows whose bank offsets differ across a warp's rows).
+    uint32_t rank;  // this CTA's rank in the cluster of the tile's slices
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int S = nslices;
+    const int maxrows = (kTcM + S - 1) / S;
+    const int ring = stages * (int)st_bytes;
+    int cw = ring / (4 * S * maxrows) - 4;
+    cw = (cw / 16) * 16;
+    if (cw > N) cw = N;
+    const int rs = cw + 4;
+    float *part = reinterpret_cast<float *>(smem);
+    auto first_row = [&](int r) { return (kTcM * r + S - 1) / S; };
+    const int owner = row * S / kTcM;  // the CTA that sums this thread's row
+    const int orow = row - first_row(owner);
+    const int rlo = first_row((int)rank), nrows = first_row((int)rank + 1) - rlo;
+    // every CTA of the cluster has finished with its stages (and has started): only
+    // now may peers store into them
+    tc_cluster_sync();
+    if (tid < S) tc_st_dsmem_int(&abort_of[rank], (uint32_t)tid, aborted ? 1 : 0);
+    for (int c0 = 0; c0 < N; c0 += cw) {
+      const int w = N - c0 < cw ? N - c0 : cw;
+      if (!aborted) {
+        const float *dst = part + ((int)rank * maxrows + orow) * rs;
+        for (int cc = 0; cc < w; cc += 16) {
+          uint32_t r[16];
+          tmem_ld16(c0 + cc, r);
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            tc_st_dsmem4(dst + cc + j, (uint32_t)owner, __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                         __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        }
+      }
+      tc_cluster_sync();  // every slice's partial sums of the owned rows (and every abort flag) are here
+      bool any_abort = false;
+      for (int q = 0; q < S; ++q) any_abort |= abort_of[q] != 0;
+      if (!any_abort) {
+        // consecutive threads on consecutive rows (coalesced stores of y[b][m]), four
+        // columns each; slices added in index order
+        for (int idx = tid; idx < nrows * (w / 4); idx += kTcThreads) {
+          const int rl = idx % nrows, c = (idx / nrows) * 4;
+          float4 v = *reinterpret_cast<const float4 *>(part + rl * rs + c);
+          for (int q = 1; q < S; ++q) {
+            const float4 u = *reinterpret_cast<const float4 *>(part + (q * maxrows + rl) * rs + c);
+            v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+          }
+          const int64_t mm = m0 + rlo + rl;
+          const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (c0 + c + j < B && mm < M) epilogue_store<Op>(a, c0 + c + j, mm, vv[j]);
+        }
+      }
+      tc_cluster_sync();  // the owners are done reading before the next columns arrive
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

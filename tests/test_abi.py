@@ -370,8 +370,9 @@ def test_plan_tensor_cores():
     # cover less than half the SMs: two CTAs per SM, as many stages as fit in 100 KB
     # (at most 8), + 1024 bytes to align them
     assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024
-    # split-K so that all CTAs run in one wave: 8 slices of 4 k-tiles of 128
-    assert p["splits"] == 8 and p["unroll"] == 4 and p["workspace_bytes"] == 8 * 32 * 4096 * 4
+    # split-K so that all CTAs run in one wave: 8 slices of 4 k-tiles of 128, one
+    # cluster per row tile, summed in the kernel (no workspace)
+    assert p["splits"] == 8 and p["unroll"] == 4 and p["workspace_bytes"] == 0
     assert p["grid"] * p["splits"] <= 2 * 152
     # tiles covering half the SMs or more (but not all), up to 64 vectors: the deep
     # ring (200 KB, one CTA per SM)
@@ -387,11 +388,15 @@ def test_plan_tensor_cores():
     assert p["smem_bytes"] == 2 * (128 + 256) * 128 + 1024
     p = g.plan_for("bf16", 28672, 4096, 32)
     assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024 and p["grid"] == 224 and p["splits"] == 1
-    # no empty slice: splits * k-tiles per slice covers K exactly once
+    # no empty slice: splits * k-tiles per slice covers K exactly once; at most 8
+    # slices (one cluster of CTAs per row tile)
     for M, Kd in ((300, 1000), (1, 64), (5000, 4104), (128, 16384)):
         p = g.plan_for("bf16", M, Kd, 40)
         kt = -(-Kd // 128)  # N = 48: 128-column k-tiles
         assert (p["splits"] - 1) * p["unroll"] < kt <= p["splits"] * p["unroll"], (M, Kd, p)
+        assert 1 <= p["splits"] <= 8 and p["workspace_bytes"] == 0, (M, Kd, p)
+    p = g.plan_for("bf16", 4096, 14336, 64)  # 9 slices would fill the wave; a cluster holds 8
+    assert p["splits"] == 8 and p["unroll"] == 14
     for dt in ("f32", "w8"):
         with pytest.raises(g.GemvError):
             g.plan_for(dt, 100, 64, 17)

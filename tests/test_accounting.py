@@ -95,13 +95,23 @@ def test_inputs_are_seeded_and_shaped():
 
 
 def test_traffic_record_matches_kernel_sources():
-    # profiles/traffic.txt carries the ncu DRAM traffic of the benchmark's dominant
-    # kernel for the kernel sources it was captured from; the record must be for the
-    # sources as committed (else the benchmark reports traffic as unknown), and the
-    # captured bytes must be the workload's Q_min within a few percent (no re-reads)
+    # profiles/traffic.txt carries the ncu DRAM traffic of the benchmark's step kernel
+    # for the kernel code it was captured from; the record must be for the code as
+    # committed (else the benchmark reports traffic as unknown), and the captured
+    # bytes must be the workload's Q_min within a few percent (no re-reads)
     import bench
 
-    t = bench.read_traffic("f32_16384x4096_b1_bias")
-    assert t is not None, "profiles/traffic.txt was captured from other kernel sources"
-    q = W.BY_NAME["f32_16384x4096_b1_bias"].qmin_bytes
+    name = W.HEADLINE[0]
+    t = bench.read_traffic(name)
+    assert t is not None, "profiles/traffic.txt was captured from other kernel code"
+    q = W.BY_NAME[name].qmin_bytes
     assert 0.99 * q <= t <= 1.03 * q, (t, q)
+
+
+def test_code_hash_ignores_comments_only():
+    import bench
+
+    a = "int f(int x) { return x + 1; }  // one\n/* two */"
+    b = "int f(int x) {\n  /* changed */ return x + 1;\n}"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(a.replace("x + 1", "x + 2"))

@@ -129,7 +129,7 @@ def test_tc_guard_bytes():
 
 
 def test_tc_in_cuda_graph():
-    M, K, B = 4096, 4096, 32  # split-K: scratch from the stream-ordered pool
+    M, K, B = 4096, 4096, 32  # split-K: the slices summed in the kernel (one cluster per tile)
     w = W.small("bf16", M, K, B, False, seed=991)
     d = U.to_device(W.make_inputs(w))
     y = torch.empty(B, M, dtype=torch.bfloat16, device="cuda")

@@ -93,7 +93,8 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
         assert p["grid"] == _cdiv(M, 128)
         ktiles = _cdiv(K, 64 * ka) if K > 0 else 1
         assert p["splits"] * p["unroll"] >= ktiles and (p["splits"] - 1) * p["unroll"] < ktiles
-        assert p["workspace_bytes"] == (p["splits"] * B * M * 4 if p["splits"] > 1 else 0)
+        # the slices of a row tile are one cluster (at most 8 CTAs), reduced in the kernel
+        assert 1 <= p["splits"] <= 8 and p["workspace_bytes"] == 0
     elif kern == K_["stream"]:
         assert B == 1 and p["threads"] == 512
     elif kern == K_["xsplit"]:
