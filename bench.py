@@ -73,10 +73,13 @@ def parse_args(argv=None):
     ap.add_argument("--only", default=None, help="sweep only these comma-separated configs")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-configuration sweep (e.g. under ncu); prints one JSON line")
+    ap.add_argument("--sweep-bare", action="store_true",
+                    help="sweep without the vendor-library and back-to-back legs (for ncu launch lists)")
     ap.add_argument("--force", default=None,
                     help="with --sweep-only: run every configuration on this kernel family where it "
                          "applies (rows_per_warp, warp_per_row, block_per_row, split_k, batched, "
-                         "scalar, stream), through the library's test hook")
+                         "scalar, stream, xsplit, tc), through the library's test hook; "
+                         "family:param passes the hook's parameter (e.g. batched:1 for the row pairs)")
     return ap.parse_args(argv)
 
 
@@ -290,7 +293,8 @@ def run_ours(args, rank, world, local_rank):
 
     if args.sweep_only:
         if args.force:
-            g.force_kernel(args.force)
+            kname, _, kparam = args.force.partition(":")
+            g.force_kernel(kname, int(kparam or 0))
         try:
             if rank == 0:
                 print(json.dumps({"sweep": sweep(args, torch, g, dev, flush, peak)}), flush=True)
@@ -473,6 +477,10 @@ def sweep(args, torch, g, dev, flush, peak):
         if plan["kernel_name"] == "tc":  # a contraction on the tensor cores: its own roofline too
             tp, _ = measured_tensor_peak_tflops()
             out[-1]["frac_of_tensor_peak"] = round(w.flops / (mean * 1e-3) / 1e12 / tp, 4)
+        if args.sweep_bare:
+            del d, y
+            torch.cuda.empty_cache()
+            continue
         if w.dtype in ("f32", "f16", "bf16") and not w.bias:
             # context: the vendor library's time for the same product on the same
             # tensors (torch.matmul -> cuBLAS), timed the same way

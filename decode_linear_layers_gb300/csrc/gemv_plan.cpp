@@ -202,6 +202,19 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 26.6) and 4 fp32 vectors (8192x8192 46.4 against 52.1 in the ring, 2048x8192
       // 18.5 against 28.5 in the row pairs)
       kernel = GEMV_KERNEL_XSPLIT;
+    } else if (xs_ok && half16 && B == 1 && K >= 8192 && M >= num_sms && M < (int64_t)num_sms * 12) {
+      // one vector of few long 16-bit rows (fewer than the streaming kernel takes): the
+      // K-split kernel spreads each row over a CTA (bf16 1024x16384 12.3 us against 15.1
+      // block per row, 1536x16384 14.4 against 18.4, 1024x8192 10.2 against 11.6, 256x16384
+      // 9.2 against 13.7 split-K; f16 1024x16384 12.3 against 16.2)
+      kernel = GEMV_KERNEL_XSPLIT;
+    } else if (dtype == GEMV_DTYPE_F32 && p.nb == 2 && nch >= 2048 && M >= (int64_t)num_sms * 2 &&
+               M < (int64_t)num_sms * 32) {
+      // two vectors of few long fp32 rows: block per row, where the batched kernels'
+      // row groups of 4 would leave most warps idle (1024x16384 24.9 us against 50.0,
+      // 2048x12288 27.6 against 41.0, 4096x14336 47.3 against 52.8, 1024x8192 16.4
+      // against 28.8; at 8192x14336 the ring leads, 79.6 against 81.3)
+      kernel = GEMV_KERNEL_BLOCK_PER_ROW;
     } else if ((B > 1 || ((dtype == GEMV_DTYPE_W8 || dtype == GEMV_DTYPE_W4) && rslices == 1 &&
                           M >= (int64_t)num_sms * (dtype == GEMV_DTYPE_W8 ? 48 : 16) && M < 65536)) &&
                batched_ok && nch >= 32) {
@@ -308,6 +321,12 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       int v;
       if (param != 0) {
         v = param - 1;
+      } else if (half16 && p.nb == 4 && M <= 2048 && mixed_ok && rslices == 1) {
+        // 4 vectors of few 16-bit rows: the mixed-precision ring (bf16 1024x16384
+        // 24.6 us against 26.8 in the row pairs, 2048x16384 26.8 against 28.7, 2048x8192
+        // 16.6 against 18.4; from 4096 rows the row pairs lead: 4096x14336 29.2 against
+        // 32.2)
+        v = GEMV_BATCHED_RING_MIXED;
       } else if (rstage < 0 ||
                  (rowpair_ok &&
                   (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2) ||
@@ -353,7 +372,11 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 30.7 deep against 33.6, B = 64 33.5 against 37.7, B = 128 49.1 against 46.3;
       // 4096 rows B = 64 23.3 against 21.4; 28672 rows B = 32 57.3 against 45.1)
       // (forced: param >= 32 is the ring size in KB)
-      const bool deep = p.nb <= 64 && tiles < num_sms && 2 * tiles >= num_sms;
+      // (and 64 or more vectors on at most a quarter as many tiles as SMs: K slices on
+      // deep rings, one CTA per SM; f16 4096x4096 B = 256 34.6 us against 40.1 on two
+      // 100 KB rings per SM, B = 64 18.8 against 20.1)
+      const bool deep = (p.nb <= 64 && tiles < num_sms && 2 * tiles >= num_sms) ||
+                        (p.nb >= 64 && 4 * tiles <= num_sms);
       // (forced: param % 1000 in 32..220 is the ring size in KB, param / 1000 % 10 in
       // 1..8 the number of K slices, param / 10000 % 10 the cluster scheduling
       // preference: 1 spread, 2 load balancing)

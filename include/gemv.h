@@ -33,9 +33,11 @@
  * Ownership and memory: every pointer is caller-owned DEVICE memory on the
  * current CUDA device.  A, x, bias and row_scale are only read; y is only written
  * and must not overlap any input (checked on the host).  The library keeps no
- * pointer after the call returns.  Only the split-K path uses scratch memory: it
- * takes it from the stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
- * caller's stream), so nothing is allocated or freed synchronously.
+ * pointer after the call returns.  Only the CUDA-core split-K paths (few long rows,
+ * or x[0..B) too large to stage whole) use scratch memory: they take it from the
+ * stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the caller's stream), so
+ * nothing is allocated or freed synchronously.  The tensor-core kernel sums its K
+ * slices in the shared memory of one thread-block cluster and needs none.
  *
  * Execution: asynchronous on `stream` (NULL = the legacy default stream).  The
  * call validates its arguments, picks a kernel from (dtype, M, K, B, alignment)
@@ -262,7 +264,9 @@ typedef enum gemv_kernel {
                                     shared-memory slots */
   GEMV_KERNEL_TC = 9             /* fp16/bf16, B > 16: tcgen05 MMA (M = 128 rows per CTA,
                                     N = B rounded up to 16), fp32 accumulators in tensor
-                                    memory, split-K when the row tiles are few; waits bounded */
+                                    memory; when the row tiles are few, up to 8 K slices per
+                                    tile run as one thread-block cluster and are summed in
+                                    its distributed shared memory; waits bounded */
 } gemv_kernel_t;
 
 /* Where a kernel reads x from (gemv_plan_t.x_staging). */
@@ -308,8 +312,11 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
  * (lanes_per_row, rows_per_warp or splits; 0 = the dispatcher's choice) when the
  * arguments allow it; GEMV_KERNEL_AUTO restores normal dispatch.  STREAM needs
  * B == 1; BATCHED needs x[0..B) to fit in shared memory and takes the variant + 1
- * (GEMV_BATCHED_*; the mixed-precision ring only for fp16/bf16); TC takes the ring
- * size in KB (32..220; smaller values keep the dispatcher's choice).  A forced kernel
+ * (GEMV_BATCHED_*; the mixed-precision ring only for fp16/bf16); TC takes
+ * param % 1000 as the ring size in KB (32..220; other values keep the dispatcher's
+ * choice), param / 1000 % 10 as the number of K slices (1..8; 0 keeps the choice) and
+ * param / 10000 % 10 as the cluster scheduling preference (1 spread, 2 load
+ * balancing, else the default).  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);

@@ -395,8 +395,11 @@ def test_plan_tensor_cores():
         kt = -(-Kd // 128)  # N = 48: 128-column k-tiles
         assert (p["splits"] - 1) * p["unroll"] < kt <= p["splits"] * p["unroll"], (M, Kd, p)
         assert 1 <= p["splits"] <= 8 and p["workspace_bytes"] == 0, (M, Kd, p)
-    p = g.plan_for("bf16", 4096, 14336, 64)  # 9 slices would fill the wave; a cluster holds 8
-    assert p["splits"] == 8 and p["unroll"] == 14
+    p = g.plan_for("bf16", 4096, 4096, 48)  # 9 slices would fill the wave; a cluster holds 8
+    assert p["splits"] == 8 and p["unroll"] == 4
+    # 64 or more vectors on few row tiles: deep rings, one CTA per SM, SMs / tiles slices
+    p = g.plan_for("f16", 4096, 4096, 256)
+    assert p["splits"] == 4 and p["smem_bytes"] == 4 * (128 + 256) * 128 + 1024
     for dt in ("f32", "w8"):
         with pytest.raises(g.GemvError):
             g.plan_for(dt, 100, 64, 17)
@@ -414,3 +417,28 @@ def test_launch_overlap_modes():
     assert L.gemv_set_launch_overlap(3) == g.ERR_INVALID_VALUE
     assert L.gemv_set_launch_overlap(-1) == g.ERR_INVALID_VALUE
     g.set_launch_overlap("launch")  # the default
+
+
+def test_plan_dispatcher_audit_cases():
+    """Shapes where a forced kernel beat the dispatcher's choice by more than 5 % on a
+    GB300, and the rules that now pick the faster kernel (CUDA-event means, cold L2)."""
+    K = g.KERNELS
+    # fp32, 2 vectors, fewer than 32 rows per SM of >= 2048 chunks: block per row
+    for M, Kd in ((1024, 16384), (2048, 12288), (4096, 14336), (1024, 8192)):
+        assert g.plan_for("f32", M, Kd, 2)["kernel"] == K["block_per_row"], (M, Kd)
+    assert g.plan_for("f32", 8192, 14336, 2)["kernel"] == K["batched"]  # the ring leads here
+    assert g.plan_for("f32", 1024, 16384, 4)["kernel"] == K["batched"]  # 4 vectors: batched
+    assert g.plan_for("f32", 4096, 4096, 2)["kernel"] == K["xsplit"]    # short rows: K split
+    # fp16/bf16, 1 vector, 1..11 rows per SM of 8192..16384 elements: the K-split kernel
+    for dt, M, Kd in (("bf16", 1024, 16384), ("bf16", 256, 16384), ("f16", 1024, 16384), ("bf16", 1536, 16384),
+                      ("bf16", 1024, 8192)):
+        assert g.plan_for(dt, M, Kd, 1)["kernel"] == K["xsplit"], (dt, M, Kd)
+    assert g.plan_for("bf16", 4096, 16384, 1)["kernel"] == K["stream"]  # from 12 rows per SM
+    assert g.plan_for("bf16", 1024, 4096, 1)["kernel"] != K["xsplit"]   # short rows keep theirs
+    # fp16/bf16, 4 vectors, up to 2048 rows: the mixed-precision ring
+    for dt, M, Kd in (("bf16", 1024, 16384), ("bf16", 2048, 16384), ("bf16", 2048, 8192), ("f16", 1024, 16384)):
+        p = g.plan_for(dt, M, Kd, 4)
+        assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING_MIXED, (dt, M, Kd, p)
+    p = g.plan_for("bf16", 4096, 14336, 4)
+    assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR
+

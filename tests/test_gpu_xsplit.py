@@ -75,11 +75,11 @@ def test_xsplit_epilogue(dtype):
 
 
 # Shapes the dispatcher itself sends to the K-split kernel (no forcing): two long
-# 16-bit rows per call, four long fp32 ones, and the fp32 one- and two-vector
-# ranges.  A reordering of the dispatcher's rules that moved them elsewhere, or a
+# 16-bit rows per call, four long fp32 ones, the fp32 one- and two-vector ranges, and
+# one vector of few long 16-bit rows.  A reordering of the dispatcher's rules that moved them elsewhere, or a
 # fault on their launch configuration, fails here.
 AUTO_XSPLIT = [("bf16", 1024, 16384, 2), ("f16", 4096, 8192, 2), ("f32", 2048, 8192, 4),
-               ("f32", 4096, 4096, 1), ("f32", 8192, 4096, 2)]
+               ("f32", 4096, 4096, 1), ("f32", 8192, 4096, 2), ("bf16", 1024, 16384, 1), ("f16", 256, 8192, 1)]
 
 
 @pytest.mark.parametrize("dtype,M,K,B", AUTO_XSPLIT)
@@ -92,3 +92,21 @@ def test_auto_dispatch_takes_xsplit(dtype, M, K, B):
     assert g.last_plan()["kernel_name"] == "xsplit", (dtype, M, K, B, g.last_plan()["kernel_name"])
     torch.cuda.synchronize()
     U.assert_close(dtype, y, y_ref, absdot, with_rounding=True, what=f"auto {dtype} {M}x{K} B={B}")
+
+
+# The other kernels the dispatcher picks for few long rows: block per row for two
+# fp32 vectors, the mixed-precision ring for four 16-bit vectors.
+@pytest.mark.parametrize("dtype,M,K,B,kernel,variant", [("f32", 1024, 8192, 2, "block_per_row", None),
+                                                        ("f32", 600, 12288, 2, "block_per_row", None),
+                                                        ("bf16", 1024, 8192, 4, "batched", g.BATCHED_RING_MIXED),
+                                                        ("f16", 2000, 4104, 3, "batched", g.BATCHED_RING_MIXED)])
+def test_auto_dispatch_few_long_rows(dtype, M, K, B, kernel, variant):
+    w = W.small(dtype, M, K, B, True, seed=M + K + B)
+    inp = W.make_inputs(w)
+    y_ref, absdot = U.oracle_for(dtype, inp)
+    y = U.run_gpu(dtype, U.to_device(inp), M, K, B)
+    p = g.last_plan()
+    assert p["kernel_name"] == kernel and (variant is None or p["variant"] == variant), p
+    torch.cuda.synchronize()
+    U.assert_close(dtype, y, y_ref, absdot, with_rounding=True, what=f"auto {dtype} {M}x{K} B={B} {kernel}")
+
