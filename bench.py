@@ -53,9 +53,12 @@ METRIC = "GEMV achieved HBM GB/s (cold L2) & % of GB300 peak; µs per y=A·x"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# the kernel code and its launch configuration: the DRAM traffic of a committed
-# ncu capture is reported only while their code (comments aside) is unchanged
-KERNEL_SOURCES = ["gemv_kernels.cuh", "gemv_launch.cuh", "gemv_plan.cpp"]
+# What the step's kernel is made of: the CUDA-core kernels' source and the launcher of
+# its family (comments stripped), and the launch configuration the dispatcher picks
+# for the workload.  The DRAM traffic of a committed ncu capture is reported only
+# while these are unchanged.
+KERNEL_SOURCE = "gemv_kernels.cuh"
+LAUNCH_SOURCE = ("gemv_launch.cuh", "cudaError_t launch_rowteam(")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 HEADLINE_DESC = "bf16 GEMV y = A.x, A 128256x4096 row-major (1.05 GB), B = 1, no bias: 1 GEMV per step"
 FP32_STEP_DESC = "f32 GEMV + bias at M=16384 over K in {16, 32, 4096}: 3 GEMVs per step"
@@ -111,19 +114,30 @@ def code_only(src: str) -> str:
     return " ".join(src.split())
 
 
-def kernel_sha() -> str:
+def kernel_sha(workload: str) -> str:
+    """Hash of the step kernel's code and of its launch configuration for `workload`."""
+    csrc = os.path.join(ROOT, "decode_linear_layers_gb300", "csrc")
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_linear_layers_gb300", "csrc", f), encoding="utf-8") as fh:
-            h.update(code_only(fh.read()).encode())
+    with open(os.path.join(csrc, KERNEL_SOURCE), encoding="utf-8") as fh:
+        h.update(code_only(fh.read()).encode())
+    with open(os.path.join(csrc, LAUNCH_SOURCE[0]), encoding="utf-8") as fh:
+        src = fh.read()
+    i = src.index(LAUNCH_SOURCE[1])
+    j = src.find("\ntemplate", i)
+    h.update(code_only(src[i:j if j >= 0 else len(src)]).encode())
+    import decode_linear_layers_gb300 as g
+
+    w = W.BY_NAME[workload]
+    plan = g.plan_for(w.dtype, w.M, w.K, w.B)
+    h.update(json.dumps({k: plan[k] for k in sorted(plan) if k != "kernel_name"}, sort_keys=True).encode())
     return h.hexdigest()[:16]
 
 
 def read_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it is for this source."""
+    """DRAM bytes per launch from the committed ncu summary, if it is for this kernel."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    sha = kernel_sha()
+    sha = kernel_sha(workload)
     cur = None
     for line in open(TRAFFIC_FILE):
         parts = line.split()

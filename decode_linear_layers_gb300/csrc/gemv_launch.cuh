@@ -240,7 +240,8 @@ cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *, cudaStream_t
   } else {
     if (p.nb < 16 || p.nb > kTcMaxN || p.nb % 16 != 0 || p.splits < 1 || p.splits > kTcMaxCluster)
       return cudaErrorInvalidValue;
-    const int ka = tc_atoms(p.nb), sb = tc_stage_bytes(p.nb, ka), stages = (p.smem_bytes - 1024) / sb;
+    const int ka = p.rows_per_warp == 1 || p.rows_per_warp == 2 ? p.rows_per_warp : tc_atoms(p.nb);
+    const int sb = tc_stage_bytes(p.nb, ka), stages = (p.smem_bytes - 1024) / sb;
     if (stages < 2 || stages > kTcMaxStages || p.smem_bytes != stages * sb + 1024) return cudaErrorInvalidValue;
     CUtensorMap map_a, map_x;
     std::memset(&map_a, 0, sizeof map_a);

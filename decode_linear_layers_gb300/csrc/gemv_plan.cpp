@@ -364,14 +364,16 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // slice (p.splits slices of p.unroll k-tiles)
       if (B <= GEMV_MAX_BATCH) p.nb = (B + 15) / 16 * 16;
       const int64_t tiles = ceil_div(M, kTcPlanTileM);
-      const int64_t ktiles = K > 0 ? ceil_div(K, (int64_t)kTcPlanTileK * tc_plan_atoms(p.nb)) : 1;
+      // 64-column swizzle atoms per stage (forced: param / 100000 % 10 in 1..2)
+      const int pa = param / 100000 % 10;
+      const int atoms = pa == 1 || pa == 2 ? pa : tc_plan_atoms(p.nb);
+      const int64_t ktiles = K > 0 ? ceil_div(K, (int64_t)kTcPlanTileK * atoms) : 1;
       // K slices so that all CTAs run in one wave (as many per SM as shared memory
       // allows).  A deep ring (one CTA per SM) for up to 64 vectors while the tiles
       // cover half the SMs or more but not all of them; otherwise two CTAs per SM,
       // which for few tiles doubles the K slices (measured, us: 14336 rows B = 32
       // 30.7 deep against 33.6, B = 64 33.5 against 37.7, B = 128 49.1 against 46.3;
       // 4096 rows B = 64 23.3 against 21.4; 28672 rows B = 32 57.3 against 45.1)
-      // (forced: param >= 32 is the ring size in KB)
       // (and 64 or more vectors on at most a quarter as many tiles as SMs: K slices on
       // deep rings, one CTA per SM; f16 4096x4096 B = 256 34.6 us against 40.1 on two
       // 100 KB rings per SM, B = 64 18.8 against 20.1)
@@ -379,10 +381,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
                         (p.nb >= 64 && 4 * tiles <= num_sms);
       // (forced: param % 1000 in 32..220 is the ring size in KB, param / 1000 % 10 in
       // 1..8 the number of K slices, param / 10000 % 10 the cluster scheduling
-      // preference: 1 spread, 2 load balancing)
+      // preference: 1 spread, 2 load balancing; param / 100000 % 10 the atoms above)
       const int pk = param % 1000, ps = param / 1000 % 10;
       const int ring_kb = pk >= 32 && pk <= 220 ? pk : deep ? 200 : 100;
-      const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb) * tc_plan_stage_bytes(p.nb) + 1024;
+      const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb, atoms) * tc_plan_stage_bytes(p.nb, atoms) + 1024;
       int64_t per_sm = kSmemPerSm / (smem + 1024);
       if (per_sm < 1) per_sm = 1;
       // (the slices of a tile run as one cluster and are summed inside the kernel, so
@@ -399,6 +401,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       p.splits = (int)s;
       p.unroll = (int)per;
       p.lanes_per_row = kTcPlanThreads;
+      p.rows_per_warp = atoms;  // (for this kernel: 64-column atoms per stage)
       p.smem_bytes = (int)smem;
       p.workspace_bytes = 0;
       p.variant = param / 10000 % 10;  // (forced only) cluster scheduling preference

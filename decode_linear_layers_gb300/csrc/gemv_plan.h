@@ -48,17 +48,23 @@ constexpr int xsplit_depth(int J) { return xsplit_rows_per_group(J) * kXsplitGro
 // swizzle atoms along K; as many stages (at most 8) as fit in the ring, plus 1024
 // bytes to align them.
 constexpr int kTcPlanThreads = 128;
+constexpr int kTcPlanMaxStages = 16;  // pipeline stages in one CTA's ring
 // K slices of one row tile run as one thread-block cluster (the portable maximum size)
 constexpr int kTcMaxCluster = 8;
 constexpr int kTcPlanTileM = 128;
 constexpr int kTcPlanTileK = 64;
 // 64-column atoms per stage: two for N <= 64, one above.
 constexpr int tc_plan_atoms(int n) { return n <= 64 ? 2 : 1; }
-constexpr int tc_plan_stage_bytes(int n) { return (kTcPlanTileM + n) * kTcPlanTileK * 2 * tc_plan_atoms(n); }
+constexpr int tc_plan_stage_bytes(int n, int atoms) { return (kTcPlanTileM + n) * kTcPlanTileK * 2 * atoms; }
+constexpr int tc_plan_stage_bytes(int n) { return tc_plan_stage_bytes(n, tc_plan_atoms(n)); }
 // ring_kb: 200 (one CTA per SM, the deeper ring) when the row tiles leave SMs
 // free, 100 (two CTAs per SM) when there are at least as many tiles as SMs.
+constexpr int tc_plan_stages(int n, int ring_kb, int atoms) {
+  return ring_kb * 1024 / tc_plan_stage_bytes(n, atoms) < kTcPlanMaxStages ? ring_kb * 1024 / tc_plan_stage_bytes(n, atoms)
+                                                                          : kTcPlanMaxStages;
+}
 constexpr int tc_plan_stages(int n, int ring_kb) {
-  return ring_kb * 1024 / tc_plan_stage_bytes(n) < 8 ? ring_kb * 1024 / tc_plan_stage_bytes(n) : 8;
+  return tc_plan_stages(n, ring_kb, tc_plan_atoms(n));
 }
 
 // Tensor maps of A (K x M) and x (K x B), 16-bit values, boxes 64 x 128 and 64 x N,

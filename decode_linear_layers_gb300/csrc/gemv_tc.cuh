@@ -33,7 +33,7 @@ namespace gemv {
 constexpr int kTcThreads = 128;  // one warpgroup: warp w reads TMEM lanes 32w..32w+31
 constexpr int kTcM = 128;        // rows per tile (the MMA's M)
 constexpr int kTcK = 64;         // K per stage: one 128-byte swizzle atom of 16-bit values
-constexpr int kTcMaxStages = 8;
+constexpr int kTcMaxStages = 16;
 constexpr int kTcMaxN = 256;
 constexpr int kTcMaxSlices = 8;  // K slices of a tile: one cluster (the portable maximum size)
 

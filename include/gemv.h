@@ -278,7 +278,8 @@ typedef enum gemv_kernel {
 typedef struct gemv_plan {
   int kernel;              /* gemv_kernel_t */
   int lanes_per_row;       /* ROWS_PER_WARP / WARP_PER_ROW / SCALAR: threads per row */
-  int rows_per_warp;       /* BATCHED: rows one warp carries at once */
+  int rows_per_warp;       /* BATCHED: rows one warp carries at once; TC: 64-column
+                              swizzle atoms of K per pipeline stage */
   int splits;              /* SPLIT_K: number of K slices (1 otherwise) */
   int unroll;              /* 16-byte chunks of A in flight per lane per step */
   int x_staging;           /* GEMV_X_GLOBAL / GEMV_X_SMEM / GEMV_X_SMEM_FP32 */
@@ -316,7 +317,8 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
  * param % 1000 as the ring size in KB (32..220; other values keep the dispatcher's
  * choice), param / 1000 % 10 as the number of K slices (1..8; 0 keeps the choice) and
  * param / 10000 % 10 as the cluster scheduling preference (1 spread, 2 load
- * balancing, else the default).  A forced kernel
+ * balancing, else the default) and param / 100000 % 10 as the 64-column atoms of K
+ * per pipeline stage (1 or 2).  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);

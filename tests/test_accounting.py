@@ -96,9 +96,9 @@ def test_inputs_are_seeded_and_shaped():
 
 def test_traffic_record_matches_kernel_sources():
     # profiles/traffic.txt carries the ncu DRAM traffic of the benchmark's step kernel
-    # for the kernel code it was captured from; the record must be for the code as
-    # committed (else the benchmark reports traffic as unknown), and the captured
-    # bytes must be the workload's Q_min within a few percent (no re-reads)
+    # for the kernel code and launch configuration it was captured from; the record
+    # must be for them as committed (else the benchmark reports traffic as unknown), and
+    # the captured bytes must be the workload's Q_min within a few percent (no re-reads)
     import bench
 
     name = W.HEADLINE[0]

@@ -89,7 +89,7 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
         ka = 2 if nb <= 64 else 1
         stage = (128 + nb) * 64 * 2 * ka
         stages = (p["smem_bytes"] - 1024) // stage
-        assert 2 <= stages <= 8 and p["smem_bytes"] == stages * stage + 1024
+        assert 2 <= stages <= 16 and p["smem_bytes"] == stages * stage + 1024
         assert p["grid"] == _cdiv(M, 128)
         ktiles = _cdiv(K, 64 * ka) if K > 0 else 1
         assert p["splits"] * p["unroll"] >= ktiles and (p["splits"] - 1) * p["unroll"] < ktiles
