@@ -18,13 +18,16 @@
 //     fp32, B == 2, >= 8 rows/SM, M < 65536
 //     K >= 8192, M >= one row/SM: fp16/bf16 with B == 2 and M <= 4096, or fp32
 //     with B == 4 and M <= 8192
+//     fp16/bf16, B == 1, K >= 8192, 1..11 rows/SM (1..15 for K >= 12288)
+//   fp32, B == 2, rows of >= 2048 chunks, 2..31 rows/SM -> BLOCK_PER_ROW
 //   BATCHED, when x[0..B) can be staged and rows have >= 32 chunks, for B >= 2,
 //     and for B == 1 of int8 (>= 48 rows/SM) or int4 (>= 16 rows/SM) below 65536
 //     rows with x staged whole: the row-pair kernel for 4..16 vectors with at most
 //     one ring row group per warp, 16 vectors of 16-bit/fp32 rows, 8 vectors of
 //     16-bit rows whose ring would stage x as stored, and x too large for the ring;
 //     otherwise the cp.async ring (mixed-precision FMAs for fp16/bf16 with 2 or 16
-//     vectors), over K slices with a second pass when x does not fit whole
+//     vectors, and with 4 vectors on up to 2048 rows), over K slices with a second
+//     pass when x does not fit whole
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
 //   B == 1, >= 16 rows/SM (fp32) or >= 12 (other types) -> STREAM (persistent
 //     warps), except fp32 rows of >= 1024 chunks whose row walk would leave the
@@ -202,11 +205,14 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // 26.6) and 4 fp32 vectors (8192x8192 46.4 against 52.1 in the ring, 2048x8192
       // 18.5 against 28.5 in the row pairs)
       kernel = GEMV_KERNEL_XSPLIT;
-    } else if (xs_ok && half16 && B == 1 && K >= 8192 && M >= num_sms && M < (int64_t)num_sms * 12) {
-      // one vector of few long 16-bit rows (fewer than the streaming kernel takes): the
-      // K-split kernel spreads each row over a CTA (bf16 1024x16384 12.3 us against 15.1
-      // block per row, 1536x16384 14.4 against 18.4, 1024x8192 10.2 against 11.6, 256x16384
-      // 9.2 against 13.7 split-K; f16 1024x16384 12.3 against 16.2)
+    } else if (xs_ok && half16 && B == 1 && K >= 8192 && M >= num_sms &&
+               M < (int64_t)num_sms * (K >= 12288 ? 16 : 12)) {
+      // one vector of few long 16-bit rows: the K-split kernel spreads each row over a
+      // CTA (bf16 1024x16384 12.3 us against 15.1 block per row, 1536x16384 14.4 against
+      // 18.4, 1024x8192 10.2 against 11.6, 256x16384 9.2 against 13.7 split-K, 2048x14336
+      // 16.4 against 17.7 streaming; f16 1024x16384 12.3 against 16.2; the streaming
+      // kernel from 12 rows per SM of 8192 elements, bf16 2048x8192 12.4 against 14.2 block
+      // per row, and from 16 of longer ones: 4096x14336 24.6 each)
       kernel = GEMV_KERNEL_XSPLIT;
     } else if (dtype == GEMV_DTYPE_F32 && p.nb == 2 && nch >= 2048 && M >= (int64_t)num_sms * 2 &&
                M < (int64_t)num_sms * 32) {

@@ -429,11 +429,13 @@ def test_plan_dispatcher_audit_cases():
     assert g.plan_for("f32", 8192, 14336, 2)["kernel"] == K["batched"]  # the ring leads here
     assert g.plan_for("f32", 1024, 16384, 4)["kernel"] == K["batched"]  # 4 vectors: batched
     assert g.plan_for("f32", 4096, 4096, 2)["kernel"] == K["xsplit"]    # short rows: K split
-    # fp16/bf16, 1 vector, 1..11 rows per SM of 8192..16384 elements: the K-split kernel
+    # fp16/bf16, 1 vector, 1..11 rows per SM of 8192..16384 elements (1..15 from 12288):
+    # the K-split kernel
     for dt, M, Kd in (("bf16", 1024, 16384), ("bf16", 256, 16384), ("f16", 1024, 16384), ("bf16", 1536, 16384),
-                      ("bf16", 1024, 8192)):
+                      ("bf16", 1024, 8192), ("bf16", 2048, 14336)):
         assert g.plan_for(dt, M, Kd, 1)["kernel"] == K["xsplit"], (dt, M, Kd)
-    assert g.plan_for("bf16", 4096, 16384, 1)["kernel"] == K["stream"]  # from 12 rows per SM
+    assert g.plan_for("bf16", 4096, 16384, 1)["kernel"] == K["stream"]  # from 16 rows per SM
+    assert g.plan_for("bf16", 4096, 14336, 1)["kernel"] == K["stream"]
     assert g.plan_for("bf16", 1024, 4096, 1)["kernel"] != K["xsplit"]   # short rows keep theirs
     # fp16/bf16, 4 vectors, up to 2048 rows: the mixed-precision ring
     for dt, M, Kd in (("bf16", 1024, 16384), ("bf16", 2048, 16384), ("bf16", 2048, 8192), ("f16", 1024, 16384)):

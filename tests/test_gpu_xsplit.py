@@ -79,7 +79,8 @@ def test_xsplit_epilogue(dtype):
 # one vector of few long 16-bit rows.  A reordering of the dispatcher's rules that moved them elsewhere, or a
 # fault on their launch configuration, fails here.
 AUTO_XSPLIT = [("bf16", 1024, 16384, 2), ("f16", 4096, 8192, 2), ("f32", 2048, 8192, 4),
-               ("f32", 4096, 4096, 1), ("f32", 8192, 4096, 2), ("bf16", 1024, 16384, 1), ("f16", 256, 8192, 1)]
+               ("f32", 4096, 4096, 1), ("f32", 8192, 4096, 2), ("bf16", 1024, 16384, 1), ("f16", 256, 8192, 1),
+               ("bf16", 2048, 14336, 1)]
 
 
 @pytest.mark.parametrize("dtype,M,K,B", AUTO_XSPLIT)
