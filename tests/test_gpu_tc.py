@@ -171,3 +171,27 @@ def test_tc_bounded_wait_reports_timeout_and_recovers():
     y2 = U.run_gpu("bf16", d, M, K, B)
     assert g.device_status() == (g.SUCCESS, 0)
     U.assert_close("bf16", y2, y_ref, absdot, with_rounding=True, what="tc after a timeout")
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_tc_every_cluster_size(S):
+    """The K slices of a row tile are summed inside one thread-block cluster: CTA r of
+    S owns rows [ceil(128 r / S), ceil(128 (r + 1) / S)), uneven when S does not divide
+    128.  Every size from 1 to 8, forced through the test hook, on a ragged last tile
+    (333 rows), a ragged K (2 S k-tiles of 128, the last one 88 columns) and a batch
+    that is not a multiple of 16 (40 vectors, N = 48), against the oracle and bitwise
+    from call to call."""
+    M, K, B = 333, 256 * S - 40, 40
+    w = W.small("bf16", M, K, B, True, seed=500 + S)
+    inp = W.make_inputs(w)
+    y_ref, absdot = U.oracle_for("bf16", inp)
+    d = U.to_device(inp)
+    g.force_kernel("tc", S * 1000)
+    y1 = U.run_gpu("bf16", d, M, K, B)
+    p = g.last_plan()
+    assert p["kernel_name"] == "tc" and p["splits"] == S, p
+    y2 = U.run_gpu("bf16", d, M, K, B)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y1), _bits(y2)), "results differ between two identical calls"
+    U.assert_close("bf16", y1, y_ref, absdot, with_rounding=True, what=f"tc cluster of {S}")
+    assert g.device_status() == (g.SUCCESS, 0)
