@@ -1271,7 +1271,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   const int64_t nch_all = K / Op::VEC;
   const int64_t nch = nch_all - c0 < chunks_per_split ? nch_all - c0 : chunks_per_split;
   if (nch <= 0) return;  // K = 0 never reaches this kernel; the plan has no empty slice
-  const int64_t nsteps = (nch + 31) / 32;
+  // the slice's x is staged in shared memory, so its chunk and step counts fit 32 bits
+  const int nch32 = (int)nch, nsteps = (nch32 + 31) / 32;
   const int64_t rowb = row_bytes<Op>(K);
   const char *A = reinterpret_cast<const char *>(a.A) + c0 * 16;
   const int64_t k0 = c0 * Op::VEC;  // first element of the slice
@@ -1296,7 +1297,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   // so are the rows' addresses of this lane's step-0 chunk (and int4 group-scale
   // rows), and a step costs one add per row.
   constexpr bool CACHE = NB <= 4;
-  int64_t pg = blockIdx.x + (int64_t)gridDim.x * warp, pj = 0;
+  int64_t pg = blockIdx.x + (int64_t)gridDim.x * warp;
+  int pj = 0;
   const char *pa[CACHE ? R : 1];
   const float *pscale[CACHE && GRP ? R : 1];
   uint32_t plive = 0;  // bit r: row r of group pg exists (none once pg >= groups)
@@ -1315,10 +1317,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   };
   set_rows();
   auto issue = [&](int stage) {
-    const int64_t c = 32 * pj + lane;
-    if (plive != 0 && c < nch) {
+    const int c = 32 * pj + lane;
+    if (plive != 0 && c < nch32) {
       const uint32_t dst = ring_s + (uint32_t)(stage * R * 32 * 16);
-      const int64_t aoff = pj * (32 * 16);
+      const int64_t aoff = (int64_t)(pj * (32 * 16));
       [[maybe_unused]] int64_t goff = 0;
       if constexpr (GRP) goff = ((c0 + c) * Op::VEC) >> a.gshift;
 #pragma unroll
@@ -1477,7 +1479,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
 #pragma unroll
       for (int b = 0; b < NB; ++b) accm[r][b] = 0.f;
     }
-    for (int64_t j = 0; j < nsteps; ++j) {
+    for (int j = 0; j < nsteps; ++j) {
       asm volatile("cp.async.wait_group %0;" ::"n"(G - 1) : "memory");  // this step has landed
       uint4 av[R];
 #pragma unroll
@@ -1490,8 +1492,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
       }
       issue(stage);  // this lane's slots of the stage are free again
       stage = stage + 1 == G ? 0 : stage + 1;
-      const int64_t c = 32 * j + lane;
-      if (c >= nch) continue;
+      const int c = 32 * j + lane;
+      if (c >= nch32) continue;
       const uint32_t xc = xs_s + (uint32_t)c * (uint32_t)WB;
       // int4 with few sums per row group: the chunk's unscaled sums, scaled once
       // after the chunk (one packed FMA per sum pair instead of scaling every weight)
