@@ -17,8 +17,9 @@
 //               kernel), optionally over one K slice of it (split-K pass 1).
 //   k_splitk_reduce  split-K pass 2: sums the slices in slice order.
 //   k_batched2  2 <= B <= 16 (row pairs): x in shared memory as stored, 2 rows per
-//               warp, the next loads in registers; mixed-precision FMAs for 16-bit
-//               rows, packed FMAs for int8/fp32 rows with up to 8 vectors.
+//               warp (4 with 16 vectors of 16-bit rows), the next loads in registers;
+//               mixed-precision FMAs for 16-bit rows, packed FMAs for int8/fp32 rows
+//               with up to 8 vectors.
 //   k_batch_ring  2 <= B <= 16: A through a per-thread cp.async ring, x in shared
 //               memory (fp32 where it fits), R rows per warp, packed FMAs.
 //   k_xsplit    B <= 4: the CTA splits K, x in fp32 registers.
@@ -959,26 +960,31 @@ __global__ void __launch_bounds__(THREADS, 1) k_batched2(const Args a) {
       }
       if (ng != g) break;
     }
-    // the R * NB sums by one reduce-scatter butterfly: lane l ends with sum
-    // l >> (5 - log2 V) (row / NB, vector % NB), replicated over 32 / V lanes
-    constexpr int V = R * NB;
+    // the R * NB sums by reduce-scatter butterflies of V <= 32 sums (RH rows each):
+    // in butterfly h, lane l ends with sum l >> (5 - log2 V) (row h * RH + index /
+    // NB, vector index % NB), replicated over 32 / V lanes
+    constexpr int V = R * NB > 32 ? 32 : R * NB, RH = V / NB;
     constexpr int LOGV = V == 32 ? 5 : V == 16 ? 4 : V == 8 ? 3 : V == 4 ? 2 : 1;
-    static_assert((1 << LOGV) == V, "R * NB must be a power of two up to 32");
-    float v[V];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int b = 0; b < NB; ++b) v[r * NB + b] = kPacked ? acc2[r][b].x + acc2[r][b].y : acc[r][b];
-    const float part = warp_reduce_scatter<V>(v, lane);
+    static_assert((1 << LOGV) == V && R % RH == 0, "R * NB must be a power of two");
     const int idx = lane >> (5 - LOGV);
     const bool owner = (lane & ((32 >> LOGV) - 1)) == 0;
-    if constexpr (SW) {
-      // gate sum b (row 0) sits at lane b * 32 / V, its up sum (row 1) 16 lanes above
-      const float up = __shfl_down_sync(0xffffffffu, part, 16);
-      if (owner && idx < NB && idx < B) epilogue_swiglu<Op>(a, idx, g, part, up);
-    } else {
-      const int r = idx / NB, b = idx % NB;
-      if (owner && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, part);
+#pragma unroll
+    for (int h = 0; h < R / RH; ++h) {
+      float v[V];
+#pragma unroll
+      for (int r = 0; r < RH; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+          v[r * NB + b] = kPacked ? acc2[h * RH + r][b].x + acc2[h * RH + r][b].y : acc[h * RH + r][b];
+      const float part = warp_reduce_scatter<V>(v, lane);
+      if constexpr (SW) {
+        // gate sum b (row 0) sits at lane b * 32 / V, its up sum (row 1) 16 lanes above
+        const float up = __shfl_down_sync(0xffffffffu, part, 16);
+        if (owner && idx < NB && idx < B) epilogue_swiglu<Op>(a, idx, g, part, up);
+      } else {
+        const int r = h * RH + idx / NB, b = idx % NB;
+        if (owner && b < B && g * R + r < M) epilogue_store<Op>(a, b, g * R + r, part);
+      }
     }
     g = ng;
   }

@@ -125,7 +125,9 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
     switch (p.variant) {
       case GEMV_BATCHED_ROWPAIR:
         if constexpr (!Op::GROUPED && NB >= 2) {  // not built for int4's group scales
-          auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, 2, 2, T>;
+          // R rows per warp (SwiGLU: the gate and up row of one output), U chunks each
+          constexpr int R = rowpair_rows(NB, A16 && SX == 2), U = R == 4 ? 1 : 2;
+          auto kern = sw ? k_batched2<Op, NB, 2, 2, T, true> : k_batched2<Op, NB, R, U, T>;
           cudaError_t e = allow_smem(kern, p.smem_bytes);
           if (e != cudaSuccess) return e;
           return launch_k(kern, dim3((unsigned)p.grid), block, (size_t)p.smem_bytes, s, a.pdl, a);

@@ -346,9 +346,9 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       }
       p.variant = v;
       if (v == GEMV_BATCHED_ROWPAIR) {
-        p.rows_per_warp = 2;
+        p.rows_per_warp = rowpair_rows(p.nb, half16);  // (SwiGLU: 2, the gate and up row)
         p.x_staging = GEMV_X_SMEM;
-        p.unroll = 2;
+        p.unroll = p.rows_per_warp == 4 ? 1 : 2;
         p.smem_bytes = (int)((int64_t)p.nb * K * sx);
       } else {
         // ring: R rows per warp, a G = 8 / R step ring; the mixed form reads x as

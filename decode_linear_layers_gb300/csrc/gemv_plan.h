@@ -16,6 +16,13 @@ constexpr int64_t kSmemPerSm = 228 * 1024;
 // Largest x the streaming kernel copies into shared memory.
 constexpr int64_t kStreamSmemMax = 96 * 1024;
 constexpr int kBatchedThreads = 512;
+// Row-pair kernel (GEMV_BATCHED_ROWPAIR): rows per warp.  16 vectors of 16-bit rows
+// take 4 (one chunk per lane in flight per row): each x chunk read from shared
+// memory, and each x half split out of its word, then feeds 4 rows instead of 2
+// (event means on GB300, us: bf16 128256x4096 B = 16 397.1 -> 344.1, 28672x4096
+// 96.0 -> 82.7, 14336x4096 51.2 -> 46.7, f16 4096x4096 21.5 -> 20.5).  Otherwise 2
+// (two chunks per lane in flight per row).
+constexpr int rowpair_rows(int nb, bool mixed16) { return (nb == 16 && mixed16) ? 4 : 2; }
 // BATCHED ring kernel: R rows per warp and a per-thread cp.async ring of G = 8 / R
 // steps: 16 warps x 8 slots x 512 bytes after x.  R = 2 for 16 vectors (the
 // accumulators' registers), for int4 with 3 or more vectors (32 weights per chunk to

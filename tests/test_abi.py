@@ -145,10 +145,14 @@ def test_plan_config_shapes():
     p = g.plan_for("f16", 4096, 4096, 1)
     assert p["kernel"] == K["stream"] and p["unroll"] == 4 and p["x_staging"] == 1
     assert p["smem_bytes"] == 4096 * 2 and p["grid"] == 2 * 152
-    p = g.plan_for("f16", 4096, 4096, 16)   # one row pair per warp: the row-pair kernel
+    p = g.plan_for("f16", 4096, 4096, 16)   # 16 vectors of 16-bit rows: the row-pair kernel, 4 rows per warp
     assert p["kernel"] == K["batched"] and p["nb"] == 16 and p["x_staging"] == 1
     assert p["variant"] == g.BATCHED_ROWPAIR
-    assert p["smem_bytes"] == 16 * 4096 * 2 and p["rows_per_warp"] == 2 and p["grid"] == 152
+    assert p["smem_bytes"] == 16 * 4096 * 2 and p["rows_per_warp"] == 4 and p["unroll"] == 1 and p["grid"] == 152
+    p = g.plan_for("f16", 4096, 4096, 8)    # fewer vectors: 2 rows per warp, 2 chunks each
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["rows_per_warp"] == 2 and p["unroll"] == 2
+    p = g.plan_for("f32", 32768, 2048, 16)  # 16 fp32 vectors: 2 rows per warp
+    assert p["variant"] == g.BATCHED_ROWPAIR and p["rows_per_warp"] == 2
     for M, Kd in ((14336, 4096), (4096, 14336)):
         assert g.plan_for("bf16", M, Kd, 1)["kernel"] == K["stream"]
     p = g.plan_for("bf16", 128256, 4096, 1)

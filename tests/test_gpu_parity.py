@@ -122,6 +122,36 @@ def test_forced_kernel(dtype, kernel, param):
                            what=f"{dtype} {kernel}/{param} M={M} K={K} B={B} bias={bias}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_rowpair_four_rows(dtype):
+    # 16 vectors of 16-bit rows: the row-pair kernel carries 4 rows per warp and sums
+    # them in two reduce-scatter butterflies.  Row counts that leave 1..3 rows in the
+    # last group, vectors 9..16 (the rest zero-padded), one chunk and a ragged chunk
+    # count; forced and by the dispatcher; repeats bitwise equal
+    seed = 500
+    for M in (1, 3, 6, 4097):
+        for K in (8, 4104):
+            for B in (9, 13, 16):
+                bias = (M + B) % 2 == 1
+                w = W.small(dtype, M, K, B, bias, seed=seed)
+                seed += 1
+                inp = W.make_inputs(w)
+                y_ref, absdot = U.oracle_for(dtype, inp)
+                d = U.to_device(inp)
+                for kernel, param in (("batched", 1), ("auto", 0)):
+                    g.force_kernel(kernel, param)
+                    y1 = U.run_gpu(dtype, d, M, K, B)
+                    plan = g.last_plan()
+                    y2 = U.run_gpu(dtype, d, M, K, B)
+                    g.force_kernel("auto")
+                    if kernel == "batched":
+                        assert plan["variant"] == g.BATCHED_ROWPAIR and plan["rows_per_warp"] == 4, plan
+                    torch.cuda.synchronize()
+                    assert torch.equal(y1, y2), "results differ between two identical calls"
+                    U.assert_close(dtype, y1, y_ref, absdot, with_rounding=True,
+                                   what=f"{dtype} {kernel} M={M} K={K} B={B} bias={bias}")
+
+
 @pytest.mark.parametrize("dtype,M,K,B", [("bf16", 4096, 14336, 16), ("w8", 8192, 8192, 16),
                                          ("f16", 3000, 14336, 9), ("bf16", 2500, 30000, 5),
                                          ("f32", 1000, 20000, 12)])
