@@ -178,8 +178,9 @@ __device__ __forceinline__ void tc_st_dsmem_int(const int *p, uint32_t rank, int
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
 }
 // Every thread of every CTA of the cluster: writes before it are visible to the
-// cluster's reads after it.
+// cluster's reads after it.  The barrier is warp-aligned: each warp first reconverges.
 __device__ __forceinline__ void tc_cluster_sync() {
+  __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sh_loaded = sh_consumed = sh_committed = -1;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncwarp();  // lane 0 of warp 0 rejoins its warp: the CTA barrier counts whole warps
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_slot;
@@ -289,6 +291,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sh_consumed = consumed;
     sh_committed = committed;
   }
+  // the two role threads rejoin their warps first: the CTA barrier counts whole warps,
+  // so without this the other lanes of warp 1 would let it complete (and the epilogue
+  // read tensor memory) before the MMA thread has seen its last commit
+  __syncwarp();
   __syncthreads();
   const bool aborted = abort_flag != 0;
   if (aborted) {
@@ -304,6 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         drained = tc_mbar_wait(&full[t % S], (uint32_t)((t / S) & 1), a.timeout_ns);
       if (!drained && a.status != nullptr) atomicOr(a.status, kTcStatusDrain);
     }
+    __syncwarp();
     __syncthreads();
   }
 
@@ -395,6 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncwarp();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
