@@ -152,8 +152,19 @@ __device__ __forceinline__ void tc_commit(uint64_t *b) {
 
 // The tensor-core path's storage types: fp16 (A/B format 0) and bf16 (format 1).
 template <class Op> struct TcFormat { static constexpr bool ok = false, bf16 = false; };
-template <> struct TcFormat<OpF16> { static constexpr bool ok = true, bf16 = false; };
-template <> struct TcFormat<OpBF16> { static constexpr bool ok = true, bf16 = true; };
+template <> struct TcFormat<OpF16> {
+  static constexpr bool ok = true, bf16 = false;
+  // the output's rounding and the residual's widening, as Op::store and Op::x_elem do them
+  __device__ static __forceinline__ unsigned short round(float v) { return __half_as_ushort(__float2half_rn(v)); }
+  __device__ static __forceinline__ float widen(unsigned short h) { return __half2float(__ushort_as_half(h)); }
+};
+template <> struct TcFormat<OpBF16> {
+  static constexpr bool ok = true, bf16 = true;
+  __device__ static __forceinline__ unsigned short round(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  __device__ static __forceinline__ float widen(unsigned short h) { return __uint_as_float((uint32_t)h << 16); }
+};
 
 // A stage holds KA = 1 or 2 swizzle atoms along K (64 or 128 columns): 128 x 64 A
 // boxes, then N x 64 x boxes.  The number of stages comes with the plan (its
@@ -330,16 +341,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nslices = (int)gridDim.y;
   if (nslices == 1) {
     if (!aborted) {
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(c0, r);
-        if (m < M) {
+      // The tile's outputs leave through shared memory (the stages are idle now): each
+      // thread stages its row's values, scale, bias and activation applied, as fp32
+      // [column][row]; then each thread takes 8 consecutive rows of one vector, adds the
+      // residual and rounds once (as epilogue_store does) and writes them with one
+      // 16-byte store instead of eight 2-byte ones.  CW columns per pass.
+      float *stg = reinterpret_cast<float *>(smem);
+      int cw = (stages * (int)st_bytes) / (kTcM * 4);
+      cw = cw / 16 * 16;
+      if (cw > N) cw = N;
+      const bool vec = M % 8 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 &&
+                       (a.residual == nullptr || (reinterpret_cast<uintptr_t>(a.residual) & 15) == 0);
+      for (int c0 = 0; c0 < N; c0 += cw) {
+        const int w = N - c0 < cw ? N - c0 : cw;
+        for (int cc = 0; cc < w; cc += 16) {
+          uint32_t r[16];
+          tmem_ld16(c0 + cc, r);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int b = c0 + j;
-            if (b < B) epilogue_store<Op>(a, b, m, __uint_as_float(r[j]));
+            float v = 0.f;
+            if (m < M) {
+              v = row_value<Op>(a, m, __uint_as_float(r[j]));
+              if (a.act == 1) v = silu(v);
+            }
+            stg[(cc + j) * kTcM + row] = v;
           }
         }
+        __syncthreads();
+        for (int k = tid; k < w * (kTcM / 8); k += kTcThreads) {
+          const int col = k / (kTcM / 8), r0 = (k % (kTcM / 8)) * 8;
+          const int b = c0 + col;
+          const int64_t mm = m0 + r0;
+          if (b >= B || mm >= M) continue;
+          const float4 lo = *reinterpret_cast<const float4 *>(stg + col * kTcM + r0);
+          const float4 hi = *reinterpret_cast<const float4 *>(stg + col * kTcM + r0 + 4);
+          float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          const int64_t i0 = (int64_t)b * M + mm;
+          if (vec) {  // M % 8 == 0: all 8 rows exist
+            if (a.residual != nullptr) {
+              const uint4 rv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(a.residual) + i0);
+              const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                v[e] += TcFormat<Op>::widen((unsigned short)(rw[e / 2] >> (16 * (e & 1))));
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[e] = (uint32_t)TcFormat<Op>::round(v[2 * e]) | ((uint32_t)TcFormat<Op>::round(v[2 * e + 1]) << 16);
+            *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(a.y) + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (mm + e >= M) break;
+              float ve = v[e];
+              if (a.residual != nullptr) ve += Op::x_elem(a.residual, i0 + e);
+              Op::store(a.y, i0 + e, ve);
+            }
+          }
+        }
+        __syncthreads();  // the staging buffer is read before the next columns overwrite it
       }
     }
   } else {

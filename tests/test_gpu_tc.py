@@ -116,6 +116,39 @@ def test_tc_epilogue(dtype):
     U.assert_close_ex(dtype, y, y_ref, absdot, 1, what=f"{dtype} tc silu + residual in place")
 
 
+@pytest.mark.parametrize("dtype", HALF)
+def test_tc_unsplit_epilogue_forms(dtype):
+    # tiles enough to fill the SMs without a K split: the outputs leave through shared
+    # memory, 8 rows of a vector per 16-byte store where M % 8 == 0 and y (and the
+    # residual) are 16-byte aligned, element by element otherwise.  Both forms, with
+    # the activation and a residual (separate and in place), against the oracle; the
+    # bytes around y untouched
+    K, B = 256, 40
+    for M, off, inplace in ((19200, 0, False), (19200, 0, True), (19200, 1, False), (19196, 0, True)):
+        w = W.small(dtype, M, K, B, True, seed=M + off)
+        inp = W.make_inputs(w)
+        xdt = U.out_dtype(dtype)
+        r = (torch.randn(B, M, generator=torch.Generator().manual_seed(off + 9)) * 2).to(xdt)
+        y_ref, _, absdot = oracle.gemv_ex(dtype, W.storage_bits(inp["A"]), W.storage_bits(inp["x"]),
+                                          W.storage_bits(inp["bias"]), None, residual=W.storage_bits(r), act=1,
+                                          nthreads=U.threads())
+        d = U.to_device(inp)
+        n = B * M
+        buf = torch.full((n + 64,), 7, dtype=xdt, device="cuda")
+        y = buf[8 + off:8 + off + n]
+        res = r.cuda()
+        if inplace:
+            y.copy_(res.view(-1))
+            res = y
+        g.gemv_ex(dtype, d["A"], None, d["x"], d["bias"], res.view(-1) if res is not y else y, y, M, K, B, 1)
+        p = g.last_plan()
+        assert p["kernel_name"] == "tc" and p["splits"] == 1, p
+        torch.cuda.synchronize()
+        assert bool((buf[:8 + off] == 7).all()) and bool((buf[8 + off + n:] == 7).all())
+        U.assert_close_ex(dtype, y.view(B, M), y_ref, absdot, 1,
+                          what=f"{dtype} tc unsplit M={M} y offset {off} in place {inplace}")
+
+
 def test_tc_guard_bytes():
     M, K, B = 333, 256, 40
     w = W.small("bf16", M, K, B, False, seed=400)
