@@ -370,9 +370,17 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // slice (p.splits slices of p.unroll k-tiles)
       if (B <= GEMV_MAX_BATCH) p.nb = (B + 15) / 16 * 16;
       const int64_t tiles = ceil_div(M, kTcPlanTileM);
-      // 64-column swizzle atoms per stage (forced: param / 100000 % 10 in 1..2)
+      // More tiles than two CTAs per SM hold at once, unsplit: the persistent form
+      // (one CTA per SM walks its tiles, deep ring, each tile's epilogue behind the next
+      // tile's copies; forced: param / 1000000 % 10 = 1 on, 2 off).  Measured on bf16
+      // 128256x4096 (us, against two CTAs per SM): B = 32 169.3 / 176.7, 64 176.4 /
+      // 188.7, 80 184.4 / 204.8, 128 191.6 / 222.8, 256 253.8 / 304.5.
+      const int pk = param % 1000, ps = param / 1000 % 10, pp = param / 1000000 % 10;
+      const bool persist = K > 0 && ps <= 1 && pp != 2 && (pp == 1 || tiles > 2 * (int64_t)num_sms);
+      // 64-column swizzle atoms per stage (forced: param / 100000 % 10 in 1..2); the
+      // persistent form takes 2 for every N (B = 128: 191.6 us against 266.2 with 1)
       const int pa = param / 100000 % 10;
-      const int atoms = pa == 1 || pa == 2 ? pa : tc_plan_atoms(p.nb);
+      const int atoms = pa == 1 || pa == 2 ? pa : persist ? 2 : tc_plan_atoms(p.nb);
       const int64_t ktiles = K > 0 ? ceil_div(K, (int64_t)kTcPlanTileK * atoms) : 1;
       // K slices so that all CTAs run in one wave (as many per SM as shared memory
       // allows).  A deep ring (one CTA per SM) for up to 64 vectors while the tiles
@@ -388,8 +396,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // (forced: param % 1000 in 32..220 is the ring size in KB, param / 1000 % 10 in
       // 1..8 the number of K slices, param / 10000 % 10 the cluster scheduling
       // preference: 1 spread, 2 load balancing; param / 100000 % 10 the atoms above)
-      const int pk = param % 1000, ps = param / 1000 % 10;
-      const int ring_kb = pk >= 32 && pk <= 220 ? pk : deep ? 200 : 100;
+      const int ring_kb = pk >= 32 && pk <= 220 ? pk : (deep || persist) ? 200 : 100;
       const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb, atoms) * tc_plan_stage_bytes(p.nb, atoms) + 1024;
       int64_t per_sm = kSmemPerSm / (smem + 1024);
       if (per_sm < 1) per_sm = 1;
@@ -407,6 +414,13 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       p.splits = (int)s;
       p.unroll = (int)per;
       p.lanes_per_row = kTcPlanThreads;
+      if (persist) {  // (threads = 192 marks the form; k-tiles per tile in unroll)
+        p.threads = kTcPlanPersistThreads;
+        p.lanes_per_row = kTcPlanPersistThreads;
+        p.grid = tiles < num_sms * per_sm ? tiles : num_sms * per_sm;  // (per_sm: 1 with the deep ring)
+        p.splits = 1;
+        p.unroll = (int)ktiles;
+      }
       p.rows_per_warp = atoms;  // (for this kernel: 64-column atoms per stage)
       p.smem_bytes = (int)smem;
       p.workspace_bytes = 0;

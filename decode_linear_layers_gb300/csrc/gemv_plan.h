@@ -55,6 +55,7 @@ constexpr int xsplit_depth(int J) { return xsplit_rows_per_group(J) * kXsplitGro
 // swizzle atoms along K; as many stages (at most 8) as fit in the ring, plus 1024
 // bytes to align them.
 constexpr int kTcPlanThreads = 128;
+constexpr int kTcPlanPersistThreads = 192;  // the persistent form: copy, MMA and 4 epilogue warps
 constexpr int kTcPlanMaxStages = 16;  // pipeline stages in one CTA's ring
 // K slices of one row tile run as one thread-block cluster (the portable maximum size)
 constexpr int kTcMaxCluster = 8;

@@ -468,4 +468,196 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
 }
 
+
+// ------------------------------------------------------------------ k_tc_persist
+// The same product for more tiles than one wave holds, without a K split: one CTA per
+// SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... with its stage ring running
+// on across tiles.  Warp 0 (lane 0) copies k-tiles, warp 1 (lane 0) issues the MMAs,
+// warps 2..5 run the epilogue.  Two accumulators of ncols columns alternate in tensor
+// memory: while the epilogue warps read tile j's (and store y), the MMAs of tile j + 1
+// fill the other, so a tile's epilogue hides behind the next tile's copies.  "accf"
+// (one arrival: the tile's last MMA commit) hands an accumulator to the epilogue;
+// "acce" (one arrival per epilogue warp) hands it back.  Epilogue warp w reads tensor
+// memory lanes 32 (w mod 4) .. + 31, the lanes a warp of that rank may access.
+constexpr int kTcPThreads = 192;
+
+__device__ __forceinline__ void tc_mbar_arrive(uint64_t *b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(tc_smem_u32(b)) : "memory");
+}
+
+template <class Op, int KA>
+__global__ void __launch_bounds__(kTcPThreads, 1)
+    k_tc_persist(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_x, const Args a,
+                 int N, int stages) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full[kTcMaxStages], empty[kTcMaxStages], accf[2], acce[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;  // set by any role on timeout
+  __shared__ long long sh_loaded, sh_consumed, sh_committed, sh_acc_committed;  // for the drain after an abort
+  pdl_enter(a, false);  // every read (TMA included) after the kernel before has finished
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t M = a.M, K = a.K;
+  const int B = a.B;
+  constexpr int KT = kTcK * KA;  // K per stage
+  const int64_t nkt = (K + KT - 1) / KT;            // k-tiles per row tile (K > 0: the planner's rule)
+  const int64_t ntiles = (M + kTcM - 1) / kTcM;
+  const int64_t my_tiles = (int64_t)blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int64_t total = my_tiles * nkt;             // k-tiles this CTA streams
+  const int S = stages;
+  unsigned char *smem = smem_raw + ((1024u - (tc_smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr uint32_t a_atom = kTcM * kTcK * 2;
+  const uint32_t x_atom = (uint32_t)N * kTcK * 2, a_bytes = a_atom * KA, st_bytes = (a_atom + x_atom) * KA;
+  const uint32_t ncols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;  // per accumulator
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_smem_u32(&tmem_slot)),
+                 "r"(2 * ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc_mbar_init(&full[s], 1);
+      tc_mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc_mbar_init(&accf[b], 1);
+      tc_mbar_init(&acce[b], 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    abort_flag = 0;
+    sh_loaded = sh_consumed = sh_committed = sh_acc_committed = -1;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncwarp();
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_slot;
+  auto stage_a = [&](int s) { return smem + (size_t)s * st_bytes; };
+  volatile int *abort = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {  // producer
+      int64_t loaded = -1;
+      for (int64_t g = 0; g < total; ++g) {
+        const int s = (int)(g % S);
+        if (g >= S && !tc_mbar_wait_or_abort(&empty[s], (uint32_t)(((g - S) / S) & 1), a.timeout_ns, abort)) break;
+        const int64_t j = g / nkt, kt = g - j * nkt;
+        const int32_t m0 = (int32_t)(((int64_t)blockIdx.x + j * gridDim.x) * kTcM);
+        tc_mbar_arrive_expect_tx(&full[s], st_bytes);
+        const int32_t k0 = (int32_t)(kt * KT);
+#pragma unroll
+        for (int jj = 0; jj < KA; ++jj) {
+          tc_tma_2d(stage_a(s) + jj * a_atom, &map_a, k0 + jj * kTcK, m0, &full[s]);
+          tc_tma_2d(stage_a(s) + a_bytes + jj * x_atom, &map_x, k0 + jj * kTcK, 0, &full[s]);
+        }
+        loaded = g;
+      }
+      sh_loaded = loaded;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = tc_idesc(TcFormat<Op>::bf16, N);
+      int64_t consumed = -1, committed = -1, acc_committed = -1;
+      bool ok = true;
+      for (int64_t j = 0; j < my_tiles && ok; ++j) {
+        const int buf = (int)(j & 1);
+        // the epilogue has read this accumulator's previous tile (j - 2)
+        if (j >= 2 && !tc_mbar_wait_or_abort(&acce[buf], (uint32_t)(((j - 2) / 2) & 1), a.timeout_ns, abort)) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        bool stalled = false;
+        for (int64_t kt = 0; kt < nkt; ++kt) {
+          const int64_t g = j * nkt + kt;
+          const int s = (int)(g % S);
+          if (!tc_mbar_wait_or_abort(&full[s], (uint32_t)((g / S) & 1), a.timeout_ns, abort)) {
+            ok = false;
+            break;
+          }
+          consumed = g;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          if (a.test_stall && blockIdx.x == 0 && g == total - 1) {  // test: the last tile never completes
+            stalled = true;
+            continue;
+          }
+          const uint32_t sa = tc_smem_u32(stage_a(s)), sx = sa + a_bytes;
+#pragma unroll
+          for (int jj = 0; jj < KA; ++jj)
+#pragma unroll
+            for (int kk = 0; kk < kTcK / 16; ++kk)
+              tc_mma(tmem + (uint32_t)buf * ncols, tc_smem_desc(sa + jj * a_atom + kk * 32),
+                     tc_smem_desc(sx + jj * x_atom + kk * 32), idesc, (kt > 0 || jj > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+          committed = g;
+        }
+        if (!ok || stalled) break;
+        tc_commit(&accf[buf]);  // arrives once every MMA of the tile has completed
+        acc_committed = j;
+      }
+      sh_consumed = consumed;
+      sh_committed = committed;
+      sh_acc_committed = acc_committed;
+    }
+  } else {
+    // epilogue warps 2..5: tensor memory lanes 32 (warp mod 4) .. + 31
+    const int ew = warp & 3;
+    const int row = ew * 32 + lane;
+    for (int64_t j = 0; j < my_tiles; ++j) {
+      const int buf = (int)(j & 1);
+      // lane 0 waits for the tile's accumulator and the warp follows it (a warp-uniform
+      // decision before the warp-aligned tensor-memory loads)
+      int ok = 0;
+      if (lane == 0) ok = tc_mbar_wait_or_abort(&accf[buf], (uint32_t)((j / 2) & 1), a.timeout_ns, abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int64_t m = ((int64_t)blockIdx.x + j * gridDim.x) * kTcM + row;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+            "%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)buf * ncols + (uint32_t)c0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (m < M) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (c0 + jj < B) epilogue_store<Op>(a, c0 + jj, m, __uint_as_float(r[jj]));
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) tc_mbar_arrive(&acce[buf]);  // this warp is done with the accumulator
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncwarp();  // the role threads rejoin their warps: the CTA barrier counts whole warps
+  __syncthreads();
+  if (abort_flag != 0) {
+    // nothing may be in flight when the CTA frees its tensor memory and exits: the last
+    // committed MMAs (their commit covers all earlier ones), every copy issued but not
+    // waited for, and the last accumulator hand-over
+    if (tid == 0) {
+      if (a.status != nullptr) atomicOr(a.status, kTcStatusMma);
+      const int64_t committed = sh_committed, consumed = sh_consumed, loaded = sh_loaded, accc = sh_acc_committed;
+      bool drained = committed < 0 ||
+                     tc_mbar_wait(&empty[committed % S], (uint32_t)((committed / S) & 1), a.timeout_ns);
+      for (int64_t t = consumed + 1; t <= loaded && drained; ++t)
+        drained = tc_mbar_wait(&full[t % S], (uint32_t)((t / S) & 1), a.timeout_ns);
+      if (drained && accc >= 0) drained = tc_mbar_wait(&accf[accc & 1], (uint32_t)((accc / 2) & 1), a.timeout_ns);
+      if (!drained && a.status != nullptr) atomicOr(a.status, kTcStatusDrain);
+    }
+    __syncwarp();
+    __syncthreads();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * ncols) : "memory");
+  }
+}
+
 }  // namespace gemv

@@ -386,10 +386,13 @@ def test_plan_tensor_cores():
     assert p["splits"] == 2 and p["smem_bytes"] == 3 * (128 + 128) * 128 + 1024
     p = g.plan_for("f16", 4096, 4096, 17)
     assert p["kernel"] == K["tc"] and p["nb"] == 32
-    # at least as many row tiles as SMs: two CTAs per SM, a 100 KB ring
-    p = g.plan_for("bf16", 128256, 4096, 256)
+    # at least as many row tiles as SMs (up to two per SM): two CTAs per SM, a 100 KB ring
+    p = g.plan_for("bf16", 38912, 4096, 256)
     assert p["kernel"] == K["tc"] and p["nb"] == 256 and p["splits"] == 1 and p["workspace_bytes"] == 0
-    assert p["smem_bytes"] == 2 * (128 + 256) * 128 + 1024
+    assert p["smem_bytes"] == 2 * (128 + 256) * 128 + 1024 and p["threads"] == 128
+    # more: the persistent form, one CTA per SM, a deep ring
+    p = g.plan_for("bf16", 128256, 4096, 256)
+    assert p["threads"] == 192 and p["grid"] == 152 and p["smem_bytes"] == 4 * (128 + 256) * 128 + 1024
     p = g.plan_for("bf16", 28672, 4096, 32)
     assert p["smem_bytes"] == 2 * (128 + 32) * 256 + 1024 and p["grid"] == 224 and p["splits"] == 1
     # no empty slice: splits * k-tiles per slice covers K exactly once; at most 8
@@ -421,6 +424,19 @@ def test_launch_overlap_modes():
     assert L.gemv_set_launch_overlap(3) == g.ERR_INVALID_VALUE
     assert L.gemv_set_launch_overlap(-1) == g.ERR_INVALID_VALUE
     g.set_launch_overlap("launch")  # the default
+
+
+def test_plan_tc_persistent():
+    # more 128-row tiles than two CTAs per SM hold (and no K split): the persistent form,
+    # 192 threads, one CTA per SM, k-tiles per tile in unroll, a deep ring
+    for M, persist in ((128256, True), (39040, True), (38912, False), (14336, False)):
+        p = g.plan_for("bf16", M, 4096, 64, num_sms=152)
+        assert p["kernel_name"] == "tc" and p["splits"] == 1, (M, p)
+        if persist:
+            assert p["threads"] == 192 and p["grid"] == 152 and p["unroll"] == 32 and p["smem_bytes"] > 150 * 1024, p
+        else:
+            assert p["threads"] == 128 and p["grid"] == -(-M // 128), p
+    assert g.plan_for("f16", 128256, 0, 64, num_sms=152)["threads"] == 128  # K = 0: the plain kernel
 
 
 def test_plan_dispatcher_audit_cases():

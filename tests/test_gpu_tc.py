@@ -8,7 +8,10 @@
   CUDA-graph capture (the split-K scratch comes from the stream-ordered pool);
 * the kernel forced for B <= 16 (N = 16);
 * bounded waits: a launch that skips one MMA reports GEMV_ERR_DEVICE_TIMEOUT through
-  gemv_get_device_status, without a fault or a hang, and the next launch is normal.
+  gemv_get_device_status, without a fault or a hang, and the next launch is normal;
+* the persistent form (one CTA per SM over its tiles, two accumulators) forced on
+  small and ragged shapes and chosen by the dispatcher for many tiles, with its
+  epilogue and its bounded waits.
 """
 from __future__ import annotations
 
@@ -62,13 +65,17 @@ def test_tc_parity(dtype, B):
 
 
 @pytest.mark.parametrize("dtype,M,K,B", [("bf16", 14336, 4096, 32), ("bf16", 4096, 14336, 128),
-                                         ("f16", 28672, 4096, 64), ("bf16", 6144, 4096, 256)])
+                                         ("f16", 28672, 4096, 64), ("bf16", 6144, 4096, 256),
+                                         ("f16", 40000, 4096, 48)])
 def test_tc_decode_sizes_sampled_rows(dtype, M, K, B):
     w = W.small(dtype, M, K, B, True, seed=5)
     inp = W.make_inputs(w)
     d = U.to_device(inp)
     y = U.run_gpu(dtype, d, M, K, B)
     torch.cuda.synchronize()
+    # more tiles than two CTAs per SM hold: the persistent form (192 threads)
+    p = g.last_plan()
+    assert (p["threads"] == 192) == (-(-M // 128) > 2 * torch.cuda.get_device_properties(0).multi_processor_count), p
     rows = np.sort(np.random.default_rng(0).choice(M, size=192, replace=False))
     sub = {"A": inp["A"][rows], "x": inp["x"], "bias": inp["bias"][rows], "scale": None}
     y_ref, absdot = U.oracle_for(dtype, sub)
@@ -147,6 +154,83 @@ def test_tc_unsplit_epilogue_forms(dtype):
         assert bool((buf[:8 + off] == 7).all()) and bool((buf[8 + off + n:] == 7).all())
         U.assert_close_ex(dtype, y.view(B, M), y_ref, absdot, 1,
                           what=f"{dtype} tc unsplit M={M} y offset {off} in place {inplace}")
+
+
+PERSIST = 1_000_000  # force parameter: the persistent form
+
+
+def _sampled(dtype, inp, y, rows, what):
+    sub = {"A": inp["A"][rows], "x": inp["x"], "bias": None if inp["bias"] is None else inp["bias"][rows],
+           "scale": None}
+    y_ref, absdot = U.oracle_for(dtype, sub)
+    U.assert_close(dtype, y[:, rows], y_ref, absdot, with_rounding=True, what=what)
+
+
+@pytest.mark.parametrize("dtype", HALF)
+@pytest.mark.parametrize("M,K,B", [(60001, 520, 17), (58368, 256, 64), (40000, 1000, 200), (300, 4096, 33)])
+def test_tc_persistent(dtype, M, K, B):
+    # one CTA per SM walking its tiles with two tensor-memory accumulators: several
+    # tiles per CTA (both accumulators reused), a partial last tile, a partial last
+    # k-tile, N from 32 to 208 (the two accumulators take all 512 columns), fewer tiles
+    # than SMs; sampled rows (with the last ones) against the oracle, repeats bitwise equal
+    w = W.small(dtype, M, K, B, (M + B) % 2 == 1, seed=M + B)
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    g.force_kernel("tc", PERSIST)
+    y1 = U.run_gpu(dtype, d, M, K, B)
+    p = g.last_plan()
+    y2 = U.run_gpu(dtype, d, M, K, B)
+    g.force_kernel("auto")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p["threads"] == 192 and p["splits"] == 1 and p["grid"] == min(-(-M // 128), sms), p
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y1), _bits(y2)), "results differ between two identical calls"
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([rng.choice(M, size=min(M, 160), replace=False), np.arange(max(0, M - 40), M)]))
+    _sampled(dtype, inp, y1, rows, f"{dtype} tc persistent M={M} K={K} B={B}")
+    assert g.device_status() == (g.SUCCESS, 0)
+
+
+@pytest.mark.parametrize("dtype", HALF)
+def test_tc_persistent_epilogue(dtype):
+    M, K, B = 40000, 256, 40
+    w = W.small(dtype, M, K, B, True, seed=78)
+    inp = W.make_inputs(w)
+    xdt = U.out_dtype(dtype)
+    r = (torch.randn(B, M, generator=torch.Generator().manual_seed(4)) * 2).to(xdt)
+    y_ref, _, absdot = oracle.gemv_ex(dtype, W.storage_bits(inp["A"]), W.storage_bits(inp["x"]),
+                                      W.storage_bits(inp["bias"]), None, residual=W.storage_bits(r), act=1,
+                                      nthreads=U.threads())
+    d = U.to_device(inp)
+    y = r.cuda()
+    g.force_kernel("tc", PERSIST)
+    g.gemv_ex(dtype, d["A"], None, d["x"], d["bias"], y, y, M, K, B, 1)
+    assert g.last_plan()["threads"] == 192
+    g.force_kernel("auto")
+    U.assert_close_ex(dtype, y, y_ref, absdot, 1, what=f"{dtype} tc persistent silu + residual in place")
+
+
+def test_tc_persistent_bounded_wait():
+    M, K, B = 40000, 512, 32
+    w = W.small("bf16", M, K, B, True, seed=991)
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    assert g.device_status() == (g.SUCCESS, 0)
+    # CTA 0 skips the MMAs of its last k-tile: its epilogue's wait for that tile's
+    # accumulator runs out after 50 ms; the CTA drains and returns, the status word says
+    # so, the other CTAs finish normally, and the next launch is normal
+    g.force_kernel("tc", PERSIST)
+    g.test_stall(True, 50_000_000)
+    y = torch.zeros(B, M, dtype=torch.bfloat16, device="cuda")
+    U.call("bf16", d, y, M, K, B)
+    assert g.last_plan()["threads"] == 192
+    st, bits = g.device_status()
+    assert st == g.ERR_DEVICE_TIMEOUT and bits & 16, (st, bits)
+    g.test_stall(False)
+    y2 = U.run_gpu("bf16", d, M, K, B)
+    g.force_kernel("auto")
+    assert g.device_status() == (g.SUCCESS, 0)
+    _sampled("bf16", inp, y2, np.arange(0, M, 97), "tc persistent after a timeout")
 
 
 def test_tc_guard_bytes():

@@ -55,7 +55,7 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
     assert B <= 16 or (half16 and B <= 256), (dtype, B)
     kern = p["kernel"]
     assert kern in K_.values() and kern != 0
-    assert p["threads"] in (128, 256, 512)
+    assert p["threads"] in (128, 192, 256, 512)
     assert p["grid"] >= 1 and p["splits"] >= 1
     assert 0 <= p["smem_bytes"] <= SMEM_MAX, p
     nch = K // vec
@@ -86,12 +86,18 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
         assert half16 and aligned and K % vec == 0
         nb = p["nb"]
         assert nb % 16 == 0 and 16 <= nb <= 256 and nb >= B
-        ka = 2 if nb <= 64 else 1
+        tiles = _cdiv(M, 128)
+        persist = tiles > 2 * sms and K > 0
+        ka = 2 if nb <= 64 or persist else 1  # (the persistent form: 128-column stages for every N)
         stage = (128 + nb) * 64 * 2 * ka
         stages = (p["smem_bytes"] - 1024) // stage
         assert 2 <= stages <= 16 and p["smem_bytes"] == stages * stage + 1024
-        assert p["grid"] == _cdiv(M, 128)
         ktiles = _cdiv(K, 64 * ka) if K > 0 else 1
+        if persist:
+            # the persistent form: one 192-thread CTA per SM over its tiles, no K split
+            assert p["threads"] == 192 and p["grid"] == sms and p["splits"] == 1 and p["unroll"] == ktiles
+        else:
+            assert p["threads"] == 128 and p["grid"] == tiles
         assert p["splits"] * p["unroll"] >= ktiles and (p["splits"] - 1) * p["unroll"] < ktiles
         # the slices of a row tile are one cluster (at most 8 CTAs), reduced in the kernel
         assert 1 <= p["splits"] <= 8 and p["workspace_bytes"] == 0
