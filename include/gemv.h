@@ -266,7 +266,11 @@ typedef enum gemv_kernel {
                                     N = B rounded up to 16), fp32 accumulators in tensor
                                     memory; when the row tiles are few, up to 8 K slices per
                                     tile run as one thread-block cluster and are summed in
-                                    its distributed shared memory; waits bounded */
+                                    its distributed shared memory; with more tiles than
+                                    two CTAs per SM hold, a persistent form (192 threads,
+                                    one CTA per SM over its tiles, two accumulators so that
+                                    a tile's epilogue overlaps the next tile's copies);
+                                    waits bounded */
 } gemv_kernel_t;
 
 /* Where a kernel reads x from (gemv_plan_t.x_staging). */
@@ -281,10 +285,11 @@ typedef struct gemv_plan {
   int rows_per_warp;       /* BATCHED: rows one warp carries at once; TC: 64-column
                               swizzle atoms of K per pipeline stage */
   int splits;              /* SPLIT_K: number of K slices (1 otherwise) */
-  int unroll;              /* 16-byte chunks of A in flight per lane per step */
+  int unroll;              /* 16-byte chunks of A in flight per lane per step; TC:
+                              k-tiles per K slice (per tile in the persistent form) */
   int x_staging;           /* GEMV_X_GLOBAL / GEMV_X_SMEM / GEMV_X_SMEM_FP32 */
   int nb;                  /* vector count the kernel is built for (>= B, power of 2) */
-  int threads;             /* threads per CTA */
+  int threads;             /* threads per CTA (TC: 192 marks the persistent form) */
   int64_t grid;            /* CTAs of the first (or only) kernel */
   int smem_bytes;          /* dynamic shared memory per CTA */
   int64_t workspace_bytes; /* split-K partial sums (stream-ordered pool) */
@@ -317,8 +322,9 @@ gemv_status_t gemv_plan_for(gemv_dtype_t dtype, int64_t M, int64_t K, int B, int
  * param % 1000 as the ring size in KB (32..220; other values keep the dispatcher's
  * choice), param / 1000 % 10 as the number of K slices (1..8; 0 keeps the choice) and
  * param / 10000 % 10 as the cluster scheduling preference (1 spread, 2 load
- * balancing, else the default) and param / 100000 % 10 as the 64-column atoms of K
- * per pipeline stage (1 or 2).  A forced kernel
+ * balancing, else the default), param / 100000 % 10 as the 64-column atoms of K
+ * per pipeline stage (1 or 2) and param / 1000000 % 10 as the persistent form (1 on
+ * wherever K > 0 and no K split is forced, 2 off).  A forced kernel
  * that cannot handle the arguments (e.g. a vectorised kernel on unaligned rows)
  * falls back to the dispatcher's choice. */
 gemv_status_t gemv_test_force_kernel(int kernel, int param);
@@ -336,7 +342,8 @@ gemv_status_t gemv_test_last_plan(gemv_plan_t *plan);
 gemv_status_t gemv_get_device_status(gemv_stream_t stream, int *bits);
 
 /* TEST ONLY — not thread-safe.  With `stall` != 0 every later GEMV_KERNEL_TC launch
- * skips the last MMA of its first CTA, so that CTA's wait for it runs out after
+ * skips the last MMA of its first CTA (in the persistent form: the MMAs of that CTA's
+ * last k-tile), so that CTA's wait for it runs out after
  * `timeout_ns` (<= 0: the default of 2 s) and gemv_get_device_status reports
  * GEMV_ERR_DEVICE_TIMEOUT.  stall = 0 restores normal launches. */
 gemv_status_t gemv_test_stall(int stall, int64_t timeout_ns);
