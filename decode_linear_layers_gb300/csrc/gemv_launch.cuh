@@ -252,11 +252,13 @@ cudaError_t launch_tc(const gemv_plan_t &p, const Args &a, float *, cudaStream_t
     if (a.K > 0 && !tc_tensor_maps(dt, a.A, a.x, a.M, a.K, a.B, p.nb, &map_a, &map_x)) return cudaErrorInvalidValue;
     if (p.threads == kTcPThreads) {  // the persistent form: one CTA per SM over its tiles
       if (p.splits != 1 || a.K <= 0 || p.grid < 1) return cudaErrorInvalidValue;
+      // the ring, then the epilogue warps' staging buffers
       auto pk = ka == 2 ? k_tc_persist<Op, 2> : k_tc_persist<Op, 1>;
-      cudaError_t e = allow_smem(pk, p.smem_bytes);
+      const int smem = p.smem_bytes + kTcPEpBytes;
+      cudaError_t e = allow_smem(pk, smem);
       if (e != cudaSuccess) return e;
-      return launch_k(pk, dim3((unsigned)p.grid), dim3(kTcPThreads), (size_t)p.smem_bytes, s, a.pdl, map_a, map_x, a,
-                      p.nb, stages);
+      return launch_k(pk, dim3((unsigned)p.grid), dim3(kTcPThreads), (size_t)smem, s, a.pdl, map_a, map_x, a, p.nb,
+                      stages);
     }
     auto kern = ka == 2 ? k_tc<Op, 2> : k_tc<Op, 1>;
     cudaError_t e = allow_smem(kern, p.smem_bytes);

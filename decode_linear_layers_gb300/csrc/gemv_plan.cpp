@@ -396,7 +396,9 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // (forced: param % 1000 in 32..220 is the ring size in KB, param / 1000 % 10 in
       // 1..8 the number of K slices, param / 10000 % 10 the cluster scheduling
       // preference: 1 spread, 2 load balancing; param / 100000 % 10 the atoms above)
-      const int ring_kb = pk >= 32 && pk <= 220 ? pk : (deep || persist) ? 200 : 100;
+      // (the persistent form adds 8 KB of epilogue staging after its ring: at most 200 KB)
+      int ring_kb = pk >= 32 && pk <= 220 ? pk : (deep || persist) ? 200 : 100;
+      if (persist && ring_kb > 200) ring_kb = 200;
       const int64_t smem = (int64_t)tc_plan_stages(p.nb, ring_kb, atoms) * tc_plan_stage_bytes(p.nb, atoms) + 1024;
       int64_t per_sm = kSmemPerSm / (smem + 1024);
       if (per_sm < 1) per_sm = 1;

@@ -480,6 +480,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // "acce" (one arrival per epilogue warp) hands it back.  Epilogue warp w reads tensor
 // memory lanes 32 (w mod 4) .. + 31, the lanes a warp of that rank may access.
 constexpr int kTcPThreads = 192;
+// after the stage ring: each epilogue warp's staging buffer, 16 columns x 32 rows fp32
+constexpr int kTcPEpBytes = 4 * 16 * 32 * 4;
 
 __device__ __forceinline__ void tc_mbar_arrive(uint64_t *b) {
   asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(tc_smem_u32(b)) : "memory");
@@ -603,7 +605,10 @@ __global__ void __launch_bounds__(kTcPThreads, 1)
   } else {
     // epilogue warps 2..5: tensor memory lanes 32 (warp mod 4) .. + 31
     const int ew = warp & 3;
-    const int row = ew * 32 + lane;
+    float *ep = reinterpret_cast<float *>(smem + (size_t)S * st_bytes) + ew * 16 * 32;
+    // 16-byte stores of 8 rows: M a multiple of 8, y and the residual 16-byte aligned
+    const bool vec = M % 8 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 &&
+                     (a.residual == nullptr || (reinterpret_cast<uintptr_t>(a.residual) & 15) == 0);
     for (int64_t j = 0; j < my_tiles; ++j) {
       const int buf = (int)(j & 1);
       // lane 0 waits for the tile's accumulator and the warp follows it (a warp-uniform
@@ -613,7 +618,8 @@ __global__ void __launch_bounds__(kTcPThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int64_t m = ((int64_t)blockIdx.x + j * gridDim.x) * kTcM + row;
+      const int64_t m0w = ((int64_t)blockIdx.x + j * gridDim.x) * kTcM + ew * 32;  // the warp's first row
+      const int64_t m = m0w + lane;
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t r[16];
         asm volatile(
@@ -623,7 +629,47 @@ __global__ void __launch_bounds__(kTcPThreads, 1)
               "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
             : "r"(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)buf * ncols + (uint32_t)c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (m < M) {
+        if (vec) {
+          // the 16 columns of the warp's 32 rows staged as fp32 [column][row] (scale, bias
+          // and activation applied), then per lane 8 rows of one column: residual added,
+          // rounded once, one 16-byte store (as epilogue_store does it, value by value)
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            float v = 0.f;
+            if (m < M) {
+              v = row_value<Op>(a, m, __uint_as_float(r[jj]));
+              if (a.act == 1) v = silu(v);
+            }
+            ep[jj * 32 + lane] = v;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cc = (lane >> 2) + 8 * h, r0 = (lane & 3) * 8;
+            const int b = c0 + cc;
+            const int64_t mm = m0w + r0;
+            if (b < B && mm < M) {  // M % 8 == 0: all 8 rows exist
+              const float4 lo = *reinterpret_cast<const float4 *>(ep + cc * 32 + r0);
+              const float4 hi = *reinterpret_cast<const float4 *>(ep + cc * 32 + r0 + 4);
+              float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              const int64_t i0 = (int64_t)b * M + mm;
+              if (a.residual != nullptr) {
+                const uint4 rv =
+                    *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(a.residual) + i0);
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] += TcFormat<Op>::widen((unsigned short)(rw[e / 2] >> (16 * (e & 1))));
+              }
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                o[e] = (uint32_t)TcFormat<Op>::round(v[2 * e]) | ((uint32_t)TcFormat<Op>::round(v[2 * e + 1]) << 16);
+              *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(a.y) + i0) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          __syncwarp();  // read before the next columns overwrite the buffer
+        } else if (m < M) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
             if (c0 + jj < B) epilogue_store<Op>(a, c0 + jj, m, __uint_as_float(r[jj]));
