@@ -23,7 +23,8 @@
 //   k_batch_ring  2 <= B <= 16: A through a per-thread cp.async ring, x in shared
 //               memory (fp32 where it fits), R rows per warp, packed FMAs.
 //   k_xsplit    B <= 4: the CTA splits K, x in fp32 registers.
-//   k_tc        fp16/bf16, 17..256 vectors: tcgen05 tensor cores (gemv_tc.cuh).
+//   k_tc        fp16/bf16, 17..256 vectors: tcgen05 tensor cores (gemv_tc.cuh; with
+//               many row tiles the persistent k_tc_persist).
 //
 // All reductions are fixed trees (xor butterflies, shared memory in warp order,
 // slices in index order): no atomics, bitwise-reproducible results.

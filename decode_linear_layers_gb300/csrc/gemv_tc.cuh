@@ -22,6 +22,9 @@
 // Every wait on an mbarrier is bounded (globaltimer); on timeout the CTA ORs a bit
 // into the device status word, waits (bounded) for its MMAs and copies in flight,
 // frees its tensor memory and returns.
+//
+// k_tc_persist (below) is the form for more tiles than two CTAs per SM hold: one CTA
+// per SM over its tiles, with copy, MMA and epilogue warps and two accumulators.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (the encoder is fetched from the driver at run time)
