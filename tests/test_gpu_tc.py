@@ -245,13 +245,17 @@ def test_tc_guard_bytes():
     assert bool((buf[:1024] == 7).all()) and bool((buf[1024 + n:] == 7).all())
 
 
-def test_tc_in_cuda_graph():
-    M, K, B = 4096, 4096, 32  # split-K: the slices summed in the kernel (one cluster per tile)
+@pytest.mark.parametrize("M,K,B,persist", [(4096, 4096, 32, False), (40000, 512, 48, True)])
+def test_tc_in_cuda_graph(M, K, B, persist):
+    # split K (the slices summed in the kernel, one cluster per tile) and the persistent
+    # form (two launches back to back: the second's tensor memory and stages after the
+    # first's under the programmatic launch overlap), captured and replayed
     w = W.small("bf16", M, K, B, False, seed=991)
     d = U.to_device(W.make_inputs(w))
     y = torch.empty(B, M, dtype=torch.bfloat16, device="cuda")
     U.call("bf16", d, y, M, K, B)
-    assert g.last_plan()["splits"] > 1
+    p = g.last_plan()
+    assert (p["threads"] == 192 and p["splits"] == 1) if persist else p["splits"] > 1, p
     torch.cuda.synchronize()
     eager = y.clone()
     s = torch.cuda.Stream()
@@ -261,11 +265,14 @@ def test_tc_in_cuda_graph():
     torch.cuda.current_stream().wait_stream(s)
     graph = torch.cuda.CUDAGraph()
     y.zero_()
+    y2 = torch.empty_like(y)
     with torch.cuda.graph(graph):
         U.call("bf16", d, y, M, K, B)
+        U.call("bf16", d, y2, M, K, B)
     graph.replay()
     torch.cuda.synchronize()
-    assert torch.equal(_bits(y), _bits(eager))
+    assert torch.equal(_bits(y), _bits(eager)) and torch.equal(_bits(y2), _bits(eager))
+    assert g.device_status() == (g.SUCCESS, 0)
 
 
 def test_tc_bounded_wait_reports_timeout_and_recovers():
