@@ -82,6 +82,29 @@ def test_tc_decode_sizes_sampled_rows(dtype, M, K, B):
     U.assert_close(dtype, y[:, rows], y_ref, absdot, what=f"{dtype} tc {M}x{K} B={B} sampled rows")
 
 
+@pytest.mark.parametrize("name", [w.name for w in W.TC_CONFIGS])
+def test_tc_configs_full_size_sampled_rows(name):
+    # the benchmark's tensor-core workloads at full size, in the launch configuration
+    # the bench times (split K in clusters, the deep ring, the persistent form):
+    # repeats bitwise equal, 256 sampled rows (the last ones among them) against the oracle
+    w = W.BY_NAME[name]
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    y1 = U.run_gpu(w.dtype, d, w.M, w.K, w.B)
+    p = g.last_plan()
+    y2 = U.run_gpu(w.dtype, d, w.M, w.K, w.B)
+    torch.cuda.synchronize()
+    assert p["kernel_name"] == "tc", p
+    assert torch.equal(_bits(y1), _bits(y2)), "results differ between two identical calls"
+    rng = np.random.default_rng(w.M + w.B)
+    rows = np.unique(np.concatenate([rng.choice(w.M, size=224, replace=False), np.arange(w.M - 32, w.M)]))
+    sub = {"A": inp["A"][rows], "x": inp["x"], "bias": None if inp["bias"] is None else inp["bias"][rows],
+           "scale": None}
+    y_ref, absdot = U.oracle_for(w.dtype, sub)
+    U.assert_close(w.dtype, y1[:, rows], y_ref, absdot, with_rounding=True,
+                   what=f"{name} [threads {p['threads']}, splits {p['splits']}] sampled rows")
+
+
 @pytest.mark.parametrize("dtype", HALF)
 def test_tc_k_zero_and_one_row(dtype):
     M, B = 200, 40
