@@ -641,6 +641,18 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
         with torch.cuda.graph(graph2):
             run()
         plain_graph_ms = timed(graph2.replay)
+        # the weights' first loads issued before each kernel's wait for the one before
+        # (valid here: no kernel of the layer writes a weight)
+        g.set_launch_overlap("weights")
+        side3 = torch.cuda.Stream()
+        side3.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side3):
+            run()
+        torch.cuda.current_stream().wait_stream(side3)
+        graph3 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph3):
+            run()
+        weights_graph_ms = timed(graph3.replay)
     finally:
         g.set_launch_overlap("launch")
     return {"layer": "bf16 B=1: " + ", ".join(f"{n} {M}x{K}" for n, M, K in DECODE_LAYER),
@@ -652,6 +664,8 @@ def decode_layer(args, torch, g, dev, flush, peak, iters=20):
             "graph_frac_of_peak": round(layer_bytes / (graph_ms * 1e-3) / 1e9 / peak, 4),
             "launch_overlap": "programmatic dependent launch (the library's default)",
             "plain_launches": {"eager_us": round(plain_eager_ms * 1e3, 2), "graph_us": round(plain_graph_ms * 1e3, 2)},
+            "weights_prefetch": {"graph_us": round(weights_graph_ms * 1e3, 2),
+                                 "graph_frac_of_peak": round(layer_bytes / (weights_graph_ms * 1e-3) / 1e9 / peak, 4)},
             "fused": dict(fused, graph_frac_of_peak=round(fused["graph_gbs"] / peak, 4))}
 
 
