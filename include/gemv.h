@@ -297,8 +297,9 @@ typedef struct gemv_plan {
 } gemv_plan_t;
 
 /* BATCHED kernel variants (gemv_plan_t.variant; also the force parameter + 1). */
-#define GEMV_BATCHED_ROWPAIR 0    /* x as stored, 2 rows per warp, the next loads in
-                                     registers; mixed-precision FMAs for fp16/bf16,
+#define GEMV_BATCHED_ROWPAIR 0    /* x as stored, 2 rows per warp (4 for 16 vectors of
+                                     fp16/bf16), the next loads in registers;
+                                     mixed-precision FMAs for fp16/bf16,
                                      packed fp32x2 FMAs for int8/fp32 with up to 8
                                      vectors */
 #define GEMV_BATCHED_RING 1       /* A through a per-thread cp.async ring in shared
