@@ -462,7 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (c0 + c + j < B && mm < M) epilogue_store<Op>(a, c0 + c + j, mm, vv[j]);
         }
       }
-      tc_cluster_sync();  // the owners are done reading before the next columns arrive
+      // the owners are done reading before the next columns arrive (after the last
+      // columns no CTA touches a peer's shared memory again: no barrier)
+      if (c0 + cw < N) tc_cluster_sync();
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
