@@ -186,10 +186,20 @@ def _addr(t, elem_size: int, min_elems: int, what: str):
     return t.data_ptr()
 
 
+_current_raw_stream = None  # (torch's current stream of the current device, as a handle)
+
+
 def _stream(stream):
+    global _current_raw_stream
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        # the raw handle straight from torch (a Stream object per call costs microseconds)
+        if _current_raw_stream is None:
+            import torch
+            get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            dev = torch._C._cuda_getDevice
+            _current_raw_stream = ((lambda: get(dev())) if get is not None
+                                   else (lambda: torch.cuda.current_stream().cuda_stream))
+        return _current_raw_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -207,12 +217,22 @@ def _sizes(M, K, B):
     return M, K, B, M * K, B * K, B * M
 
 
+_entry = {}  # entry points by name, looked up once
+
+
+def _fn(name):
+    f = _entry.get(name)
+    if f is None:
+        f = _entry[name] = getattr(lib(), name)
+    return f
+
+
 def _float_gemv(name, esize, A, x, bias, y, M, K, B, stream):
     M, K, B, na, nx, ny = _sizes(M, K, B)
     args = (_addr(A, esize, na, "A"), _addr(x, esize, nx, "x"),
             _addr(bias, esize, M if bias is not None else 0, "bias"),
             _addr(y, esize, ny, "y"))
-    _check(getattr(lib(), name)(*args, M, K, B, _stream(stream)))
+    _check(_fn(name)(*args, M, K, B, _stream(stream)))
 
 
 def gemv_f32(A, x, bias, y, M, K, B, stream=None) -> None:
