@@ -255,7 +255,7 @@ def gemv_w8(A, row_scale, x, bias, y, M, K, B, stream=None) -> None:
     M, K, B, na, nx, ny = _sizes(M, K, B)
     args = (_addr(A, 1, na, "A"), _addr(row_scale, 4, M, "row_scale"), _addr(x, 2, nx, "x"),
             _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
-    _check(lib().gemv_w8(*args, M, K, B, _stream(stream)))
+    _check(_fn("gemv_w8")(*args, M, K, B, _stream(stream)))
 
 
 OVERLAP = {"off": 0, "launch": 1, "weights": 2}
@@ -312,7 +312,7 @@ def gemv_w4(A, group_scale, x, bias, y, M, K, B, stream=None) -> None:
     na, ns = _a_count("w4", M, K)
     args = (_addr(A, 1, na, "A"), _addr(group_scale, 4, ns, "group_scale"), _addr(x, 2, nx, "x"),
             _addr(bias, 2, M if bias is not None else 0, "bias"), _addr(y, 2, ny, "y"))
-    _check(lib().gemv_w4(*args, M, K, B, _stream(stream)))
+    _check(_fn("gemv_w4")(*args, M, K, B, _stream(stream)))
 
 
 def gemv_bf16_splitk_noalloc(A, x, bias, y, M, K, B, stream=None) -> None:
@@ -345,7 +345,7 @@ def gemv_ex(dtype, A, row_scale, x, bias, residual, y, M, K, B, act=ACT_NONE, st
     args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, ns, "row_scale"), _addr(x, sx, nx, "x"),
             _addr(bias, sx, M if bias is not None else 0, "bias"),
             _addr(residual, sx, ny if residual is not None else 0, "residual"), _addr(y, sx, ny, "y"))
-    _check(lib().gemv_ex(DTYPE_CODES[dtype], *args, M, K, B, int(act), _stream(stream)))
+    _check(_fn("gemv_ex")(DTYPE_CODES[dtype], *args, M, K, B, int(act), _stream(stream)))
 
 
 def gemv_swiglu(dtype, A, row_scale, x, bias, y, I, K, B, stream=None) -> None:
@@ -357,4 +357,4 @@ def gemv_swiglu(dtype, A, row_scale, x, bias, y, I, K, B, stream=None) -> None:
     args = (_addr(A, sa, na, "A"), _addr(row_scale, 4, ns, "row_scale"),
             _addr(x, sx, max(0, B * K), "x"), _addr(bias, sx, M2 if bias is not None else 0, "bias"),
             _addr(y, sx, max(0, B * I), "y"))
-    _check(lib().gemv_swiglu(DTYPE_CODES[dtype], *args, I, K, B, _stream(stream)))
+    _check(_fn("gemv_swiglu")(DTYPE_CODES[dtype], *args, I, K, B, _stream(stream)))
