@@ -169,6 +169,36 @@ template <> struct TcFormat<OpBF16> {
   __device__ static __forceinline__ float widen(unsigned short h) { return __uint_as_float((uint32_t)h << 16); }
 };
 
+// 16 accumulator columns of a warp's 32 tensor-memory lanes (this thread's lane):
+// `addr` = tensor memory base + (first lane << 16) + first column.  Warp-aligned.
+__device__ __forceinline__ void tc_tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(addr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// y[i0 .. i0 + 7] of a 16-bit output: v (scale, bias and activation applied) plus the
+// residual's 8 values, each rounded once (as epilogue_store does it value by value),
+// one 16-byte store.  y and the residual 16-byte aligned at i0.
+template <class Op>
+__device__ __forceinline__ void tc_store8(const Args &a, int64_t i0, float (&v)[8]) {
+  if (a.residual != nullptr) {
+    const uint4 rv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(a.residual) + i0);
+    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] += TcFormat<Op>::widen((unsigned short)(rw[e / 2] >> (16 * (e & 1))));
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    o[e] = (uint32_t)TcFormat<Op>::round(v[2 * e]) | ((uint32_t)TcFormat<Op>::round(v[2 * e + 1]) << 16);
+  *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(a.y) + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // A stage holds KA = 1 or 2 swizzle atoms along K (64 or 128 columns): 128 x 64 A
 // boxes, then N x 64 x boxes.  The number of stages comes with the plan (its
 // shared-memory size).
@@ -332,15 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row = warp * 32 + lane;  // this thread's tile row: TMEM lane 32 * warp + lane
   const int64_t m = m0 + row;
   // 16 accumulator columns c0 .. c0 + 15 of this thread's row
-  auto tmem_ld16 = [&](int c0, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-  };
+  auto tmem_ld16 = [&](int c0, uint32_t (&r)[16]) { tc_tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r); };
   const int nslices = (int)gridDim.y;
   if (nslices == 1) {
     if (!aborted) {
@@ -381,18 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
           const int64_t i0 = (int64_t)b * M + mm;
           if (vec) {  // M % 8 == 0: all 8 rows exist
-            if (a.residual != nullptr) {
-              const uint4 rv = *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(a.residual) + i0);
-              const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                v[e] += TcFormat<Op>::widen((unsigned short)(rw[e / 2] >> (16 * (e & 1))));
-            }
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              o[e] = (uint32_t)TcFormat<Op>::round(v[2 * e]) | ((uint32_t)TcFormat<Op>::round(v[2 * e + 1]) << 16);
-            *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(a.y) + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+            tc_store8<Op>(a, i0, v);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -627,13 +638,7 @@ __global__ void __launch_bounds__(kTcPThreads, 1)
       const int64_t m = m0w + lane;
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t r[16];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-            "%15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)buf * ncols + (uint32_t)c0));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tc_tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)buf * ncols + (uint32_t)c0, r);
         if (vec) {
           // the 16 columns of the warp's 32 rows staged as fp32 [column][row] (scale, bias
           // and activation applied), then per lane 8 rows of one column: residual added,
@@ -657,20 +662,7 @@ __global__ void __launch_bounds__(kTcPThreads, 1)
               const float4 lo = *reinterpret_cast<const float4 *>(ep + cc * 32 + r0);
               const float4 hi = *reinterpret_cast<const float4 *>(ep + cc * 32 + r0 + 4);
               float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-              const int64_t i0 = (int64_t)b * M + mm;
-              if (a.residual != nullptr) {
-                const uint4 rv =
-                    *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned short *>(a.residual) + i0);
-                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] += TcFormat<Op>::widen((unsigned short)(rw[e / 2] >> (16 * (e & 1))));
-              }
-              uint32_t o[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                o[e] = (uint32_t)TcFormat<Op>::round(v[2 * e]) | ((uint32_t)TcFormat<Op>::round(v[2 * e + 1]) << 16);
-              *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(a.y) + i0) =
-                  make_uint4(o[0], o[1], o[2], o[3]);
+              tc_store8<Op>(a, (int64_t)b * M + mm, v);
             }
           }
           __syncwarp();  // read before the next columns overwrite the buffer
