@@ -757,17 +757,15 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(const Args a, float *part
   }
 }
 
-// Split-K pass 2: one thread per (b, m); slices summed in index order.
+// Split-K pass 2: one thread per (b, m), vector b = blockIdx.y; slices summed in
+// index order.
 template <class Op>
 __global__ void __launch_bounds__(kThreads) k_splitk_reduce(const Args a, const float *partial,
                                                             int splits) {
   pdl_enter(a, false);  // the partial sums come from the kernel before
   const int64_t M = a.M;
-  const int64_t total = M * a.B;
-  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * kThreads) {
-    const int b = (int)(i / M);
-    const int64_t m = i - (int64_t)b * M;
+  const int b = (int)blockIdx.y;
+  for (int64_t m = (int64_t)blockIdx.x * kThreads + threadIdx.x; m < M; m += (int64_t)gridDim.x * kThreads) {
     float s = 0.f;
     for (int j = 0; j < splits; ++j) s += partial[((int64_t)j * a.B + b) * M + m];
     epilogue_store<Op>(a, b, m, s);
@@ -1040,6 +1038,7 @@ __global__ void __launch_bounds__(THREADS, CPS) k_stream(const Args a) {
   auto row_live = [&](int64_t r) -> bool { return r < M; };
   int64_t row = blockIdx.x + (int64_t)gridDim.x * warp;
   if (SW && row >= half) row = M;  // a pair index past the last pair: no work
+  int64_t unit = warp;  // the row's (pair's) unit index in the CTA: warp + WARPS * j
   int64_t base = 0;
   float gate_val = 0.f;
   uint4 buf[U];
@@ -1170,7 +1169,7 @@ __global__ void __launch_bounds__(THREADS, CPS) k_stream(const Args a) {
     const float s = group_sum<32>(e + o);
     if (lane == 0) {
       const bool up = SW && row >= half;
-      const int64_t t = kStage ? ((up ? row - half : row) - blockIdx.x) / gridDim.x : 0;  // unit index in the CTA
+      const int64_t t = kStage ? unit : 0;
       RowPre p{1.f, 0.f, 0.f};
       if (kStage && staged && t < THREADS) {
         p.bias = ops[up ? 2 : 0][t];
@@ -1184,6 +1183,7 @@ __global__ void __launch_bounds__(THREADS, CPS) k_stream(const Args a) {
       else if (!up) gate_val = v;
       else Op::store(a.y, row - half, silu(gate_val) * v);
     }
+    if (!SW || row >= half) unit += WARPS;  // (with SW: after the pair's up row)
     row = next_row(row);
   }
 }
@@ -1368,12 +1368,26 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   // (with weight prefetch before the launch dependency is resolved, A's first steps go
   // out first and x's copy after the wait, as the newest group)
   const bool x_first = a.pdl != 2;
+  // Both staging loops visit items tid, tid + THREADS, ... of the order [vector (or
+  // vector pair)][quad].  A thread carries its item's (vector, quad) position in 32
+  // bits (the slice's x fits in shared memory) and steps it without dividing: a
+  // 64-bit division per item cost about 3 instructions per weight of A at 4 vectors.
+  const uint32_t nq32 = (uint32_t)nq, nch32u = (uint32_t)nch;
+  const uint32_t step_v = (uint32_t)THREADS / nq32, step_q = (uint32_t)THREADS % nq32;
+  auto advance = [&](uint32_t &v, uint32_t &q) {
+    v += step_v;
+    q += step_q;
+    if (q >= nq32) {
+      q -= nq32;
+      ++v;
+    }
+  };
   auto copy_x = [&]() {
-    for (int64_t i = tid; i < (int64_t)B * nq; i += THREADS) {
-      const int64_t b = i / nq, q = i - b * nq;
-      const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
-      const uint32_t dst = xs_s + (uint32_t)(((b * PPV + w) * nch + c) * WB);
-      const unsigned char *sp = xsrc + (b * K + 4 * q) * SX;
+    uint32_t b = (uint32_t)tid / nq32, q = (uint32_t)tid % nq32;
+    for (; b < (uint32_t)B; advance(b, q)) {
+      const uint32_t c = q / QW, w = q % QW;  // chunk 4q / VEC, quad (4q mod VEC) / 4
+      const uint32_t dst = xs_s + ((b * PPV + w) * nch32u + c) * WB;
+      const unsigned char *sp = xsrc + ((int64_t)b * K + 4 * (int64_t)q) * SX;
       if constexpr (WB == 16)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(sp) : "memory");
       else
@@ -1419,43 +1433,44 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
         widen4(v.x, v.y, f, typename Op::TX());
       }
     };
-    constexpr int NV = PAIRS ? NP : NB;  // items per quad index: vector pairs or vectors
-    const int64_t items = (int64_t)NV * nq;
-    for (int64_t i0 = tid; i0 < items; i0 += 8 * THREADS) {
+    constexpr uint32_t NV = PAIRS ? NP : NB;  // items per quad index: vector pairs or vectors
+    uint32_t iv = (uint32_t)tid / nq32, q = (uint32_t)tid % nq32;
+    while (iv < NV) {
+      // the loads of 8 items, then (walking the same 8 positions again) their stores
+      const uint32_t iv0 = iv, q0 = q;
       uint4 v0[8], v1[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int64_t i = i0 + (int64_t)u * THREADS;
         v0[u] = make_uint4(0, 0, 0, 0);
         v1[u] = make_uint4(0, 0, 0, 0);
-        if (i < items) {
-          const int64_t iv = i / nq, q = i - iv * nq;
+        if (iv < NV) {
           v0[u] = load_quad(PAIRS ? 2 * iv : iv, q);
           if (PAIRS) v1[u] = load_quad(2 * iv + 1, q);
         }
+        advance(iv, q);
       }
+      iv = iv0;
+      q = q0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t i = i0 + (int64_t)u * THREADS;
-        if (i >= items) continue;
-        const int64_t iv = i / nq, q = i - iv * nq;
-        const int64_t c = (4 * q) / Op::VEC, w = ((4 * q) % Op::VEC) / 4;
+      for (int u = 0; u < 8; ++u, advance(iv, q)) {
+        if (iv >= NV) continue;
+        const uint32_t c = q / QW, w = q % QW;
         if constexpr (PAIRS && XE == 4) {
           float f0[4], f1[4];
           to_f32(v0[u], f0);
           to_f32(v1[u], f1);
-          unsigned char *d0 = smem + ((iv * PPV + 2 * w) * nch + c) * WB;
+          unsigned char *d0 = smem + ((iv * PPV + 2 * w) * nch32u + c) * WB;
           *reinterpret_cast<float4 *>(d0) = make_float4(f0[0], f1[0], f0[1], f1[1]);
           *reinterpret_cast<float4 *>(d0 + pstride) = make_float4(f0[2], f1[2], f0[3], f1[3]);
         } else if constexpr (PAIRS) {
-          unsigned char *d = smem + ((iv * PPV + w) * nch + c) * WB;
+          unsigned char *d = smem + ((iv * PPV + w) * nch32u + c) * WB;
           *reinterpret_cast<uint4 *>(d) =
               make_uint4(__byte_perm(v0[u].x, v1[u].x, 0x5410), __byte_perm(v0[u].x, v1[u].x, 0x7632),
                          __byte_perm(v0[u].y, v1[u].y, 0x5410), __byte_perm(v0[u].y, v1[u].y, 0x7632));
         } else {  // widened to fp32, one vector's quads
           float f0[4];
           to_f32(v0[u], f0);
-          unsigned char *d = smem + ((iv * PPV + w) * nch + c) * WB;
+          unsigned char *d = smem + ((iv * PPV + w) * nch32u + c) * WB;
           *reinterpret_cast<float4 *>(d) = make_float4(f0[0], f0[1], f0[2], f0[3]);
         }
       }

@@ -114,11 +114,10 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
       e = launch_k(kern, dim3((unsigned)p.grid, (unsigned)p.splits), block, (size_t)p.smem_bytes, s, a.pdl, a,
                    p.splits > 1 ? ws : nullptr, cps);
       if (e != cudaSuccess || p.splits == 1) return e;
-      const int64_t total = a.M * a.B;
-      int64_t g = (total + kThreads - 1) / kThreads;
+      int64_t g = (a.M + kThreads - 1) / kThreads;  // (b, m): grid row b, m grid-strided
       if (g > 65535) g = 65535;
-      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
-                      p.splits);
+      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g, (unsigned)a.B), dim3(kThreads), 0, s, a.pdl, a,
+                      (const float *)ws, p.splits);
     };
     constexpr int SX = (int)sizeof(typename Op::TX);
     constexpr bool A16 = sizeof(typename Op::TA) == 2;  // mixed-precision FMAs need 16-bit A
@@ -215,11 +214,10 @@ cudaError_t launch_nb(const gemv_plan_t &p, const Args &a, float *ws, cudaStream
       cudaError_t e = launch_k(k_blockrow<Op, NB, kUnrollBlockRow>, dim3((unsigned)p.grid, (unsigned)p.splits),
                                dim3(kThreads), 0, s, a.pdl, a, ws, per);
       if (e != cudaSuccess) return e;
-      const int64_t total = a.M * a.B;
-      int64_t g = (total + kThreads - 1) / kThreads;
+      int64_t g = (a.M + kThreads - 1) / kThreads;  // (b, m): grid row b, m grid-strided
       if (g > 65535) g = 65535;
-      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g), dim3(kThreads), 0, s, a.pdl, a, (const float *)ws,
-                      p.splits);
+      return launch_k(k_splitk_reduce<Op>, dim3((unsigned)g, (unsigned)a.B), dim3(kThreads), 0, s, a.pdl, a,
+                      (const float *)ws, p.splits);
     }
     case GEMV_KERNEL_BATCHED:
       return launch_batched<Op, NB>(p, a, ws, s);
