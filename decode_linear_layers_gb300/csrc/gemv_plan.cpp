@@ -311,10 +311,17 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // measured faster (GB300, event means in us, clean-L2 flush), else the ring,
       // with mixed-precision FMAs for fp16/bf16 with 2 vectors (bf16 14336x4096
       // B = 2 23.9 against 26.6 packed) and packed FMAs otherwise.  Row pair:
-      // - 4..16 vectors (int8: 2..16) with at most one ring row group per warp, fp32
-      //   excepted (int8 8192x8192 B = 4 28.6 against 30.7 ring, 4096x4096 B = 2 10.3
-      //   against 12.3, f16 6144x4096 B = 8 20.6 against 22.5; fp32 8192x4096 B = 8
-      //   32.9 against 30.6 ring);
+      // - at most one row pair per warp (M <= 2 x 16 x SMs) with 4..16 vectors (int8:
+      //   2..16), fp32 with 3..4 vectors excepted (bf16 4096x4096 B = 4 13.1 against
+      //   14.1 ring, 4096x8192 20.3 against 21.3; int8 4096x4096 B = 2 10.3 against
+      //   12.3, 2048x8192 B = 4 12.3 against 16.2; fp32 4096x4096 B = 8 20.2 against
+      //   20.8, but B = 4 19.5 against 16.6 ring, 2048x4096 16.6 against 12.9);
+      // - above that, at most one ring row group per warp (M <= 4 x 16 x SMs) for 4
+      //   vectors of int8 and 5..8 of fp16/bf16 (int8 8192x8192 B = 4 26.4 against
+      //   27.3 ring; bf16 8192x8192 B = 8 36.9 against 40.9).  The ring takes the
+      //   other shapes of that range since its x staging lost its divisions: bf16
+      //   6144x4096 B = 4 16.1 against 18.5, 8192x8192 B = 4 30.5 against 32.6; int8
+      //   6144x4096 B = 2 12.3 against 14.4, 9216x4096 B = 8 24.6 against 26.6;
       // - 16 vectors of fp16/bf16/fp32 whenever x fits (bf16 14336x4096 53.2 against
       //   61.4 mixed ring, 128256x4096 409.6 against 450.6, fp32 32768x2048 75.8
       //   against 82.0; int8 14336x4096 is a tie and keeps the ring);
@@ -324,6 +331,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
       // - x too large for the ring, or for its whole K (the ring's slices).
       const int64_t ring_group_rows = ring_rows(p.nb, dtype == GEMV_DTYPE_W4, dtype == GEMV_DTYPE_F32);
       const bool one_group_per_warp = M <= (int64_t)num_sms * 16 * ring_group_rows;
+      const bool one_pair_per_warp = M <= (int64_t)num_sms * 16 * 2;
       int v;
       if (param != 0) {
         v = param - 1;
@@ -335,9 +343,10 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         v = GEMV_BATCHED_RING_MIXED;
       } else if (rstage < 0 ||
                  (rowpair_ok &&
-                  (rslices > 1 || (p.nb >= 4 && M <= (int64_t)num_sms * 16 * 2) ||
-                   ((p.nb >= 4 || (dtype == GEMV_DTYPE_W8 && p.nb >= 2)) && dtype != GEMV_DTYPE_F32 &&
-                    one_group_per_warp) ||
+                  (rslices > 1 ||
+                   (one_pair_per_warp && (p.nb >= 8 || (p.nb == 4 && dtype != GEMV_DTYPE_F32) ||
+                                          (dtype == GEMV_DTYPE_W8 && p.nb >= 2))) ||
+                   (one_group_per_warp && ((dtype == GEMV_DTYPE_W8 && p.nb == 4) || (half16 && p.nb == 8))) ||
                    (p.nb == 16 && dtype != GEMV_DTYPE_W8) ||
                    (p.nb == 8 && half16 && rstage == GEMV_X_SMEM)))) {
         v = GEMV_BATCHED_ROWPAIR;

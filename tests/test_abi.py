@@ -232,7 +232,8 @@ def test_plan_batched_staging():
     assert g.plan_for("w8", 14336, 4096, 2)["variant"] == g.BATCHED_RING
     p = g.plan_for("bf16", 16384, 4096, 8)  # vector pairs, 4 rows per warp, 2-step ring
     assert p["variant"] == g.BATCHED_RING and p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["unroll"] == 2
-    # up to one ring row group per warp (M <= 4 x 16 x 152), fp32 excepted: the row pairs
+    # up to one ring row group per warp (M <= 4 x 16 x 152), 8 vectors of fp16/bf16 and
+    # 4 of int8: the row pairs
     assert g.plan_for("bf16", 8192, 4096, 8)["variant"] == g.BATCHED_ROWPAIR
     assert g.plan_for("f32", 8192, 4096, 8)["variant"] == g.BATCHED_RING
     # 8 vectors of fp16/bf16 whose ring would read x as stored (fp32 x 192 KB): row pairs
@@ -463,4 +464,24 @@ def test_plan_dispatcher_audit_cases():
         assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING_MIXED, (dt, M, Kd, p)
     p = g.plan_for("bf16", 4096, 14336, 4)
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR
+    # 3..4 fp32 vectors up to one row pair per warp: the ring (fp32 4096x4096 B = 4
+    # 16.6 us against 19.5 in the row pairs, 2048x4096 12.9 against 16.6)
+    for M, B in ((1024, 4), (2048, 4), (4096, 4), (4096, 3)):
+        p = g.plan_for("f32", M, 4096, B)
+        assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING, (M, B, p)
+    assert g.plan_for("f32", 4096, 4096, 8)["variant"] == g.BATCHED_ROWPAIR  # 8 vectors keep them
+    # beyond one row pair per warp: the ring for 4 vectors of fp16/bf16 and 2 or 8 of
+    # int8 (bf16 8192x8192 B = 4 30.5 against 32.6, 6144x4096 16.1 against 18.5; int8
+    # 6144x4096 B = 2 12.3 against 14.4, 9216x4096 B = 8 24.6 against 26.6) ...
+    for dt, M, Kd, B in (("bf16", 8192, 8192, 4), ("bf16", 6144, 4096, 4), ("f16", 6144, 4096, 4),
+                         ("bf16", 9216, 4096, 3), ("w8", 6144, 4096, 2), ("w8", 9216, 4096, 8), ("w8", 8192, 8192, 8)):
+        p = g.plan_for(dt, M, Kd, B)
+        assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING, (dt, M, Kd, B, p)
+    # ... while 4 vectors of int8 and 8 of fp16/bf16 keep the row pairs up to one ring
+    # row group per warp (int8 8192x8192 B = 4 26.4 against 27.3, bf16 8192x8192 B = 8
+    # 36.9 against 40.9), as do all of these up to one row pair per warp
+    for dt, M, Kd, B in (("w8", 8192, 8192, 4), ("bf16", 8192, 8192, 8), ("w8", 4096, 4096, 4),
+                         ("bf16", 4096, 4096, 4), ("w8", 4096, 8192, 2), ("bf16", 4096, 4096, 8)):
+        p = g.plan_for(dt, M, Kd, B)
+        assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR, (dt, M, Kd, B, p)
 
