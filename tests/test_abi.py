@@ -257,9 +257,11 @@ def test_plan_batched_staging():
     p = g.plan_for("bf16", 4096, 14336, 16)   # 1792 chunks in 3 slices of 598
     assert p["variant"] == g.BATCHED_RING_MIXED and p["splits"] == 3 and p["grid"] == 50
     assert p["smem_bytes"] == 16 * 598 * 8 * 2 + ring and p["workspace_bytes"] == 3 * 16 * 4096 * 4
-    p = g.plan_for("bf16", 4096, 14336, 8)    # 8 x 14336 bf16 (229 KB): two slices
-    assert p["variant"] == g.BATCHED_RING and p["splits"] == 2 and p["x_staging"] == 1
+    p = g.plan_for("bf16", 4096, 14336, 8)    # 8 x 14336 bf16 (229 KB): two slices, mixed FMAs
+    assert p["variant"] == g.BATCHED_RING_MIXED and p["splits"] == 2 and p["x_staging"] == 1
     assert p["smem_bytes"] == 8 * 7168 * 2 + ring
+    p = g.plan_for("bf16", 1024, 16384, 8)
+    assert p["variant"] == g.BATCHED_RING_MIXED and p["splits"] == 2
     p = g.plan_for("bf16", 4096, 14336, 4)    # the row-pair kernel's x fits (115 KB)
     assert p["variant"] == g.BATCHED_ROWPAIR and p["splits"] == 1
     # padded vectors are staged too (zeros): B = 3 and B = 9 stage 4 and 16 vectors

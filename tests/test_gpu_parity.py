@@ -154,7 +154,7 @@ def test_rowpair_four_rows(dtype):
 
 @pytest.mark.parametrize("dtype,M,K,B", [("bf16", 4096, 14336, 16), ("w8", 8192, 8192, 16),
                                          ("f16", 3000, 14336, 9), ("bf16", 2500, 30000, 5),
-                                         ("f32", 1000, 20000, 12)])
+                                         ("f32", 1000, 20000, 12), ("bf16", 1024, 16384, 8)])
 def test_batched_k_slices(dtype, M, K, B):
     # x[0..B) too large to stage whole: the ring over K slices, partial sums and a
     # fixed-order second pass (sampled rows against the oracle, with bias; repeats
