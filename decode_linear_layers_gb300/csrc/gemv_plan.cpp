@@ -22,12 +22,13 @@
 //   fp32, B == 2, rows of >= 2048 chunks, 2..31 rows/SM -> BLOCK_PER_ROW
 //   BATCHED, when x[0..B) can be staged and rows have >= 32 chunks, for B >= 2,
 //     and for B == 1 of int8 (>= 48 rows/SM) or int4 (>= 16 rows/SM) below 65536
-//     rows with x staged whole: the row-pair kernel for 4..16 vectors with at most
-//     one ring row group per warp, 16 vectors of 16-bit/fp32 rows, 8 vectors of
-//     16-bit rows whose ring would stage x as stored, and x too large for the ring;
-//     otherwise the cp.async ring (mixed-precision FMAs for fp16/bf16 with 2 or 16
-//     vectors, and with 4 vectors on up to 2048 rows), over K slices with a second
-//     pass when x does not fit whole
+//     rows with x staged whole: the row-pair kernel for at most one row pair per
+//     warp with 4..16 vectors (int8 2..16, fp32 5..16), for at most one ring row
+//     group per warp with 4 int8 or 5..8 fp16/bf16 vectors, for 16 vectors of
+//     16-bit/fp32 rows, 8 vectors of 16-bit rows whose ring would stage x as stored,
+//     and x too large for the ring; otherwise the cp.async ring (mixed-precision FMAs
+//     for fp16/bf16 with 2 or 16 vectors, 5..8 over K slices, and 4 vectors on up to
+//     2048 rows), over K slices with a second pass when x does not fit whole
 //   M >= 65536                            -> WARP_PER_ROW (non-persistent grid)
 //   B == 1, >= 16 rows/SM (fp32) or >= 12 (other types) -> STREAM (persistent
 //     warps), except fp32 rows of >= 1024 chunks whose row walk would leave the
