@@ -1293,6 +1293,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
   const int64_t xbytes = (int64_t)(PAIRS ? NP : NB) * PPV * pstride;
   const uint32_t xs_s = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t ring_s = xs_s + (uint32_t)xbytes + (uint32_t)((warp * G * R * 32 + lane) * 16);
+  // Shared-memory reads of the ring slots and of x.  int4 (except 8 vectors) uses
+  // plain loads, which the compiler schedules freely (the copies' waits and issues,
+  // inline assembly with a memory clobber, still order them); the inline-assembly
+  // loads made it spill: int4 8192x8192 B = 16 93.4 -> 76.8 us, B = 4 32.7 -> 30.9
+  // (event means).  8 int4 vectors (45.6 -> 47.0) and the other types (int8
+  // 8192x8192 B = 8 39.9 -> 41.0) keep the assembly loads.
+  constexpr bool PLAIN_LDS = Op::GROUPED && NB != 8;
+  auto ld16 = [&](uint32_t s) -> uint4 {
+    if constexpr (PLAIN_LDS) return *reinterpret_cast<const uint4 *>(smem + (s - xs_s));
+    else return lds16(s);
+  };
+  auto ld8 = [&](uint32_t s) -> uint2 {
+    if constexpr (PLAIN_LDS) return *reinterpret_cast<const uint2 *>(smem + (s - xs_s));
+    else return lds8(s);
+  };
   // int4: each slot's group scale, in a second ring [warp][stage][row][lane] of floats
   constexpr bool GRP = Op::GROUPED;
   const uint32_t sc_s = xs_s + (uint32_t)xbytes + (uint32_t)(WARPS * G * R * 32 * 16) +
@@ -1505,12 +1520,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
       asm volatile("cp.async.wait_group %0;" ::"n"(G - 1) : "memory");  // this step has landed
       uint4 av[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) av[r] = lds16(ring_s + (uint32_t)((stage * R + r) * 32 * 16));
+      for (int r = 0; r < R; ++r) av[r] = ld16(ring_s + (uint32_t)((stage * R + r) * 32 * 16));
       float gsc[GRP ? R : 1];
       if constexpr (GRP) {
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(gsc[r]) : "r"(sc_s + (uint32_t)((stage * R + r) * 32 * 4)));
+        for (int r = 0; r < R; ++r) {
+          const uint32_t sa = sc_s + (uint32_t)((stage * R + r) * 32 * 4);
+          if constexpr (PLAIN_LDS) gsc[r] = *reinterpret_cast<const float *>(smem + (sa - xs_s));
+          else asm volatile("ld.shared.f32 %0, [%1];" : "=f"(gsc[r]) : "r"(sa));
+        }
       }
       issue(stage);  // this lane's slots of the stage are free again
       stage = stage + 1 == G ? 0 : stage + 1;
@@ -1543,7 +1561,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
           }
 #pragma unroll
           for (int b = 0; b < NB; ++b) {
-            const uint2 h = lds8(xc + (uint32_t)(b * PPV + w) * ps32);
+            const uint2 h = ld8(xc + (uint32_t)(b * PPV + w) * ps32);
             unsigned short xh[4];
             split_halves(h.x, xh[0], xh[1]);
             split_halves(h.y, xh[2], xh[3]);
@@ -1568,14 +1586,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
           for (int p = 0; p < NP; ++p) {
             float2 X[4];
             if constexpr (XE == 4) {
-              const uint4 u0 = lds16(xc + (uint32_t)(p * PPV + 2 * w) * ps32);
-              const uint4 u1 = lds16(xc + (uint32_t)(p * PPV + 2 * w + 1) * ps32);
+              const uint4 u0 = ld16(xc + (uint32_t)(p * PPV + 2 * w) * ps32);
+              const uint4 u1 = ld16(xc + (uint32_t)(p * PPV + 2 * w + 1) * ps32);
               X[0] = make_float2(__uint_as_float(u0.x), __uint_as_float(u0.y));
               X[1] = make_float2(__uint_as_float(u0.z), __uint_as_float(u0.w));
               X[2] = make_float2(__uint_as_float(u1.x), __uint_as_float(u1.y));
               X[3] = make_float2(__uint_as_float(u1.z), __uint_as_float(u1.w));
             } else {
-              const uint4 u = lds16(xc + (uint32_t)(p * PPV + w) * ps32);
+              const uint4 u = ld16(xc + (uint32_t)(p * PPV + w) * ps32);
               X[0] = widen2(u.x, typename Op::TX());
               X[1] = widen2(u.y, typename Op::TX());
               X[2] = widen2(u.z, typename Op::TX());
@@ -1596,11 +1614,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_batch_ring(const Args a, float *
             const uint32_t xa = xc + (uint32_t)(b * PPV + w) * ps32;
             float2 x01, x23;
             if constexpr (XE == 4) {
-              const uint4 u = lds16(xa);
+              const uint4 u = ld16(xa);
               x01 = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
               x23 = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
             } else {
-              const uint2 h = lds8(xa);
+              const uint2 h = ld8(xa);
               float f[4];
               widen4(h.x, h.y, f, typename Op::TX());
               x01 = make_float2(f[0], f[1]);
