@@ -20,8 +20,9 @@
 //               warp (4 with 16 vectors of 16-bit rows), the next loads in registers;
 //               mixed-precision FMAs for 16-bit rows, packed FMAs for int8/fp32 rows
 //               with up to 8 vectors.
-//   k_batch_ring  2 <= B <= 16: A through a per-thread cp.async ring, x in shared
-//               memory (fp32 where it fits), R rows per warp, packed FMAs.
+//   k_batch_ring  2 <= B <= 16, and int8/int4 with B = 1: A through a per-thread
+//               cp.async ring, x in shared memory (fp32 where it fits), R rows per
+//               warp, packed FMAs (mixed-precision FMAs for some 16-bit forms).
 //   k_xsplit    B <= 4: the CTA splits K, x in fp32 registers.
 //   k_tc        fp16/bf16, 17..256 vectors: tcgen05 tensor cores (gemv_tc.cuh; with
 //               many row tiles the persistent k_tc_persist).
@@ -37,7 +38,7 @@
 
 namespace gemv {
 
-constexpr int kThreads = 256;  // every kernel runs 8 warps per CTA
+constexpr int kThreads = 256;  // 8 warps: the row-team, block-per-row and second-pass CTAs
 constexpr int kWarps = kThreads / 32;
 
 struct Args {
