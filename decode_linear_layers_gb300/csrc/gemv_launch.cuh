@@ -133,10 +133,10 @@ cudaError_t launch_batched(const gemv_plan_t &p, const Args &a, float *ws, cudaS
         }
         return cudaErrorInvalidValue;
       case GEMV_BATCHED_RING: {
-        constexpr int R = ring_rows(NB, Op::GROUPED, sizeof(typename Op::TA) == 4), G = 8 / R;
+        constexpr int R = ring_rows(NB, Op::GROUPED, sizeof(typename Op::TA) == 4), G = ring_slots(NB) / R;
         constexpr int MODE = NB >= 8 ? kRingPairs : kRingEvenOdd;
         const bool x32 = p.x_staging == GEMV_X_SMEM_FP32 || SX == 4;
-        if (!sw && p.rows_per_warp != R) return cudaErrorInvalidValue;
+        if (!sw && (p.rows_per_warp != R || p.unroll != G)) return cudaErrorInvalidValue;
         if (sw)
           return x32 ? ring(k_batch_ring<Op, NB, 2, 4, 4, true, MODE>) : ring(k_batch_ring<Op, NB, 2, 4, SX, true, MODE>);
         return x32 ? ring(k_batch_ring<Op, NB, R, G, 4, false, MODE>) : ring(k_batch_ring<Op, NB, R, G, SX, false, MODE>);

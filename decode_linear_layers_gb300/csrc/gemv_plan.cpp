@@ -85,7 +85,7 @@ static bool rowpair_fits(int nb, int64_t K, int sx) { return (int64_t)nb * K * s
 // x staging of the BATCHED ring kernel: fp32 where x and the ring fit, else as
 // stored; -1 if x does not fit.
 static int ring_staging(int nb, int64_t K, int sx, int64_t extra) {
-  const int64_t room = kRingSmemMax - kRingBytes - extra;
+  const int64_t room = kRingSmemMax - ring_bytes(nb) - extra;
   if (sx != 4 && (int64_t)nb * K * 4 <= room) return GEMV_X_SMEM_FP32;
   if ((int64_t)nb * K * sx <= room) return GEMV_X_SMEM;
   return -1;
@@ -127,7 +127,7 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
   // the ring kernel over rslices K slices (x staged per slice), the row-pair kernel
   // over all of K (int4: the ring also carries each slot's group scale; the row-pair
   // kernel is not built for grouped scales)
-  const int64_t rextra = dtype == GEMV_DTYPE_W4 ? kRingScaleBytes : 0;
+  const int64_t rextra = dtype == GEMV_DTYPE_W4 ? ring_scale_bytes(p.nb) : 0;
   const int rslices = nch == 0 ? 0 : ring_slices(p.nb, nch, vec, sx, rextra);
   const int64_t rcps = rslices > 0 ? ceil_div(nch, rslices) : 0;  // chunks per slice
   const int rstage = rslices > 0 ? ring_staging(p.nb, rcps * vec, sx, rextra) : -1;
@@ -365,14 +365,14 @@ gemv_status_t plan(int dtype, int64_t M, int64_t K, int B, bool aligned16, int n
         p.unroll = p.rows_per_warp == 4 ? 1 : 2;
         p.smem_bytes = (int)((int64_t)p.nb * K * sx);
       } else {
-        // ring: R rows per warp, a G = 8 / R step ring; the mixed form reads x as
+        // ring: R rows per warp, a G = slots / R step ring; the mixed form reads x as
         // stored.  Over rslices K slices (x too large to stage whole): grid.x CTAs per
         // slice, one CTA per SM in all, partial sums [slice][b][m], then a second pass.
         const int xs = v == GEMV_BATCHED_RING_MIXED ? GEMV_X_SMEM : rstage;
         p.rows_per_warp = v == GEMV_BATCHED_RING_MIXED ? 2 : ring_rows(p.nb, dtype == GEMV_DTYPE_W4, dtype == GEMV_DTYPE_F32);
         p.x_staging = xs;
-        p.unroll = 8 / p.rows_per_warp;
-        p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + kRingBytes + rextra);
+        p.unroll = ring_slots(p.nb) / p.rows_per_warp;
+        p.smem_bytes = (int)((int64_t)p.nb * rcps * vec * (xs == GEMV_X_SMEM_FP32 ? 4 : sx) + ring_bytes(p.nb) + rextra);
         p.splits = rslices;
         p.grid = num_sms / rslices > 0 ? num_sms / rslices : 1;
         p.workspace_bytes = rslices > 1 ? (int64_t)rslices * B * M * 4 : 0;

@@ -23,8 +23,8 @@ constexpr int kBatchedThreads = 512;
 // 96.0 -> 82.7, 14336x4096 51.2 -> 46.7, f16 4096x4096 21.5 -> 20.5).  Otherwise 2
 // (two chunks per lane in flight per row).
 constexpr int rowpair_rows(int nb, bool mixed16) { return (nb == 16 && mixed16) ? 4 : 2; }
-// BATCHED ring kernel: R rows per warp and a per-thread cp.async ring of G = 8 / R
-// steps: 16 warps x 8 slots x 512 bytes after x.  R = 2 for 16 vectors (the
+// BATCHED ring kernel: R rows per warp and a per-thread cp.async ring of G = slots / R
+// steps: 16 warps x slots x 512 bytes after x (ring_slots below).  R = 2 for 16 vectors (the
 // accumulators' registers), for int4 with 3 or more vectors (32 weights per chunk to
 // decode) and for fp32 with 4 vectors, else 4 (measured on GB300, event means in us:
 // int4 8192x8192 B = 1 18.8 with R = 4 against 19.6 with R = 2, int4 14336x4096
@@ -32,8 +32,14 @@ constexpr int rowpair_rows(int nb, bool mixed16) { return (nb == 16 && mixed16) 
 // 28.6; bf16 14336x4096 B = 4 29.3 against 27.1 and int8 8192x8192 B = 4 32.8
 // against 32.5 keep R = 4).  SwiGLU: R = 2.
 constexpr int64_t kRingSmemMax = 227 * 1024;  // dynamic shared memory one CTA may use
-constexpr int64_t kRingBytes = 16 * 8 * 512;
-constexpr int64_t kRingScaleBytes = 16 * 8 * 32 * 4;  // int4: a group scale per slot
+// Ring slots per thread (G x R): 8 (64 KB per CTA), and 16 (128 KB) for one vector,
+// whose steps are short and whose warps wait on HBM (ncu: long_scoreboard the top
+// stall).  Event means (us, A/B in one run, 8 -> 16 slots): int8 16384x8192 B = 1
+// 28.3 -> 26.9, 32768x8192 47.8 -> 46.9, 14336x4096 16.6 -> 16.5, 8192x8192 18.4
+// either way; int4 within 1.3 %.
+constexpr int ring_slots(int nb) { return nb == 1 ? 16 : 8; }
+constexpr int64_t ring_bytes(int nb) { return (int64_t)16 * ring_slots(nb) * 512; }
+constexpr int64_t ring_scale_bytes(int nb) { return (int64_t)16 * ring_slots(nb) * 32 * 4; }  // int4: a group scale per slot
 constexpr int ring_rows(int nb, bool grouped, bool a32) {
   return nb == 16 ? 2 : grouped ? (nb <= 2 ? 4 : 2) : (a32 && nb == 4) ? 2 : 4;
 }

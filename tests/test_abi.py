@@ -174,9 +174,10 @@ def test_plan_config_shapes():
     assert g.plan_for("f32", 2048, 8192, 2)["kernel"] == K["xsplit"]
     # one vector of int8 with fewer than 48 rows per SM: the streaming kernel
     assert g.plan_for("w8", 4096, 16384, 1)["kernel"] == K["stream"]
-    p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp
+    p = g.plan_for("w8", 8192, 8192, 1)     # one vector of int8: the ring, 4 rows per warp, 4 steps
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["nb"] == 1
-    assert p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["smem_bytes"] == 8192 * 4 + 64 * 1024
+    assert p["x_staging"] == 2 and p["rows_per_warp"] == 4 and p["unroll"] == 4
+    assert p["smem_bytes"] == 8192 * 4 + 128 * 1024  # one vector: a 16-slot (128 KB) ring
     p = g.plan_for("w8", 8192, 8192, 4)     # at most one ring row group per warp: the row pairs
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_ROWPAIR and p["x_staging"] == 1
     assert p["rows_per_warp"] == 2 and p["smem_bytes"] == 4 * 8192 * 2
@@ -272,9 +273,10 @@ def test_plan_batched_staging():
     assert p["kernel"] == K["batched"] and p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 2
     assert p["x_staging"] == 2 and p["smem_bytes"] == 4 * 8192 * 4 + ring + 16 * 1024
     # one or two vectors of int4 (and fp32 with 4 vectors, 2 rows): rows per warp as measured
+    # (one vector: 16 ring slots per thread, so 4 steps)
     for B in (1, 2):
         p = g.plan_for("w4", 14336, 4096, B)
-        assert p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 4 and p["unroll"] == 2
+        assert p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 4 and p["unroll"] == (4 if B == 1 else 2)
     p = g.plan_for("f32", 8192, 4096, 4)
     assert p["variant"] == g.BATCHED_RING and p["rows_per_warp"] == 2 and p["unroll"] == 4
 
@@ -354,8 +356,8 @@ def test_w4_host_checks():
 
 def test_plan_w4():
     K = g.KERNELS
-    p = g.plan_for("w4", 8192, 8192, 1)   # one vector: the ring (x fp32, group-scale ring)
-    assert p["kernel"] == K["batched"] and p["nb"] == 1 and p["smem_bytes"] == 8192 * 4 + 64 * 1024 + 16 * 1024
+    p = g.plan_for("w4", 8192, 8192, 1)   # one vector: the ring (x fp32, 16 slots, group-scale ring)
+    assert p["kernel"] == K["batched"] and p["nb"] == 1 and p["smem_bytes"] == 8192 * 4 + 128 * 1024 + 32 * 1024
     p = g.plan_for("w4", 65536, 8192, 1)  # 65536 rows and more: not the ring
     assert p["kernel"] == K["warp_per_row"]
     for B, slices in ((2, 1), (4, 1), (9, 2), (16, 2)):  # the batched ring kernel

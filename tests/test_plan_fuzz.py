@@ -74,13 +74,14 @@ def test_plan_invariants(dtype, M, kmul, kpad, B, aligned, sms):
         else:
             if v == g.BATCHED_RING_MIXED:
                 assert half16 and p["rows_per_warp"] == 2 and p["x_staging"] == 1
-            assert p["rows_per_warp"] * p["unroll"] == 8
+            slots = 16 if p["nb"] == 1 else 8  # ring slots per thread
+            assert p["rows_per_warp"] * p["unroll"] == slots
             assert p["rows_per_warp"] * p["nb"] <= 32
             cps = _cdiv(nch, p["splits"])
             assert (p["splits"] - 1) * cps < nch
             xe = 4 if p["x_staging"] == 2 or dtype == "f32" else 2
-            extra = 16 * 1024 if dtype == "w4" else 0
-            assert p["smem_bytes"] == p["nb"] * cps * vec * xe + 64 * 1024 + extra
+            extra = slots * 2 * 1024 if dtype == "w4" else 0  # a 4-byte group scale per slot
+            assert p["smem_bytes"] == p["nb"] * cps * vec * xe + slots * 8 * 1024 + extra
             assert p["workspace_bytes"] == (p["splits"] * B * M * 4 if p["splits"] > 1 else 0)
     elif kern == K_["tc"]:
         assert half16 and aligned and K % vec == 0
