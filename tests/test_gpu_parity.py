@@ -152,6 +152,29 @@ def test_rowpair_four_rows(dtype):
                                    what=f"{dtype} {kernel} M={M} K={K} B={B} bias={bias}")
 
 
+@pytest.mark.parametrize("dtype,M,K,xs", [("w8", 7300, 8192, 2), ("w8", 7300, 32768, 1),
+                                          ("w4", 2500, 8192, 2), ("w4", 2500, 32768, 1)])
+def test_one_vector_ring(dtype, M, K, xs):
+    # one vector of int8/int4 rows in the ring kernel (4 steps of 4 rows in flight per
+    # warp), x staged as fp32 (xs = 2) or, for long rows, as stored (xs = 1); a ragged
+    # last row group; sampled rows against the oracle, repeats bitwise equal
+    w = W.small(dtype, M, K, 1, True, seed=M + K)
+    inp = W.make_inputs(w)
+    d = U.to_device(inp)
+    y1 = U.run_gpu(dtype, d, M, K, 1)
+    plan = g.last_plan()
+    assert plan["kernel_name"] == "batched" and plan["variant"] == g.BATCHED_RING, plan
+    assert plan["nb"] == 1 and plan["rows_per_warp"] == 4 and plan["unroll"] == 4 and plan["x_staging"] == xs, plan
+    y2 = U.run_gpu(dtype, d, M, K, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "results differ between two identical calls"
+    rows = np.unique(np.append(np.random.default_rng(2).choice(M, size=150, replace=False), [M - 1]))
+    sub = {k: (None if inp[k] is None else inp[k][rows]) for k in ("A", "bias", "scale")}
+    sub["x"] = inp["x"]
+    y_ref, absdot = U.oracle_for(dtype, sub)
+    U.assert_close(dtype, y1[:, rows], y_ref, absdot, with_rounding=True, what=f"{dtype} {M}x{K} B=1 xs={xs}")
+
+
 @pytest.mark.parametrize("dtype,M,K,B", [("bf16", 4096, 14336, 16), ("w8", 8192, 8192, 16),
                                          ("f16", 3000, 14336, 9), ("bf16", 2500, 30000, 5),
                                          ("f32", 1000, 20000, 12), ("bf16", 1024, 16384, 8)])
