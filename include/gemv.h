@@ -285,7 +285,9 @@ typedef struct gemv_plan {
   int rows_per_warp;       /* BATCHED: rows one warp carries at once; TC: 64-column
                               swizzle atoms of K per pipeline stage */
   int splits;              /* SPLIT_K: number of K slices (1 otherwise) */
-  int unroll;              /* 16-byte chunks of A in flight per lane per step; TC:
+  int unroll;              /* 16-byte chunks of A in flight per lane per step; the
+                              BATCHED ring: steps in flight (ring slots per thread /
+                              rows_per_warp: 16 slots for one vector, else 8); TC:
                               k-tiles per K slice (per tile in the persistent form) */
   int x_staging;           /* GEMV_X_GLOBAL / GEMV_X_SMEM / GEMV_X_SMEM_FP32 */
   int nb;                  /* vector count the kernel is built for (>= B, power of 2) */
